@@ -1,0 +1,238 @@
+"""ctypes binding of libcpring.so: argument marshalling only.
+
+Every computation runs in the library's CUDA kernels; torch supplies device
+memory and streams.  If the library is missing the calls raise instead of
+falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libcpring.so")
+
+CP_OK = 0
+STATUS_NAMES = {
+    0: "CP_OK", -1: "CP_ERR_NULL", -2: "CP_ERR_SHAPE", -3: "CP_ERR_UNSUPPORTED",
+    -4: "CP_ERR_ALIGN", -5: "CP_ERR_CUDA", -6: "CP_ERR_BUFFER", -7: "CP_ERR_DOC_OFFSETS",
+    -8: "CP_ERR_TIMEOUT", -9: "CP_ERR_DEVICE",
+}
+STATUS_CODES = {v: k for k, v in STATUS_NAMES.items()}
+
+_lib = None
+_lock = threading.Lock()
+
+_vp, _i, _i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+_SIGS = {
+    "cp_ring_attn_fwd": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp],
+    "cp_ring_attn_fwd_f32": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp],
+    "cp_ring_step": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _vp, _vp],
+    "cp_ring_step_f32": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _vp, _vp],
+    "cp_lse_merge": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp],
+    "cp_lse_finalize": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp],
+    "cp_ring_schedule": [_i, _i, _i, _i, _i, _vp, _vp, _i64, ctypes.POINTER(_i64)],
+    "cp_ring_traffic": [_i64, _i64, _i64, _i64, _i, _i, _i, ctypes.POINTER(_i64)],
+    "cp_get_last_status": [_vp],
+    "cp_status_string": [_i],
+    "cp_launch_counts": [ctypes.POINTER(_i64)],
+}
+
+
+class CpError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        self.name = STATUS_NAMES.get(status, str(status))
+        super().__init__(f"{fn} failed: {self.name} ({status})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (loaded once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'`")
+            handle = ctypes.CDLL(LIB_PATH)
+            for name, argtypes in _SIGS.items():
+                fn = getattr(handle, name)
+                fn.argtypes = argtypes
+                if name == "cp_status_string":
+                    fn.restype = ctypes.c_char_p
+                elif name == "cp_launch_counts":
+                    fn.restype = None
+                else:
+                    fn.restype = _i
+            _lib = handle
+    return _lib
+
+
+def _check(fn: str, st: int) -> None:
+    if st != CP_OK:
+        raise CpError(fn, st)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape=None) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def doc_offsets_tensor(doc_offsets, device) -> Optional[torch.Tensor]:
+    """doc_offsets (list, numpy array or tensor) as a device int32 tensor."""
+    if doc_offsets is None:
+        return None
+    if isinstance(doc_offsets, torch.Tensor):
+        t = doc_offsets.to(device=device, dtype=torch.int32)
+    else:
+        t = torch.tensor([int(x) for x in doc_offsets], dtype=torch.int32, device=device)
+    return t.contiguous()
+
+
+# --------------------------------------------------------------------- C ABI
+def cp_ring_attn_fwd(q, k, v, out, lse, n_shards: int, causal: bool = True,
+                     doc_offsets: Optional[torch.Tensor] = None, stream=None) -> None:
+    """bf16 fused forward; q, k, v, out [B,S,H,d] bf16, lse [B,H,S] fp32."""
+    B, S, H, d = q.shape
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _need(t, n, torch.bfloat16, (B, S, H, d))
+    _need(lse, "lse", torch.float32, (B, H, S))
+    if doc_offsets is not None:
+        _need(doc_offsets, "doc_offsets", torch.int32)
+    _check("cp_ring_attn_fwd", lib().cp_ring_attn_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, H, d, int(n_shards),
+        int(bool(causal)), _ptr(doc_offsets), _stream(stream)))
+
+
+def cp_ring_attn_fwd_f32(q, k, v, out, lse, n_shards: int, causal: bool = True,
+                         doc_offsets: Optional[torch.Tensor] = None, stream=None) -> None:
+    """fp32 fused forward; q, k, v, out [B,S,H,d] fp32, lse [B,H,S] fp32."""
+    B, S, H, d = q.shape
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _need(t, n, torch.float32, (B, S, H, d))
+    _need(lse, "lse", torch.float32, (B, H, S))
+    if doc_offsets is not None:
+        _need(doc_offsets, "doc_offsets", torch.int32)
+    _check("cp_ring_attn_fwd_f32", lib().cp_ring_attn_fwd_f32(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, H, d, int(n_shards),
+        int(bool(causal)), _ptr(doc_offsets), _stream(stream)))
+
+
+def cp_ring_step(q, k, v, o_part, m_part, l_part, n_shards: int, i: int, j: int,
+                 causal: bool = True, doc_offsets: Optional[torch.Tensor] = None,
+                 stream=None) -> None:
+    """One partial step (i, j).  bf16 or fp32 q/k/v (dispatched on dtype);
+    o_part [B,S/N,H,d] fp32, m_part and l_part [B,H,S/N] fp32."""
+    B, S, H, d = q.shape
+    L = S // int(n_shards) if n_shards else 0
+    dt = q.dtype
+    if dt not in (torch.bfloat16, torch.float32):
+        raise TypeError("q must be bf16 or fp32")
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, dt, (B, S, H, d))
+    _need(o_part, "o_part", torch.float32, (B, L, H, d))
+    _need(m_part, "m_part", torch.float32, (B, H, L))
+    _need(l_part, "l_part", torch.float32, (B, H, L))
+    if doc_offsets is not None:
+        _need(doc_offsets, "doc_offsets", torch.int32)
+    name = "cp_ring_step" if dt == torch.bfloat16 else "cp_ring_step_f32"
+    _check(name, getattr(lib(), name)(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o_part), _ptr(m_part), _ptr(l_part), B, S, H, d,
+        int(n_shards), int(i), int(j), int(bool(causal)), _ptr(doc_offsets), _stream(stream)))
+
+
+def cp_lse_merge(o_acc, m_acc, l_acc, o_part, m_part, l_part, stream=None) -> None:
+    """In-place online merge of (o_part, m_part, l_part) into (o_acc, m_acc, l_acc)."""
+    B, rows, H, d = o_acc.shape
+    _need(o_acc, "o_acc", torch.float32)
+    _need(o_part, "o_part", torch.float32, (B, rows, H, d))
+    for t, n in ((m_acc, "m_acc"), (l_acc, "l_acc"), (m_part, "m_part"), (l_part, "l_part")):
+        _need(t, n, torch.float32, (B, H, rows))
+    _check("cp_lse_merge", lib().cp_lse_merge(
+        _ptr(o_acc), _ptr(m_acc), _ptr(l_acc), _ptr(o_part), _ptr(m_part), _ptr(l_part),
+        B, rows, H, d, _stream(stream)))
+
+
+def cp_lse_finalize(o_acc, m_acc, l_acc, out, lse, stream=None) -> None:
+    """out = o_acc / l_acc (bf16 or fp32 by out's dtype), lse = m + log(l)."""
+    B, rows, H, d = o_acc.shape
+    _need(o_acc, "o_acc", torch.float32)
+    for t, n in ((m_acc, "m_acc"), (l_acc, "l_acc"), (lse, "lse")):
+        _need(t, n, torch.float32, (B, H, rows))
+    if out.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("out must be bf16 or fp32")
+    _need(out, "out", out.dtype, (B, rows, H, d))
+    _check("cp_lse_finalize", lib().cp_lse_finalize(
+        _ptr(o_acc), _ptr(m_acc), _ptr(l_acc), _ptr(out), _ptr(lse), B, rows, H, d,
+        int(out.dtype == torch.bfloat16), _stream(stream)))
+
+
+def cp_ring_schedule(S: int, n_shards: int, tile_q: int, tile_k: int, causal: bool = True,
+                     doc_offsets: Optional[Sequence[int]] = None):
+    """Host-side skip schedule: list of (q tile, kv tile) pairs."""
+    L = lib()
+    n = ctypes.c_int64(0)
+    docs = None
+    if doc_offsets is not None:
+        arr = (ctypes.c_int32 * len(doc_offsets))(*[int(x) for x in doc_offsets])
+        docs = ctypes.cast(arr, ctypes.c_void_p)
+    _check("cp_ring_schedule", L.cp_ring_schedule(S, n_shards, tile_q, tile_k, int(bool(causal)),
+                                                  docs, None, 0, ctypes.byref(n)))
+    cnt = n.value
+    buf = (ctypes.c_int32 * max(1, 2 * cnt))()
+    _check("cp_ring_schedule", L.cp_ring_schedule(S, n_shards, tile_q, tile_k, int(bool(causal)),
+                                                  docs, ctypes.cast(buf, ctypes.c_void_p), cnt,
+                                                  ctypes.byref(n)))
+    return [(buf[2 * x], buf[2 * x + 1]) for x in range(cnt)]
+
+
+def cp_ring_traffic(B: int, S: int, H: int, d: int, dtype_bytes: int, n_shards: int,
+                    causal: bool = False):
+    """Per-rank send + receive bytes of the virtual ring."""
+    out = (ctypes.c_int64 * n_shards)()
+    _check("cp_ring_traffic", lib().cp_ring_traffic(B, S, H, d, dtype_bytes, n_shards,
+                                                    int(bool(causal)), out))
+    return list(out)
+
+
+def cp_get_last_status(stream=None) -> int:
+    """Synchronise the stream, read and clear the device error word."""
+    return int(lib().cp_get_last_status(_stream(stream)))
+
+
+def cp_status_string(status: int) -> str:
+    return lib().cp_status_string(int(status)).decode()
+
+
+def launch_counts():
+    """(tcgen05 attention, fp32 attention, merge/finalize, doc scan) launches so far."""
+    buf = (ctypes.c_int64 * 4)()
+    lib().cp_launch_counts(buf)
+    return tuple(buf)

@@ -1,0 +1,736 @@
+// Ring-attention forward for bf16 inputs on sm_103a tensor cores (tcgen05).
+//
+// What is computed ("上下文並行（Context Parallelism, CP）", compassingai.com,
+// section 線上 Softmax, algorithm "Ring Attention + FlashAttention 分塊計算"):
+// every virtual rank i holds the query shard Q_i and visits the K/V shards j
+// in ascending ring order; for each visited block it forms
+// S = Q K^T / sqrt(d) with the causal / document mask, the row max, P =
+// exp(S - m), the row sum and P V, and folds them into a running (O, m, l)
+// with the online-softmax merge; at the end O / l and the log-sum-exp are
+// written.  Shard pairs and tiles with no visible (q, k) are never loaded or
+// computed (section 因果掩碼的特殊處理).  The inner tile loop that the page
+// leaves out is this kernel's main loop.
+//
+// GB300 mapping.  One persistent CTA per SM (320 threads):
+//   warps 0-3  softmax + merge + epilogue for query tile 0 (128 rows)
+//   warps 4-7  the same for query tile 1 (the next 128 rows)
+//   warp  8    TMA producer: Q tiles once per work item, then K/V tiles of
+//              each visited shard into a 2-stage shared-memory ring
+//              (the ring's send/receive becomes this double-buffered walk)
+//   warp  9    a single thread issues every tcgen05.mma
+// TMEM (512 columns): S_0 | S_1 | O_0 | O_1.  S_t = Q_t K^T lands in TMEM
+// (fp32); the softmax warps read it with tcgen05.ld, write P (bf16 pairs)
+// back over S_t, and the MMA thread issues O_t += P V with P taken from TMEM.
+// While one warpgroup does its exponentials the tensor cores work on the
+// other tile, so the two tiles ping-pong.
+//
+// Running state.  m is kept in base-2 units (scores pre-multiplied by
+// log2(e)/sqrt(d)).  The reference point used for the exponentials moves
+// only when the row max grows by more than 2^8 (so most tiles need no
+// rescale of O); the exact row max is tracked separately and the result is
+// converted to the pages' (O, m, l) with m the true row max at the end.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdio>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace cpring {
+namespace {
+
+constexpr int kBM = 128;        // query rows per tile = TMEM lanes
+constexpr int kBN = 128;        // key rows per K/V tile
+constexpr int kQTiles = 2;      // query tiles per work item
+constexpr int kStages = 2;      // K/V ring depth
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kTmemCols = 512;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr unsigned long long kTimeoutNs = 4000000000ull;  // per wait
+
+template <int D>
+struct Layout {
+  static constexpr int kTileBytes = kBM * D * 2;    // 128 rows x D bf16
+  static constexpr int kPanelBytes = kBM * 64 * 2;  // 128 rows x 64 cols (one swizzle panel)
+  static constexpr int kPanels = D / 64;
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + kQTiles * kTileBytes;
+  static constexpr int kVOff = kKOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr int kBytes = kBarOff + 256;
+  static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024 B
+};
+
+// mbarrier slots (8 bytes each) after the tiles
+enum Bar : int {
+  kQFull = 0,
+  kQEmpty = 1,
+  kKFull = 2,     // + stage
+  kVFull = 4,     // + stage
+  kKEmpty = 6,    // + stage: K tile consumed by both S MMAs
+  kVEmpty = 8,    // + stage: V tile consumed by both PV MMAs
+  kSFull = 10,    // + tile
+  kPReady = 12,   // + tile
+  kOBar = 14,     // + tile
+  kDrain = 16,
+  kNumBars = 17
+};
+constexpr int kTmemSlot = kNumBars * 8;       // u32: TMEM base address
+constexpr int kAbortSlot = kNumBars * 8 + 4;  // u32: CTA abort flag
+
+struct KParams {
+  int B, S, H, L, n_shards;
+  int q_shard, k_shard;  // -1 = all shards
+  int causal;
+  const int32_t* doc_offsets;
+  const int32_t* doc_info;
+  int n_qshards;
+  int pairs_per_shard;   // ceil(L / 256)
+  int tiles_per_shard;   // ceil(L / 128)
+  int n_items;
+  float scale_log2;      // log2(e) / sqrt(d)
+  __nv_bfloat16* out;
+  float* lse;
+  float* o_part;
+  float* m_part;
+  float* l_part;
+  int* err;
+  unsigned long long timeout_ns;
+};
+
+struct Item {
+  int b, h, i;
+  int q0[kQTiles];
+  int rows[kQTiles];
+  int f_lo[kQTiles], f_hi[kQTiles];  // flattened K/V tile range (empty if lo > hi)
+  int F_lo, F_hi;
+  int klo, khi;                      // key range this launch may use
+};
+
+// Document [start, end) containing token r.
+__device__ __forceinline__ int2 doc_span(const KParams& p, int n_docs, int r) {
+  if (p.doc_offsets == nullptr) return make_int2(0, p.S);
+  int lo = 0, hi = n_docs;
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (__ldg(p.doc_offsets + mid) <= r) lo = mid; else hi = mid;
+  }
+  return make_int2(__ldg(p.doc_offsets + lo), __ldg(p.doc_offsets + lo + 1));
+}
+
+__device__ __forceinline__ int flat_tile(const KParams& p, int key) {
+  int j = key / p.L;
+  return j * p.tiles_per_shard + (key - j * p.L) / kBN;
+}
+
+__device__ __forceinline__ void tile_keys(const KParams& p, int f, int& ks, int& ke) {
+  int j = f / p.tiles_per_shard;
+  int kt = f - j * p.tiles_per_shard;
+  ks = j * p.L + kt * kBN;
+  ke = min(ks + kBN, (j + 1) * p.L);
+}
+
+// Work item w (heaviest first): (b, h, query shard, pair of 128-row tiles).
+// A tile's visible keys are [max(doc_start(q_first), klo), min(h(q_last), khi)]
+// with h(q) = q (causal) or doc_end(q) - 1: every key of that interval is
+// seen by at least one row of the tile, so the K/V tiles it touches are
+// exactly the tiles holding a visible (q, k).
+__device__ void decode_item(const KParams& p, int n_docs, int w, Item& it) {
+  const int BH = p.B * p.H;
+  const int slots = p.n_qshards * p.pairs_per_shard;
+  const int g = slots - 1 - w / BH;
+  const int bh = w % BH;
+  it.b = bh / p.H;
+  it.h = bh - it.b * p.H;
+  const int ii = g / p.pairs_per_shard;
+  const int pp = g - ii * p.pairs_per_shard;
+  it.i = (p.q_shard < 0) ? ii : p.q_shard;
+  it.klo = (p.k_shard < 0) ? 0 : p.k_shard * p.L;
+  it.khi = (p.k_shard < 0) ? p.S - 1 : (p.k_shard + 1) * p.L - 1;
+  const int shard_end = (it.i + 1) * p.L;
+  it.F_lo = INT_MAX;
+  it.F_hi = -1;
+#pragma unroll
+  for (int t = 0; t < kQTiles; ++t) {
+    const int q0 = it.i * p.L + pp * (kBM * kQTiles) + t * kBM;
+    const int rows = max(0, min(kBM, shard_end - q0));
+    it.q0[t] = q0;
+    it.rows[t] = rows;
+    it.f_lo[t] = 1;
+    it.f_hi[t] = 0;
+    if (rows > 0) {
+      const int qa = q0, qb = q0 + rows - 1;
+      const int2 da = doc_span(p, n_docs, qa);
+      const int lo = max(da.x, it.klo);
+      int hi;
+      if (p.causal) {
+        hi = qb;
+      } else {
+        hi = doc_span(p, n_docs, qb).y - 1;
+      }
+      hi = min(hi, it.khi);
+      if (lo <= hi) {
+        it.f_lo[t] = flat_tile(p, lo);
+        it.f_hi[t] = flat_tile(p, hi);
+        it.F_lo = min(it.F_lo, it.f_lo[t]);
+        it.F_hi = max(it.F_hi, it.f_hi[t]);
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ int item_of(int k, int c, int G) {
+  return k * G + ((k & 1) ? (G - 1 - c) : c);
+}
+
+// ---------------------------------------------------------------- waits
+// Single-thread bounded wait.  Returns false on abort or timeout.
+__device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                      const KParams& p, bool honour_abort = true) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (honour_abort && *abort_flag) return false;
+    if ((it & 255u) == 0) {
+      const uint64_t now = ptx::globaltimer();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > p.timeout_ns) {
+        *abort_flag = 1u;
+        atomicOr(p.err, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// Warp-uniform bounded wait (every lane calls it; all lanes get one answer).
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity,
+                                          volatile uint32_t* abort_flag, const KParams& p) {
+  uint64_t t0 = 0;
+  const int lane = threadIdx.x & 31;
+  for (uint32_t it = 1;; ++it) {
+    const bool ok = ptx::mbar_try_wait(bar, parity);
+    if (__any_sync(0xffffffffu, ok)) return true;
+    if (__any_sync(0xffffffffu, *abort_flag != 0u)) return false;
+    if ((it & 255u) == 0) {
+      int tout = 0;
+      if (lane == 0) {
+        const uint64_t now = ptx::globaltimer();
+        if (t0 == 0) {
+          t0 = now;
+        } else if (now - t0 > p.timeout_ns) {
+          *abort_flag = 1u;
+          atomicOr(p.err, kErrTimeout);
+          tout = 1;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, tout, 0)) return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- kernel
+template <int D, bool kPartial>
+__global__ void __launch_bounds__(kThreads, 1)
+    ring_attn_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                          const __grid_constant__ CUtensorMap tmap_k,
+                          const __grid_constant__ CUtensorMap tmap_v, const KParams p) {
+  using Lay = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_u32(smem);
+  const uint32_t bars = sbase + Lay::kBarOff;
+  auto bar = [&](int idx) -> uint32_t { return bars + 8u * static_cast<uint32_t>(idx); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kBarOff + kTmemSlot);
+  volatile uint32_t* abort_flag =
+      reinterpret_cast<volatile uint32_t*>(smem + Lay::kBarOff + kAbortSlot);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  int n_docs = 1;
+  if (p.doc_offsets != nullptr) {
+    n_docs = __ldg(p.doc_info);
+    if (n_docs <= 0) return;  // malformed doc_offsets: the scan already flagged it
+  }
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar(kQFull), 1);
+    ptx::mbar_init(bar(kQEmpty), 1);
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(bar(kKFull + s), 1);
+      ptx::mbar_init(bar(kVFull + s), 1);
+      ptx::mbar_init(bar(kKEmpty + s), 1);
+      ptx::mbar_init(bar(kVEmpty + s), 1);
+    }
+    for (int t = 0; t < kQTiles; ++t) {
+      ptx::mbar_init(bar(kSFull + t), 1);
+      ptx::mbar_init(bar(kPReady + t), 128);
+      ptx::mbar_init(bar(kOBar + t), 1);
+    }
+    ptx::mbar_init(bar(kDrain), 1);
+    *abort_flag = 0u;
+    ptx::fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int G = gridDim.x;
+  const int c = blockIdx.x;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      ptx::tma_prefetch_desc(&tmap_q);
+      ptx::tma_prefetch_desc(&tmap_k);
+      ptx::tma_prefetch_desc(&tmap_v);
+      uint32_t kv_iter = 0, q_iter = 0, k_loads = 0, v_loads = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int w = item_of(k, c, G);
+        if (w >= p.n_items) break;
+        Item it;
+        decode_item(p, n_docs, w, it);
+        if (it.F_lo > it.F_hi) continue;
+        if (!wait1(bar(kQEmpty), (q_iter & 1u) ^ 1u, abort_flag, p)) { ok = false; break; }
+        ptx::mbar_arrive_expect_tx(bar(kQFull), kQTiles * Lay::kTileBytes);
+        for (int t = 0; t < kQTiles; ++t)
+          for (int pn = 0; pn < Lay::kPanels; ++pn)
+            ptx::tma_load_4d(sbase + Lay::kQOff + t * Lay::kTileBytes + pn * Lay::kPanelBytes,
+                             &tmap_q, bar(kQFull), pn * 64, it.h, it.q0[t], it.b);
+        ++q_iter;
+        for (int f = it.F_lo; f <= it.F_hi; ++f) {
+          const uint32_t st = kv_iter % kStages;
+          const uint32_t ph = (kv_iter / kStages) & 1u;
+          int ks, ke;
+          tile_keys(p, f, ks, ke);
+          if (!wait1(bar(kKEmpty + st), ph ^ 1u, abort_flag, p)) { ok = false; break; }
+          ptx::mbar_arrive_expect_tx(bar(kKFull + st), Lay::kTileBytes);
+          for (int pn = 0; pn < Lay::kPanels; ++pn)
+            ptx::tma_load_4d(sbase + Lay::kKOff + st * Lay::kTileBytes + pn * Lay::kPanelBytes,
+                             &tmap_k, bar(kKFull + st), pn * 64, it.h, ks, it.b);
+          ++k_loads;
+          if (!wait1(bar(kVEmpty + st), ph ^ 1u, abort_flag, p)) { ok = false; break; }
+          ptx::mbar_arrive_expect_tx(bar(kVFull + st), Lay::kTileBytes);
+          for (int pn = 0; pn < Lay::kPanels; ++pn)
+            ptx::tma_load_4d(sbase + Lay::kVOff + st * Lay::kTileBytes + pn * Lay::kPanelBytes,
+                             &tmap_v, bar(kVFull + st), pn * 64, it.h, ks, it.b);
+          ++v_loads;
+          ++kv_iter;
+        }
+      }
+      // Let every copy this thread started land before the CTA can exit.
+      if (q_iter > 0) wait1(bar(kQFull), (q_iter - 1) & 1u, abort_flag, p, false);
+      for (uint32_t s = 0; s < kStages; ++s) {
+        if (k_loads > s) {  // loads into stage s: (k_loads - 1 - s) / kStages + 1
+          const uint32_t uses = (k_loads - 1 - s) / kStages + 1;
+          wait1(bar(kKFull + s), (uses - 1) & 1u, abort_flag, p, false);
+        }
+        if (v_loads > s) {
+          const uint32_t uses = (v_loads - 1 - s) / kStages + 1;
+          wait1(bar(kVFull + s), (uses - 1) & 1u, abort_flag, p, false);
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(kBM, kBN, false);
+      constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kBM, D, true);
+      uint32_t kv_iter = 0, q_iter = 0;
+      uint32_t p_cnt[kQTiles] = {0u, 0u};
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int w = item_of(k, c, G);
+        if (w >= p.n_items) break;
+        Item it;
+        decode_item(p, n_docs, w, it);
+        if (it.F_lo > it.F_hi) continue;
+        if (!wait1(bar(kQFull), q_iter & 1u, abort_flag, p)) { ok = false; break; }
+        ++q_iter;
+        ptx::tc_fence_after();
+        int pend[kQTiles] = {-1, -1};
+        bool first_pv[kQTiles] = {true, true};
+        uint32_t prev_st = 0, prev_ph = 0;
+        bool have_prev = false, prev_v_ready = false;
+        for (int f = it.F_lo; f <= it.F_hi && ok; ++f) {
+          const uint32_t st = kv_iter % kStages;
+          const uint32_t ph = (kv_iter / kStages) & 1u;
+          if (!wait1(bar(kKFull + st), ph, abort_flag, p)) { ok = false; break; }
+          ptx::tc_fence_after();
+          for (int t = 0; t < kQTiles && ok; ++t) {
+            if (pend[t] >= 0) {
+              // O_t += P_t V(previous tile): P_t from TMEM, V (MN-major) from smem
+              if (!prev_v_ready) {
+                if (!wait1(bar(kVFull + prev_st), prev_ph, abort_flag, p)) { ok = false; break; }
+                prev_v_ready = true;
+              }
+              if (!wait1(bar(kPReady + t), p_cnt[t] & 1u, abort_flag, p)) { ok = false; break; }
+              ++p_cnt[t];
+              ptx::tc_fence_after();
+              const uint32_t vbase = sbase + Lay::kVOff + prev_st * Lay::kTileBytes;
+#pragma unroll
+              for (int s = 0; s < kBN / 16; ++s) {
+                const uint64_t bdesc =
+                    ptx::smem_desc_sw128(vbase + s * 16 * 128, Lay::kPanelBytes, 1024);
+                ptx::mma_ts(tmem_base + 256 + t * D, tmem_base + t * 128 + s * 8, bdesc,
+                            kIdescPV, (first_pv[t] && s == 0) ? 0u : 1u);
+              }
+              first_pv[t] = false;
+              ptx::mma_commit(bar(kOBar + t));
+              pend[t] = -1;
+            }
+            if (f >= it.f_lo[t] && f <= it.f_hi[t]) {
+              // S_t = Q_t K^T (both K-major, 128-byte swizzled panels of 64 columns)
+              const uint32_t qbase = sbase + Lay::kQOff + t * Lay::kTileBytes;
+              const uint32_t kbase = sbase + Lay::kKOff + st * Lay::kTileBytes;
+#pragma unroll
+              for (int s = 0; s < D / 16; ++s) {
+                const uint32_t off = (s >> 2) * Lay::kPanelBytes + (s & 3) * 32;
+                const uint64_t adesc = ptx::smem_desc_sw128(qbase + off, 16, 1024);
+                const uint64_t bdesc = ptx::smem_desc_sw128(kbase + off, 16, 1024);
+                ptx::mma_ss(tmem_base + t * 128, adesc, bdesc, kIdescQK, s > 0 ? 1u : 0u);
+              }
+              ptx::mma_commit(bar(kSFull + t));
+              pend[t] = f;
+            }
+          }
+          if (!ok) break;
+          ptx::mma_commit(bar(kKEmpty + st));                      // K(f) read by every S
+          if (have_prev) ptx::mma_commit(bar(kVEmpty + prev_st));  // V(f-1) read by every PV
+          prev_st = st;
+          prev_ph = ph;
+          have_prev = true;
+          prev_v_ready = false;
+          ++kv_iter;
+        }
+        if (!ok) break;
+        ptx::mma_commit(bar(kQEmpty));  // every S of this item has been issued
+        for (int t = 0; t < kQTiles && ok; ++t) {
+          if (pend[t] < 0) continue;
+          if (!prev_v_ready) {
+            if (!wait1(bar(kVFull + prev_st), prev_ph, abort_flag, p)) { ok = false; break; }
+            prev_v_ready = true;
+          }
+          if (!wait1(bar(kPReady + t), p_cnt[t] & 1u, abort_flag, p)) { ok = false; break; }
+          ++p_cnt[t];
+          ptx::tc_fence_after();
+          const uint32_t vbase = sbase + Lay::kVOff + prev_st * Lay::kTileBytes;
+#pragma unroll
+          for (int s = 0; s < kBN / 16; ++s) {
+            const uint64_t bdesc =
+                ptx::smem_desc_sw128(vbase + s * 16 * 128, Lay::kPanelBytes, 1024);
+            ptx::mma_ts(tmem_base + 256 + t * D, tmem_base + t * 128 + s * 8, bdesc, kIdescPV,
+                        (first_pv[t] && s == 0) ? 0u : 1u);
+          }
+          first_pv[t] = false;
+          ptx::mma_commit(bar(kOBar + t));
+          pend[t] = -1;
+        }
+        if (ok && have_prev) ptx::mma_commit(bar(kVEmpty + prev_st));
+      }
+      // Wait until every MMA this thread issued has finished.
+      ptx::mma_commit(bar(kDrain));
+      wait1(bar(kDrain), 0u, abort_flag, p, false);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;  // query tile of this warpgroup
+    const int wq = warp & 3;  // TMEM lane quarter
+    const int row_in_tile = wq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem_base + lane_off + static_cast<uint32_t>(t * 128);
+    const uint32_t tO = tmem_base + lane_off + 256u + static_cast<uint32_t>(t * D);
+    const float sc = p.scale_log2;
+    uint32_t s_cnt = 0, pv_cnt = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int w = item_of(k, c, G);
+      if (w >= p.n_items) break;
+      Item it;
+      decode_item(p, n_docs, w, it);
+      const int rows = it.rows[t];
+      if (rows == 0) continue;
+      const bool row_valid = row_in_tile < rows;
+      const int r = it.q0[t] + row_in_tile;
+      int klo_r = 0, khi_r = -1;
+      if (row_valid) {
+        const int2 ds = doc_span(p, n_docs, r);
+        klo_r = max(ds.x, it.klo);
+        khi_r = min(p.causal ? r : ds.y - 1, it.khi);
+      }
+      const int rloc = r - it.i * p.L;
+      const size_t mrow = (static_cast<size_t>(it.b) * p.H + it.h) * p.L + rloc;
+      if (it.f_lo[t] > it.f_hi[t]) {
+        // No visible key for the whole tile (a skipped step): empty partial.
+        if (kPartial && row_valid) {
+          float4* o4 = reinterpret_cast<float4*>(
+              p.o_part + ((static_cast<size_t>(it.b) * p.L + rloc) * p.H + it.h) * D);
+#pragma unroll
+          for (int x = 0; x < D / 4; ++x) o4[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+          p.m_part[mrow] = -INFINITY;
+          p.l_part[mrow] = 0.f;
+        }
+        continue;
+      }
+      float m_used = -INFINITY, m_true = -INFINITY, l_run = 0.f;
+      for (int f = it.f_lo[t]; f <= it.f_hi[t]; ++f) {
+        if (!wait_warp(bar(kSFull + t), s_cnt & 1u, abort_flag, p)) { ok = false; break; }
+        ++s_cnt;
+        ptx::tc_fence_after();
+        uint32_t sv[4][32];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) ptx::tmem_ld32(tS + ch * 32, sv[ch]);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) ptx::reg_fence(sv[ch]);
+        int ks, ke;
+        tile_keys(p, f, ks, ke);
+        const int c_lo = klo_r - ks;
+        const int c_hi = min(khi_r, ke - 1) - ks;
+        if (c_lo > 0 || c_hi < kBN - 1) {
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+            for (int x = 0; x < 32; ++x) {
+              const int cc = ch * 32 + x;
+              if (cc < c_lo || cc > c_hi) sv[ch][x] = __float_as_uint(-INFINITY);
+            }
+        }
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          mx0 = fmaxf(mx0, __uint_as_float(sv[0][x]));
+          mx1 = fmaxf(mx1, __uint_as_float(sv[1][x]));
+          mx2 = fmaxf(mx2, __uint_as_float(sv[2][x]));
+          mx3 = fmaxf(mx3, __uint_as_float(sv[3][x]));
+        }
+        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sc;
+        m_true = fmaxf(m_true, m_tile);
+        float alpha = 1.f;
+        bool rescale_o = false;
+        if (m_tile > m_used + kRescaleLog2) {
+          rescale_o = (m_used != -INFINITY);
+          alpha = rescale_o ? ptx::ex2(m_used - m_tile) : 0.f;
+          l_run *= alpha;
+          m_used = m_tile;
+        }
+        const float base = (m_used == -INFINITY) ? 0.f : m_used;
+        float ls0 = 0.f, ls1 = 0.f;
+        uint32_t pk[2][32];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+          for (int x = 0; x < 16; ++x) {
+            const float p0 = ptx::ex2(fmaf(__uint_as_float(sv[ch][2 * x]), sc, -base));
+            const float p1 = ptx::ex2(fmaf(__uint_as_float(sv[ch][2 * x + 1]), sc, -base));
+            ls0 += p0;
+            ls1 += p1;
+            pk[ch >> 1][(ch & 1) * 16 + x] = ptx::pack_bf16(p0, p1);
+          }
+        l_run += ls0 + ls1;
+        ptx::tmem_st32(tS, pk[0]);
+        ptx::tmem_st32(tS + 32, pk[1]);
+        if (__any_sync(0xffffffffu, rescale_o)) {
+          // O_t holds the sum up to the previous tile once that PV is done.
+          if (!wait_warp(bar(kOBar + t), (pv_cnt - 1u) & 1u, abort_flag, p)) { ok = false; break; }
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t ov[32];
+            ptx::tmem_ld32(tO + ch * 32, ov);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence(ov);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * alpha);
+            ptx::tmem_st32(tO + ch * 32, ov);
+          }
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(kPReady + t));
+        ++pv_cnt;
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      if (!wait_warp(bar(kOBar + t), (pv_cnt - 1u) & 1u, abort_flag, p)) { ok = false; break; }
+      ptx::tc_fence_after();
+      if (!kPartial) {
+        const float inv_l = 1.f / l_run;
+        uint4* dst = reinterpret_cast<uint4*>(
+            p.out + ((static_cast<size_t>(it.b) * p.S + r) * p.H + it.h) * D);
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t ov[32];
+          ptx::tmem_ld32(tO + ch * 32, ov);
+          ptx::tmem_wait_ld();
+          ptx::reg_fence(ov);
+          if (row_valid) {
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              uint4 v4;
+              v4.x = ptx::pack_bf16(__uint_as_float(ov[8 * x + 0]) * inv_l,
+                                    __uint_as_float(ov[8 * x + 1]) * inv_l);
+              v4.y = ptx::pack_bf16(__uint_as_float(ov[8 * x + 2]) * inv_l,
+                                    __uint_as_float(ov[8 * x + 3]) * inv_l);
+              v4.z = ptx::pack_bf16(__uint_as_float(ov[8 * x + 4]) * inv_l,
+                                    __uint_as_float(ov[8 * x + 5]) * inv_l);
+              v4.w = ptx::pack_bf16(__uint_as_float(ov[8 * x + 6]) * inv_l,
+                                    __uint_as_float(ov[8 * x + 7]) * inv_l);
+              dst[ch * 4 + x] = v4;
+            }
+          }
+        }
+        if (row_valid) {
+          p.lse[(static_cast<size_t>(it.b) * p.H + it.h) * p.S + r] =
+              (m_used + log2f(l_run)) * 0.69314718055994531f;
+        }
+      } else {
+        const bool empty = (m_true == -INFINITY);
+        const float fac = empty ? 0.f : ptx::ex2(m_used - m_true);
+        float4* dst = reinterpret_cast<float4*>(
+            p.o_part + ((static_cast<size_t>(it.b) * p.L + rloc) * p.H + it.h) * D);
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t ov[32];
+          ptx::tmem_ld32(tO + ch * 32, ov);
+          ptx::tmem_wait_ld();
+          ptx::reg_fence(ov);
+          if (row_valid) {
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+              dst[ch * 8 + x] = make_float4(__uint_as_float(ov[4 * x + 0]) * fac,
+                                            __uint_as_float(ov[4 * x + 1]) * fac,
+                                            __uint_as_float(ov[4 * x + 2]) * fac,
+                                            __uint_as_float(ov[4 * x + 3]) * fac);
+          }
+        }
+        if (row_valid) {
+          p.m_part[mrow] = empty ? -INFINITY : m_true * 0.69314718055994531f;
+          p.l_part[mrow] = empty ? 0.f : l_run * fac;
+        }
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// [B, S, H, D] bf16 viewed as a 4-D tensor (D, H, S, B); box = 64 x 1 x 128 x 1.
+bool make_map(CUtensorMap* m, const void* base, int B, int S, int H, int D) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
+                           static_cast<cuuint64_t>(S) * H * D * 2};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kBM), 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D, bool kPartial>
+cudaError_t launch_t(const AttnArgs& a, cudaStream_t stream) {
+  using Lay = Layout<D>;
+  static_assert(Lay::kAlloc <= 232448, "shared memory budget");
+  auto kern = ring_attn_bf16_kernel<D, kPartial>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kAlloc);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, a.q, a.B, a.S, a.H, D) || !make_map(&mk, a.k, a.B, a.S, a.H, D) ||
+      !make_map(&mv, a.v, a.B, a.S, a.H, D))
+    return cudaErrorInvalidValue;
+
+  KParams p{};
+  p.B = a.B;
+  p.S = a.S;
+  p.H = a.H;
+  p.n_shards = a.n_shards;
+  p.L = a.S / a.n_shards;
+  p.q_shard = a.q_shard;
+  p.k_shard = a.k_shard;
+  p.causal = a.causal;
+  p.doc_offsets = a.doc_offsets;
+  p.doc_info = a.doc_info;
+  p.n_qshards = (a.q_shard < 0) ? a.n_shards : 1;
+  p.pairs_per_shard = (p.L + kBM * kQTiles - 1) / (kBM * kQTiles);
+  p.tiles_per_shard = (p.L + kBN - 1) / kBN;
+  const long long items = static_cast<long long>(a.B) * a.H * p.n_qshards * p.pairs_per_shard;
+  if (items > INT_MAX) return cudaErrorInvalidValue;
+  p.n_items = static_cast<int>(items);
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.lse = a.lse;
+  p.o_part = a.o_part;
+  p.m_part = a.m_part;
+  p.l_part = a.l_part;
+  p.err = device_error_word();
+  if (!p.err) return cudaErrorInvalidValue;
+  p.timeout_ns = kTimeoutNs;
+  const int grid = static_cast<int>(std::min<long long>(items, sm_count()));
+  if (grid <= 0) return cudaSuccess;
+  kern<<<grid, kThreads, Lay::kAlloc, stream>>>(mq, mk, mv, p);
+  count_launch(0);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bf16(const AttnArgs& a, cudaStream_t stream) {
+  const bool partial = (a.k_shard >= 0);
+  if (a.d == 128) return partial ? launch_t<128, true>(a, stream) : launch_t<128, false>(a, stream);
+  if (a.d == 64) return partial ? launch_t<64, true>(a, stream) : launch_t<64, false>(a, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace cpring

@@ -1,0 +1,57 @@
+// Host-side declarations shared by the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime_api.h>
+
+#include "../../include/cpring.h"
+
+namespace cpring {
+
+// What one launch computes: every query shard (q_shard < 0) or one shard
+// (q_shard = i), against every key shard (k_shard < 0) or one (k_shard = j).
+struct AttnArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  int B, S, H, d, n_shards;
+  int q_shard, k_shard;
+  int causal;
+  const int32_t* doc_offsets;  // device or null
+  const int32_t* doc_info;     // device scratch written by the doc scan, or null
+  // fused outputs
+  void* out;
+  float* lse;
+  // partial (one step) outputs
+  float* o_part;
+  float* m_part;
+  float* l_part;
+};
+
+// Sticky device error word (bits of kErr*), owned by merge.cu.
+constexpr int kErrDocOffsets = 1;
+constexpr int kErrTimeout = 2;
+int* device_error_word();   // device address for the current device, or null
+
+// Launchers: return cudaSuccess or the launch error.
+cudaError_t launch_attn_bf16(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_attn_f32(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_doc_scan(const int32_t* doc_offsets, int S, int32_t* doc_info,
+                            cudaStream_t stream);
+cudaError_t launch_merge(float* o_acc, float* m_acc, float* l_acc, const float* o_part,
+                         const float* m_part, const float* l_part, int B, int rows, int H, int d,
+                         cudaStream_t stream);
+cudaError_t launch_finalize(const float* o_acc, const float* m_acc, const float* l_acc, void* out,
+                            float* lse, int B, int rows, int H, int d, int out_is_bf16,
+                            cudaStream_t stream);
+
+// Host launch counters (index: 0 tcgen05 attention, 1 fp32 attention,
+// 2 merge/finalize, 3 doc scan).
+void count_launch(int which);
+
+// Multiprocessor count of the current device (cached per device).
+int sm_count();
+// Compute capability major*10+minor of the current device (cached).
+int device_cc();
+
+}  // namespace cpring

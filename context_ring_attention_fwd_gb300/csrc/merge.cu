@@ -1,0 +1,262 @@
+// Standalone online-softmax merge and final normalisation, the doc_offsets
+// scan, and the library's per-device error word.
+//
+// Merge ("上下文並行（Context Parallelism, CP）", compassingai.com, section
+// 線上 Softmax, the 線上合併 lines of the algorithm):
+//   m_new = max(m, m'); O = O e^{m - m_new} + O' e^{m' - m_new};
+//   l = l e^{m - m_new} + l' e^{m' - m_new}; m = m_new.
+// Finalisation (last line of the same algorithm): O / l, plus the
+// log-sum-exp m + log l.
+//
+// Both are elementwise over [B, rows, H, d] fp32 state and bound by HBM
+// bandwidth: one warp per (b, row, h) reads its two scalars (m, l) once and
+// streams the d-vector with 16-byte accesses; the grid is a multiple of the
+// SM count and strides over all rows.
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include <atomic>
+#include <cmath>
+#include <mutex>
+
+#include "internal.h"
+
+namespace cpring {
+
+// Sticky error word: one per device that loads this library.
+__device__ int g_cp_error_word;
+
+namespace {
+
+constexpr int kMergeThreads = 256;
+
+__device__ __forceinline__ void merge_factors(float m, float mp, float& a, float& c, float& mn) {
+  mn = fmaxf(m, mp);
+  if (mn == -INFINITY) {  // both empty
+    a = 0.f;
+    c = 0.f;
+    return;
+  }
+  a = (m == -INFINITY) ? 0.f : expf(m - mn);
+  c = (mp == -INFINITY) ? 0.f : expf(mp - mn);
+}
+
+__global__ void __launch_bounds__(kMergeThreads)
+    lse_merge_kernel(float* __restrict__ o_acc, float* __restrict__ m_acc,
+                     float* __restrict__ l_acc, const float* __restrict__ o_part,
+                     const float* __restrict__ m_part, const float* __restrict__ l_part, int B,
+                     int rows, int H, int d, bool vec4) {
+  const int lane = threadIdx.x & 31;
+  const long long n = static_cast<long long>(B) * rows * H;
+  const long long wstride = static_cast<long long>(gridDim.x) * (kMergeThreads / 32);
+  for (long long w = static_cast<long long>(blockIdx.x) * (kMergeThreads / 32) + (threadIdx.x >> 5);
+       w < n; w += wstride) {
+    // w enumerates (b, row, h) in memory order of O
+    const int h = static_cast<int>(w % H);
+    const long long br = w / H;
+    const int row = static_cast<int>(br % rows);
+    const int b = static_cast<int>(br / rows);
+    const size_t mi = (static_cast<size_t>(b) * H + h) * rows + row;
+    const float m = m_acc[mi], mp = m_part[mi];
+    float a, c, mn;
+    merge_factors(m, mp, a, c, mn);
+    float* o = o_acc + static_cast<size_t>(w) * d;
+    const float* op = o_part + static_cast<size_t>(w) * d;
+    if (vec4) {
+      for (int x = lane; x < d / 4; x += 32) {
+        float4 u = reinterpret_cast<float4*>(o)[x];
+        const float4 q = reinterpret_cast<const float4*>(op)[x];
+        u.x = u.x * a + q.x * c;
+        u.y = u.y * a + q.y * c;
+        u.z = u.z * a + q.z * c;
+        u.w = u.w * a + q.w * c;
+        reinterpret_cast<float4*>(o)[x] = u;
+      }
+    } else {
+      for (int x = lane; x < d; x += 32) o[x] = o[x] * a + op[x] * c;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      l_acc[mi] = l_acc[mi] * a + l_part[mi] * c;
+      m_acc[mi] = mn;
+    }
+  }
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(kMergeThreads)
+    lse_finalize_kernel(const float* __restrict__ o_acc, const float* __restrict__ m_acc,
+                        const float* __restrict__ l_acc, void* __restrict__ out,
+                        float* __restrict__ lse, int B, int rows, int H, int d, bool vec4) {
+  const int lane = threadIdx.x & 31;
+  const long long n = static_cast<long long>(B) * rows * H;
+  const long long wstride = static_cast<long long>(gridDim.x) * (kMergeThreads / 32);
+  for (long long w = static_cast<long long>(blockIdx.x) * (kMergeThreads / 32) + (threadIdx.x >> 5);
+       w < n; w += wstride) {
+    const int h = static_cast<int>(w % H);
+    const long long br = w / H;
+    const int row = static_cast<int>(br % rows);
+    const int b = static_cast<int>(br / rows);
+    const size_t mi = (static_cast<size_t>(b) * H + h) * rows + row;
+    const float l = l_acc[mi];
+    const float inv = (l > 0.f) ? 1.f / l : 0.f;
+    const float* o = o_acc + static_cast<size_t>(w) * d;
+    if (kBf16) {
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(out) + static_cast<size_t>(w) * d;
+      if (vec4) {
+        for (int x = lane; x < d / 4; x += 32) {
+          const float4 u = reinterpret_cast<const float4*>(o)[x];
+          __nv_bfloat162 lo = __floats2bfloat162_rn(u.x * inv, u.y * inv);
+          __nv_bfloat162 hi = __floats2bfloat162_rn(u.z * inv, u.w * inv);
+          reinterpret_cast<__nv_bfloat162*>(dst)[2 * x] = lo;
+          reinterpret_cast<__nv_bfloat162*>(dst)[2 * x + 1] = hi;
+        }
+      } else {
+        for (int x = lane; x < d; x += 32) dst[x] = __float2bfloat16_rn(o[x] * inv);
+      }
+    } else {
+      float* dst = static_cast<float*>(out) + static_cast<size_t>(w) * d;
+      if (vec4) {
+        for (int x = lane; x < d / 4; x += 32) {
+          float4 u = reinterpret_cast<const float4*>(o)[x];
+          u.x *= inv;
+          u.y *= inv;
+          u.z *= inv;
+          u.w *= inv;
+          reinterpret_cast<float4*>(dst)[x] = u;
+        }
+      } else {
+        for (int x = lane; x < d; x += 32) dst[x] = o[x] * inv;
+      }
+    }
+    if (lane == 0) lse[mi] = (l > 0.f) ? m_acc[mi] + logf(l) : -INFINITY;
+  }
+}
+
+// Scan a device doc_offsets array that ends at the first entry equal to S.
+// Writes the number of documents to info[0], or -1 (and raises the error
+// word) when the array is not 0 = o_0 < o_1 < ... < o_n = S.  The scan reads
+// one entry at a time and never past the terminator or past S + 1 entries.
+__global__ void doc_scan_kernel(const int32_t* __restrict__ offs, int S, int32_t* info,
+                                int* err) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  int32_t prev = offs[0];
+  bool ok = (prev == 0) && (S > 0);
+  int n = 0;
+  if (ok) {
+    for (int idx = 1; idx <= S; ++idx) {
+      const int32_t x = offs[idx];
+      if (x <= prev || x > S) {
+        ok = false;
+        break;
+      }
+      prev = x;
+      if (x == S) {
+        n = idx;
+        break;
+      }
+    }
+    if (n == 0) ok = false;
+  }
+  info[0] = ok ? n : -1;
+  if (!ok) atomicOr(err, kErrDocOffsets);
+}
+
+int grid_for(long long warps) {
+  const long long blocks = (warps + (kMergeThreads / 32) - 1) / (kMergeThreads / 32);
+  const long long cap = 8LL * sm_count();
+  return static_cast<int>(std::max<long long>(1, std::min(blocks, cap)));
+}
+
+std::atomic<long long> g_launches[4];
+
+}  // namespace
+
+void count_launch(int which) { g_launches[which].fetch_add(1, std::memory_order_relaxed); }
+
+int* device_error_word() {
+  // One address per device; cudaGetSymbolAddress is called with the device
+  // current and the result cached for that device.
+  static std::mutex mu;
+  static int* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_cp_error_word) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<int*>(p);
+  }
+  return addr[dev];
+}
+
+int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 1;
+  }
+  return cache[dev];
+}
+
+int device_cc() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev] == 0) {
+    int ma = 0, mi = 0;
+    cudaDeviceGetAttribute(&ma, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&mi, cudaDevAttrComputeCapabilityMinor, dev);
+    cache[dev] = ma * 10 + mi;
+  }
+  return cache[dev];
+}
+
+cudaError_t launch_doc_scan(const int32_t* doc_offsets, int S, int32_t* doc_info,
+                            cudaStream_t stream) {
+  int* err = device_error_word();
+  if (!err) return cudaErrorInvalidValue;
+  doc_scan_kernel<<<1, 32, 0, stream>>>(doc_offsets, S, doc_info, err);
+  count_launch(3);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge(float* o_acc, float* m_acc, float* l_acc, const float* o_part,
+                         const float* m_part, const float* l_part, int B, int rows, int H, int d,
+                         cudaStream_t stream) {
+  const long long n = static_cast<long long>(B) * rows * H;
+  const bool vec4 = (d % 4 == 0) && ((reinterpret_cast<uintptr_t>(o_acc) |
+                                       reinterpret_cast<uintptr_t>(o_part)) % 16 == 0);
+  lse_merge_kernel<<<grid_for(n), kMergeThreads, 0, stream>>>(o_acc, m_acc, l_acc, o_part, m_part,
+                                                              l_part, B, rows, H, d, vec4);
+  count_launch(2);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const float* o_acc, const float* m_acc, const float* l_acc, void* out,
+                            float* lse, int B, int rows, int H, int d, int out_is_bf16,
+                            cudaStream_t stream) {
+  const long long n = static_cast<long long>(B) * rows * H;
+  const bool vec4 = (d % 4 == 0) && ((reinterpret_cast<uintptr_t>(o_acc) |
+                                       reinterpret_cast<uintptr_t>(out)) % 16 == 0);
+  if (out_is_bf16)
+    lse_finalize_kernel<true><<<grid_for(n), kMergeThreads, 0, stream>>>(o_acc, m_acc, l_acc, out,
+                                                                         lse, B, rows, H, d,
+                                                                         vec4 && d % 8 == 0);
+  else
+    lse_finalize_kernel<false><<<grid_for(n), kMergeThreads, 0, stream>>>(o_acc, m_acc, l_acc, out,
+                                                                          lse, B, rows, H, d, vec4);
+  count_launch(2);
+  return cudaGetLastError();
+}
+
+}  // namespace cpring
+
+extern "C" void cp_launch_counts(int64_t* counts4) {
+  if (!counts4) return;
+  for (int i = 0; i < 4; ++i)
+    counts4[i] = cpring::g_launches[i].load(std::memory_order_relaxed);
+}

@@ -1,0 +1,199 @@
+/*
+ * cpring — context-parallel ring-attention forward on one GB300 (sm_103a).
+ *
+ * The method: the sequence is cut into N contiguous equal shards; every
+ * query shard Q_i visits the K/V shards j in ring order, computes a partial
+ * attention against each and folds it into a running (O_i, m_i, l_i) with the
+ * online-softmax merge; causally dead steps (j > i) are skipped; the output is
+ * O_i / l_i and the log-sum-exp.  Sources: the "上下文並行（Context
+ * Parallelism, CP）" page (compassingai.com), sections 數學基礎, 線上 Softmax
+ * (algorithm "Ring Attention + FlashAttention 分塊計算") and 因果掩碼的特殊處理;
+ * the "大语言模型并行策略（五）：上下文并行" page (wangyu.me), sections
+ * Attention 的流式计算, Ring Attention and 通信模式; the "Context Parallel"
+ * page (process-cxr.github.io), sections 基本机制 and 常见失败模式 (document
+ * boundaries of packed samples).
+ *
+ * All N virtual ranks run on one GPU: the ring's send/receive becomes a
+ * double-buffered walk over K/V tiles that TMA streams from HBM.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  Layout      q, k, v, out: [B, S, H, d], row-major, d fastest (contiguous).
+ *              lse: [B, H, S] fp32, natural log.  Per-step state: O as
+ *              [B, S/N, H, d] fp32, m and l as [B, H, S/N] fp32 (natural-log
+ *              units: m is the row max of q.k/sqrt(d)).
+ *  Shards      shard i = tokens [i*S/N, (i+1)*S/N); S % N must be 0.
+ *  Masks       causal: key k visible to query q iff k <= q.  doc_offsets:
+ *              NULL = one document per batch row; otherwise a DEVICE int32
+ *              array 0 = o_0 < o_1 < ... < o_n = S, read up to and including
+ *              the first entry equal to S (cu_seqlens style); the same
+ *              boundaries apply to every batch row; key k is visible to q
+ *              only if both lie in the same document.
+ *  Ownership   the caller owns every buffer and the stream.  Calls are
+ *              asynchronous on `stream`; only cp_get_last_status
+ *              synchronises.  When doc_offsets is given the library takes a
+ *              16-byte stream-ordered scratch allocation for the call.
+ *  Errors      arguments are checked on the host before any launch; a
+ *              violation returns a negative cp_status and launches nothing.
+ *              Faults found on the device (malformed doc_offsets, a wait
+ *              that ran out) set a sticky device error word; the call that
+ *              found them writes none of its outputs, and the error is
+ *              reported by cp_get_last_status.
+ *  Pointers    q/k/v/out/o_part: 16-byte aligned; lse/m/l: 4-byte aligned.
+ */
+#ifndef CPRING_H
+#define CPRING_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int cp_status;
+
+enum {
+  CP_OK = 0,
+  CP_ERR_NULL = -1,         /* a required pointer is NULL                       */
+  CP_ERR_SHAPE = -2,        /* sizes out of range, S % N != 0, i/j out of range */
+  CP_ERR_UNSUPPORTED = -3,  /* head dim not supported by this entry point       */
+  CP_ERR_ALIGN = -4,        /* a pointer is not aligned as required             */
+  CP_ERR_CUDA = -5,         /* a CUDA runtime call or launch failed             */
+  CP_ERR_BUFFER = -6,       /* an output buffer is too small                    */
+  CP_ERR_DOC_OFFSETS = -7,  /* doc_offsets not 0 < ... < S terminated by S      */
+  CP_ERR_TIMEOUT = -8,      /* a bounded device wait ran out; outputs invalid   */
+  CP_ERR_DEVICE = -9        /* current device is not an sm_103 GPU              */
+};
+
+/*
+ * Fused ring-attention forward, bf16 inputs and output, fp32 accumulation.
+ * ("Context Parallelism", 線上 Softmax algorithm, run for every rank i with
+ * the causal skip of 因果掩碼的特殊處理; log-sum-exp in natural log.)
+ *
+ *  q, k, v   device, bf16 [B,S,H,d], read only.
+ *  out       device, bf16 [B,S,H,d], written: softmax(q k^T/sqrt(d)) v.
+ *  lse       device, fp32 [B,H,S], written: log sum_k exp(q.k/sqrt(d)).
+ *  B,S,H     >= 1; S < 2^31; n_shards in [1, S], S % n_shards == 0.
+ *  d         64 or 128.
+ *  causal    0 or 1.
+ *  doc_offsets  NULL or device int32 (see Masks).
+ *  stream    CUDA stream (0 = legacy default stream).
+ * Runs on tcgen05 tensor cores; K/V tiles of each shard are streamed by TMA
+ * into a double-buffered shared-memory ring.  The result does not depend on
+ * n_shards beyond floating-point rounding.
+ */
+cp_status cp_ring_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                           int B, int S, int H, int d, int n_shards, int causal,
+                           const int32_t* doc_offsets, cudaStream_t stream);
+
+/* Same operation in true fp32 (CUDA-core FFMA, no TF32): q, k, v, out are
+ * float [B,S,H,d]; d in [1, 128]; 4-byte alignment suffices. */
+cp_status cp_ring_attn_fwd_f32(const float* q, const float* k, const float* v, float* out,
+                               float* lse, int B, int S, int H, int d, int n_shards, int causal,
+                               const int32_t* doc_offsets, cudaStream_t stream);
+
+/*
+ * One partial-attention step for the shard pair (i, j) ("Context
+ * Parallelism", 線上 Softmax algorithm, the body of the j loop before the
+ * merge): S_ij = Q_i K_j^T / sqrt(d) with the causal/document mask,
+ * m_ij = rowmax(S_ij), P_ij = exp(S_ij - m_ij), l_ij = rowsum(P_ij),
+ * O_ij = P_ij V_j (unnormalised).
+ *
+ *  q, k, v   device bf16 [B,S,H,d] (the whole sequence; the call reads
+ *            Q rows of shard i and K/V rows of shard j only).
+ *  o_part    device fp32 [B,S/N,H,d], written.
+ *  m_part    device fp32 [B,H,S/N], written (natural-log units).
+ *  l_part    device fp32 [B,H,S/N], written.
+ *  i, j      0 <= i, j < n_shards.
+ * Rows of Q_i that see no key of shard j get m = -inf, l = 0, O = 0.
+ */
+cp_status cp_ring_step(const void* q, const void* k, const void* v, float* o_part,
+                       float* m_part, float* l_part, int B, int S, int H, int d, int n_shards,
+                       int i, int j, int causal, const int32_t* doc_offsets,
+                       cudaStream_t stream);
+
+/* cp_ring_step with fp32 q, k, v (CUDA-core FFMA); d in [1, 128]. */
+cp_status cp_ring_step_f32(const float* q, const float* k, const float* v, float* o_part,
+                           float* m_part, float* l_part, int B, int S, int H, int d,
+                           int n_shards, int i, int j, int causal,
+                           const int32_t* doc_offsets, cudaStream_t stream);
+
+/*
+ * Online-softmax merge of a partial into a running state, in place
+ * ("Context Parallelism", 線上 Softmax algorithm, 線上合併 lines):
+ *   m_new = max(m_acc, m_part)
+ *   o_acc = o_acc * exp(m_acc - m_new) + o_part * exp(m_part - m_new)
+ *   l_acc = l_acc * exp(m_acc - m_new) + l_part * exp(m_part - m_new)
+ *   m_acc = m_new
+ * A state with m = -inf is empty and contributes nothing (no (-inf)-(-inf)).
+ *  o_acc, o_part  device fp32 [B,rows,H,d]; m_*, l_* device fp32 [B,H,rows].
+ *  rows >= 1, d in [1, 128].  o_acc must not alias o_part.
+ */
+cp_status cp_lse_merge(float* o_acc, float* m_acc, float* l_acc, const float* o_part,
+                       const float* m_part, const float* l_part, int B, int rows, int H, int d,
+                       cudaStream_t stream);
+
+/*
+ * Final normalisation ("Context Parallelism", 線上 Softmax algorithm, last
+ * line O_i = O_i / l_i) and the log-sum-exp m + log(l).
+ *  out   device [B,rows,H,d]: bf16 if out_is_bf16, else fp32.
+ *  lse   device fp32 [B,H,rows].
+ * Rows with l = 0 (no visible key) get out = 0 and lse = -inf.
+ */
+cp_status cp_lse_finalize(const float* o_acc, const float* m_acc, const float* l_acc, void* out,
+                          float* lse, int B, int rows, int H, int d, int out_is_bf16,
+                          cudaStream_t stream);
+
+/*
+ * Host-only, integer: the skip schedule ("Context Parallelism",
+ * 因果掩碼的特殊處理: steps with no causal dependency are skipped).
+ * Each shard is cut into tiles from its first row (tile_q rows for queries,
+ * tile_k for keys; a tile never crosses a shard boundary); tiles are numbered
+ * in order across shards.  A (q tile, kv tile) pair is listed iff at least
+ * one of its (q, k) is visible.  Pairs are ordered by q tile, then by kv tile
+ * ascending (the ascending ring order).  With tile_q = tile_k = S/N the list
+ * is the shard-pair schedule, N(N+1)/2 pairs when causal without documents.
+ *  doc_offsets_host  NULL or HOST int32 (same format as on the device).
+ *  pairs_out  host int32 [2*max_pairs] or NULL (count only).
+ *  n_pairs    host, written: the number of pairs.
+ * Returns CP_ERR_BUFFER (after writing max_pairs pairs and *n_pairs) when
+ * the list does not fit.
+ */
+cp_status cp_ring_schedule(int S, int n_shards, int tile_q, int tile_k, int causal,
+                           const int32_t* doc_offsets_host, int32_t* pairs_out, int64_t max_pairs,
+                           int64_t* n_pairs);
+
+/*
+ * Host-only, integer: bytes each virtual rank would send plus receive if the
+ * K/V blocks travelled a real ring ("大语言模型并行策略（五）：上下文并行",
+ * 通信模式: 2 x (G/N) x (N-1), G = K and V bytes of the whole sequence,
+ * G = 2*B*S*H*d*dtype_bytes).  With causal != 0, a block of shard s is only
+ * forwarded to ranks r > s, so rank i receives i blocks and sends i+1
+ * (none for the last rank).
+ *  per_rank_bytes  host int64 [n_shards], written.
+ */
+cp_status cp_ring_traffic(int64_t B, int64_t S, int64_t H, int64_t d, int dtype_bytes,
+                          int n_shards, int causal, int64_t* per_rank_bytes);
+
+/*
+ * Synchronise `stream`, then read and clear the sticky device error word of
+ * the current device: CP_OK, CP_ERR_DOC_OFFSETS or CP_ERR_TIMEOUT (the
+ * lowest code wins when several were raised); CP_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+cp_status cp_get_last_status(cudaStream_t stream);
+
+/* A static, human-readable name for a status code. */
+const char* cp_status_string(cp_status status);
+
+/* Number of tcgen05 kernel launches, fp32 kernel launches, merge/finalize
+ * launches and doc-scan launches made by this process so far (host-side
+ * counters, for launch accounting in benchmarks). */
+void cp_launch_counts(int64_t* counts4);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPRING_H */

@@ -1,0 +1,311 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Tolerances (fixed for this hot path): fp32 inputs within max-abs 1e-4 of the
+oracle; bf16 inputs with fp32 accumulation within max-abs 2e-2 and mean-abs
+2e-3, applied to the output and, with the same max-abs bound, to the
+log-sum-exp.  Full-size workloads are checked on seeded samples of query
+rows (512 per head) plus the Q = 0 closed form over every row.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import context_ring_attention_fwd_gb300 as pkg
+from context_ring_attention_fwd_gb300 import inputs
+from oracle import ref
+
+pytestmark = pytest.mark.gpu
+
+F32_TOL = 1e-4
+BF16_MAX, BF16_MEAN = 2e-2, 2e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    if not os.path.exists(pkg.LIB_PATH):
+        from context_ring_attention_fwd_gb300 import _build
+        _build.build()
+    pkg.lib()
+    torch.cuda.set_device(0)
+    yield
+    assert pkg.cp_get_last_status() == 0
+
+
+DEV = "cuda"
+
+
+def _np(t):
+    return t.detach().float().cpu().numpy()
+
+
+def _check_bf16(out, lse, want_o, want_l, what=""):
+    e = np.abs(_np(out) - want_o)
+    el = np.abs(_np(lse) - want_l)
+    assert np.all(np.isfinite(_np(out))), what
+    assert e.max() <= BF16_MAX, (what, e.max())
+    assert e.mean() <= BF16_MEAN, (what, e.mean())
+    assert el.max() <= BF16_MAX, (what, el.max())
+
+
+def _check_f32(out, lse, want_o, want_l, what=""):
+    assert np.abs(_np(out) - want_o).max() <= F32_TOL, what
+    assert np.abs(_np(lse) - want_l).max() <= F32_TOL, what
+
+
+# ----------------------------------------------------------------- fp32 path
+def test_tiny_f32_workload():
+    w = inputs.BY_NAME["tiny_f32_causal"]
+    q, k, v, docs = inputs.workload_inputs(w)
+    out, lse = pkg.ring_attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), w.n_shards, w.causal, docs)
+    want_o, want_l = ref.attention(q.numpy(), k.numpy(), v.numpy(), w.causal, docs)
+    _check_f32(out, lse, want_o, want_l)
+    assert pkg.cp_get_last_status() == 0
+
+
+@pytest.mark.parametrize("causal,docs", [(True, None), (False, None), (True, [0, 37, 100, 192]),
+                                         (False, [0, 60, 61, 192])])
+def test_f32_steps_and_merge_against_oracle(causal, docs):
+    B, S, H, d, N = 2, 192, 2, 48, 3
+    q, k, v = inputs.make_qkv(B, S, H, d, seed=3, dtype=torch.float32)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    dd = pkg.doc_offsets_tensor(docs, DEV)
+    L = S // N
+    for i in range(N):
+        for j in range(N):
+            o = torch.empty((B, L, H, d), device=DEV)
+            m = torch.empty((B, H, L), device=DEV)
+            l = torch.empty((B, H, L), device=DEV)
+            pkg.cp_ring_step(qd, kd, vd, o, m, l, N, i, j, causal, dd)
+            wo, wm, wl = ref.partial_step(q.numpy(), k.numpy(), v.numpy(), N, i, j, causal, docs)
+            empty = ~np.isfinite(wm)
+            assert np.array_equal(~np.isfinite(_np(m)), empty)
+            assert np.all(_np(l)[empty] == 0)
+            np.testing.assert_allclose(_np(m)[~empty], wm[~empty], rtol=0, atol=F32_TOL)
+            np.testing.assert_allclose(_np(l), wl, rtol=1e-5, atol=F32_TOL)
+            np.testing.assert_allclose(_np(o), wo, rtol=1e-5, atol=F32_TOL)
+    want_o, want_l = ref.attention(q.numpy(), k.numpy(), v.numpy(), causal, docs)
+    for order in ("ascending", "ring", [2, 0, 1]):
+        out, lse = pkg.ring_attn_composed(qd, kd, vd, N, causal, docs, order)
+        _check_f32(out, lse, want_o, want_l, order)
+    out, lse = pkg.ring_attn_fwd(qd, kd, vd, N, causal, docs)
+    _check_f32(out, lse, want_o, want_l, "fused")
+
+
+# ----------------------------------------------------------------- bf16 path
+BF16_CASES = [
+    # B, S, H, d, N, causal, docs
+    (1, 128, 1, 128, 1, True, None),          # one tile
+    (1, 128, 1, 128, 1, False, None),
+    (1, 512, 2, 128, 1, True, None),          # several tiles, one pair of q tiles
+    (2, 768, 3, 128, 3, True, None),          # shards of 256
+    (1, 640, 2, 128, 2, False, None),         # shards of 320: ragged tiles inside shards
+    (1, 1000, 2, 64, 5, True, None),          # d = 64, shards of 200
+    (1, 1000, 2, 128, 4, False, None),        # S not a multiple of the tile
+    (1, 1024, 2, 128, 4, True, [0, 100, 101, 300, 777, 1024]),
+    (2, 896, 2, 64, 7, False, [0, 128, 500, 896]),
+]
+
+
+@pytest.mark.parametrize("B,S,H,d,N,causal,docs", BF16_CASES)
+def test_bf16_fused_against_oracle(B, S, H, d, N, causal, docs):
+    q, k, v = inputs.make_qkv(B, S, H, d, seed=S + d + N, dtype=torch.bfloat16)
+    out, lse = pkg.ring_attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), N, causal, docs)
+    assert pkg.cp_get_last_status() == 0
+    want_o, want_l = ref.attention(_np(q), _np(k), _np(v), causal, docs)
+    _check_bf16(out, lse, want_o, want_l)
+
+
+@pytest.mark.parametrize("causal,docs", [(True, None), (False, None),
+                                         (True, [0, 300, 301, 700, 1024])])
+def test_bf16_steps_against_oracle(causal, docs):
+    B, S, H, d, N = 1, 1024, 2, 128, 4
+    q, k, v = inputs.make_qkv(B, S, H, d, seed=77, dtype=torch.bfloat16)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    dd = pkg.doc_offsets_tensor(docs, DEV)
+    L = S // N
+    qn, kn, vn = _np(q), _np(k), _np(v)
+    for i in range(N):
+        for j in range(N):
+            o = torch.full((B, L, H, d), 7.0, device=DEV)
+            m = torch.full((B, H, L), 7.0, device=DEV)
+            l = torch.full((B, H, L), 7.0, device=DEV)
+            pkg.cp_ring_step(qd, kd, vd, o, m, l, N, i, j, causal, dd)
+            wo, wm, wl = ref.partial_step(qn, kn, vn, N, i, j, causal, docs)
+            empty = ~np.isfinite(wm)
+            assert np.array_equal(~np.isfinite(_np(m)), empty), (i, j)
+            assert np.all(_np(l)[empty] == 0) and np.all(_np(o)[np.transpose(empty, (0, 2, 1))] == 0)
+            # m and l exactly as the pages define them (true row max); P in bf16
+            np.testing.assert_allclose(_np(m)[~empty], wm[~empty], rtol=0, atol=1e-3)
+            rel_l = np.abs(_np(l) - wl) / np.maximum(wl, 1.0)
+            assert rel_l.max() <= 1e-2, (i, j, rel_l.max())
+            # compare the normalised partial O_ij / l_ij
+            lw = np.transpose(np.where(empty, 1.0, wl), (0, 2, 1))[..., None]
+            lg = np.transpose(np.where(empty, 1.0, _np(l)), (0, 2, 1))[..., None]
+            e = np.abs(_np(o) / lg - wo / lw)
+            assert e.max() <= BF16_MAX and e.mean() <= BF16_MEAN, (i, j, e.max())
+
+
+@pytest.mark.parametrize("order", ["ascending", "ring", [3, 1, 0, 2]])
+def test_bf16_composed_ring_any_order(order):
+    B, S, H, d, N = 1, 1024, 2, 128, 4
+    q, k, v = inputs.make_qkv(B, S, H, d, seed=78, dtype=torch.bfloat16)
+    out, lse = pkg.ring_attn_composed(q.to(DEV), k.to(DEV), v.to(DEV), N, True, None, order)
+    want_o, want_l = ref.attention(_np(q), _np(k), _np(v), True, None)
+    _check_bf16(out, lse, want_o, want_l, str(order))
+
+
+def test_bf16_deterministic_and_guard_bands():
+    B, S, H, d, N = 1, 1536, 4, 128, 3
+    q, k, v = (t.to(DEV) for t in inputs.make_qkv(B, S, H, d, seed=5, dtype=torch.bfloat16))
+    pad = 4096
+    out_buf = torch.full((B * S * H * d + 2 * pad,), 3.0, dtype=torch.bfloat16, device=DEV)
+    lse_buf = torch.full((B * H * S + 2 * pad,), 3.0, dtype=torch.float32, device=DEV)
+    out = out_buf[pad:pad + B * S * H * d].view(B, S, H, d)
+    lse = lse_buf[pad:pad + B * H * S].view(B, H, S)
+    pkg.cp_ring_attn_fwd(q, k, v, out, lse, N, True)
+    o1, l1 = out.clone(), lse.clone()
+    for _ in range(3):
+        pkg.cp_ring_attn_fwd(q, k, v, out, lse, N, True)
+        assert torch.equal(out, o1) and torch.equal(lse, l1)
+    assert torch.all(out_buf[:pad] == 3.0) and torch.all(out_buf[-pad:] == 3.0)
+    assert torch.all(lse_buf[:pad] == 3.0) and torch.all(lse_buf[-pad:] == 3.0)
+
+
+def test_bf16_causal_poisoning_of_unneeded_shards():
+    # Rows of shard i never read K/V of shards > i: NaN there changes nothing.
+    B, S, H, d, N = 1, 2048, 2, 128, 4
+    q, k, v = (t.to(DEV) for t in inputs.make_qkv(B, S, H, d, seed=9, dtype=torch.bfloat16))
+    out, lse = pkg.ring_attn_fwd(q, k, v, N, True)
+    L = S // N
+    for i in range(N - 1):
+        kp, vp = k.clone(), v.clone()
+        kp[:, (i + 1) * L:] = float("nan")
+        vp[:, (i + 1) * L:] = float("nan")
+        o2, l2 = pkg.ring_attn_fwd(q, kp, vp, N, True)
+        rows = slice(0, (i + 1) * L)
+        assert torch.equal(o2[:, rows], out[:, rows]), i
+        assert torch.equal(l2[:, :, rows], lse[:, :, rows]), i
+    # with documents: whole tiles before the first document start of a shard
+    docs = [0, 700, 1300, 2048]
+    out, lse = pkg.ring_attn_fwd(q, k, v, N, True, docs)
+    i = 2                                            # shard [1024, 1536): first doc starts at 700
+    cut = (700 // 128) * 128
+    kp, vp = k.clone(), v.clone()
+    kp[:, :cut] = float("nan")
+    vp[:, :cut] = float("nan")
+    kp[:, (i + 1) * L:] = float("nan")
+    vp[:, (i + 1) * L:] = float("nan")
+    o2, l2 = pkg.ring_attn_fwd(q, kp, vp, N, True, docs)
+    rows = slice(i * L, (i + 1) * L)
+    assert torch.equal(o2[:, rows], out[:, rows])
+    assert torch.equal(l2[:, :, rows], lse[:, :, rows])
+
+
+def test_bf16_empty_step_is_identity():
+    B, S, H, d, N = 1, 512, 2, 128, 4
+    q, k, v = (t.to(DEV) for t in inputs.make_qkv(B, S, H, d, seed=2, dtype=torch.bfloat16))
+    L = S // N
+    o = torch.full((B, L, H, d), 5.0, device=DEV)
+    m = torch.full((B, H, L), 5.0, device=DEV)
+    l = torch.full((B, H, L), 5.0, device=DEV)
+    pkg.cp_ring_step(q, k, v, o, m, l, N, 1, 3, True)      # j > i: fully masked
+    assert torch.all(o == 0) and torch.all(l == 0) and torch.all(torch.isneginf(m))
+
+
+def test_malformed_doc_offsets_reported():
+    B, S, H, d, N = 1, 256, 1, 128, 2
+    q, k, v = (t.to(DEV) for t in inputs.make_qkv(B, S, H, d, seed=2, dtype=torch.bfloat16))
+    out = torch.full_like(q, 9.0)
+    lse = torch.full((B, H, S), 9.0, device=DEV)
+    for bad in ([0, 100, 100, 256], [1, 256], [0, 300], [0, 50, 20, 256]):
+        dd = torch.tensor(bad, dtype=torch.int32, device=DEV)
+        pkg.cp_ring_attn_fwd(q, k, v, out, lse, N, True, dd)
+        assert pkg.cp_get_last_status() == pkg.STATUS_CODES["CP_ERR_DOC_OFFSETS"], bad
+        assert torch.all(out == 9.0) and torch.all(lse == 9.0)
+    assert pkg.cp_get_last_status() == 0
+
+
+def test_native_kernels_launch():
+    before = pkg.launch_counts()
+    q, k, v = (t.to(DEV) for t in inputs.make_qkv(1, 256, 1, 128, seed=1, dtype=torch.bfloat16))
+    pkg.ring_attn_fwd(q, k, v, 2, True)
+    pkg.ring_attn_fwd(q.float(), k.float(), v.float(), 2, True)
+    after = pkg.launch_counts()
+    assert after[0] == before[0] + 1 and after[1] == before[1] + 1
+
+
+# ------------------------------------------------------------ full workloads
+def _device_inputs(w):
+    q, k, v = inputs.make_qkv(w.B, w.S, w.H, w.d, w.seed, w.torch_dtype, w.scale, device=DEV)
+    docs = (inputs.make_doc_offsets(w.S, w.seed + 1, w.doc_min, w.doc_max)
+            if w.packed_docs else None)
+    return q, k, v, docs
+
+
+def _sampled_check(w, q, k, v, docs, out, lse, n_rows=512, heads=None):
+    qn, kn, vn = _np(q), _np(k), _np(v)
+    on, ln = _np(out), _np(lse)
+    errs, errs_l = [], []
+    heads = range(w.H) if heads is None else heads
+    for b in range(w.B):
+        for h in heads:
+            rows = inputs.sample_rows(w.S, n_rows, seed=w.seed * 100 + b * w.H + h)
+            wo, wl = ref.attention_rows(qn, kn, vn, b, h, rows, w.causal, docs)
+            errs.append(np.abs(on[b, rows, h] - wo))
+            errs_l.append(np.abs(ln[b, h, rows] - wl))
+    e = np.concatenate([x.ravel() for x in errs])
+    el = np.concatenate([x.ravel() for x in errs_l])
+    assert e.max() <= BF16_MAX and e.mean() <= BF16_MEAN, (w.name, e.max(), e.mean())
+    assert el.max() <= BF16_MAX, (w.name, el.max())
+
+
+def _zero_q_check(w, k, v, docs):
+    q0 = torch.zeros_like(k)
+    out, lse = pkg.ring_attn_fwd(q0, k, v, w.n_shards, w.causal, docs)
+    cf_o, cf_l = ref.zero_query_closed_form(_np(v), w.causal, docs)
+    e = np.abs(_np(out) - cf_o)
+    assert e.max() <= BF16_MAX and e.mean() <= BF16_MEAN, (w.name, e.max(), e.mean())
+    assert np.abs(_np(lse) - cf_l).max() <= BF16_MAX
+
+
+def test_workload_causal_8k_and_shard_invariance():
+    w = inputs.BY_NAME["bf16_causal_8k"]
+    q, k, v, docs = _device_inputs(w)
+    outs = {}
+    for N in (1, 2, 4, 8):
+        outs[N] = pkg.ring_attn_fwd(q, k, v, N, w.causal, docs)
+    _sampled_check(w, q, k, v, docs, *outs[w.n_shards], n_rows=256)
+    for N in (1, 2, 8):
+        e = (outs[N][0].float() - outs[w.n_shards][0].float()).abs()
+        assert e.max().item() <= BF16_MAX and e.mean().item() <= BF16_MEAN
+    _zero_q_check(w, k, v, docs)
+
+
+def test_workload_full_32k():
+    w = inputs.BY_NAME["bf16_full_32k"]
+    q, k, v, docs = _device_inputs(w)
+    out, lse = pkg.ring_attn_fwd(q, k, v, w.n_shards, w.causal, docs)
+    _sampled_check(w, q, k, v, docs, out, lse, n_rows=128)
+    _zero_q_check(w, k, v, docs)
+
+
+def test_workload_causal_128k():
+    w = inputs.BY_NAME["bf16_causal_128k"]
+    q, k, v, docs = _device_inputs(w)
+    out, lse = pkg.ring_attn_fwd(q, k, v, w.n_shards, w.causal, docs)
+    assert pkg.cp_get_last_status() == 0
+    _sampled_check(w, q, k, v, docs, out, lse, n_rows=512, heads=range(0, w.H, 4))
+    _zero_q_check(w, k, v, docs)
+
+
+def test_workload_packed_docs_64k():
+    w = inputs.BY_NAME["bf16_causal_packed_64k"]
+    q, k, v, docs = _device_inputs(w)
+    out, lse = pkg.ring_attn_fwd(q, k, v, w.n_shards, w.causal, docs)
+    assert pkg.cp_get_last_status() == 0
+    _sampled_check(w, q, k, v, docs, out, lse, n_rows=512, heads=range(0, w.H, 2))
+    _zero_q_check(w, k, v, docs)
