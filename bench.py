@@ -1,0 +1,405 @@
+"""Benchmark of the ring-attention forward on GB300.
+
+One step = one cp_ring_attn_fwd call over the whole workload (every virtual
+rank, every visible K/V tile) with Q/K/V already resident in HBM.  The
+metric is effective causal TFLOP/s: 4 d FLOPs per visible (q, k) pair, summed
+over (b, h), divided by the device time of the step.  Inputs are far larger
+than L2 (3 GiB at the 128K workload), so no flush is needed between steps.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload NAME] [--no-cpu-baseline]
+For N > 1 it is launched by torch.distributed.run, one process per GPU; each
+rank runs an independent replica of the workload (the single-GPU path has no
+exchange step to shard), the step time is the max over ranks and the value is
+the work of all ranks divided by that time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from context_ring_attention_fwd_gb300 import inputs  # noqa: E402
+
+METRIC = "effective causal TFLOP/s of ring-attention fwd (1 GB300) and % of bf16 dense peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "bf16_causal_128k"
+
+
+# ------------------------------------------------------------------ helpers
+def visible_pairs(S: int, causal: bool, docs) -> int:
+    """Visible (q, k) pairs of one (b, h): S(S+1)/2 causal, S^2 full, and per
+    document L(L+1)/2 or L^2 with packed documents."""
+    spans = [S] if docs is None else [b - a for a, b in zip(docs[:-1], docs[1:])]
+    return sum(L * (L + 1) // 2 if causal else L * L for L in spans)
+
+
+def effective_flops(w, docs) -> int:
+    return 4 * w.d * visible_pairs(w.S, w.causal, docs) * w.B * w.H
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend)
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        if device is not None and torch.distributed.get_backend() == "nccl":
+            torch.distributed.barrier(device_ids=[device.index])
+        else:
+            torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Max of a host scalar over all ranks (timing only, no data path)."""
+    if world <= 1:
+        return float(x)
+    dev = device if (device is not None and torch.distributed.get_backend() == "nccl") else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("bf16_tflops"), d.get("bf16_tflops_sustained"), "measured"
+    return 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power) if power else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def gpu_index(local_rank: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        items = [x.strip() for x in vis.split(",") if x.strip()]
+        if local_rank < len(items) and items[local_rank].isdigit():
+            return int(items[local_rank])
+    return local_rank
+
+
+# ------------------------------------------------------------ oracle timing
+def oracle_sample(w, get_head, docs, budget_s: float, rows_per_head: int, seed: int = 0,
+                  max_heads: int = 1 << 30):
+    """Time the fp64 oracle on sampled query rows of the workload, one (b, h)
+    head after another, until the budget is spent (at least one head).
+    get_head(b, h) returns that head's q, k, v as [1, S, 1, d] fp32 numpy
+    arrays (fetched outside the timed part).  Returns (effective FLOPs
+    done, seconds, description)."""
+    from oracle import ref  # the CPU baseline leg: the only bench use of the oracle
+
+    flops = 0
+    heads_done = 0
+    dt = 0.0
+    combos = [(b, h) for b in range(w.B) for h in range(w.H)]
+    rng = np.random.default_rng(seed)
+    rng.shuffle(combos)
+    kk = np.asarray(docs) if docs is not None else None
+    for b, h in combos[:max_heads]:
+        rows = inputs.sample_rows(w.S, rows_per_head, seed=seed * 1000 + b * w.H + h)
+        qh, kh, vh = get_head(b, h)
+        t0 = time.perf_counter()
+        ref.attention_rows(qh, kh, vh, 0, 0, rows, w.causal, docs)
+        dt += time.perf_counter() - t0
+        # visible keys of each sampled row
+        if kk is None:
+            cnt = (rows + 1) if w.causal else np.full(rows.shape, w.S)
+        else:
+            t = np.searchsorted(kk, rows, side="right") - 1
+            cnt = (rows - kk[t] + 1) if w.causal else (kk[t + 1] - kk[t])
+        flops += int(4 * w.d * int(np.sum(cnt)))
+        heads_done += 1
+        if dt >= budget_s:
+            break
+    desc = (f"{rows_per_head} seeded query rows x {heads_done} (b,h) heads of "
+            f"{w.name} ({w.describe()}), fp64 numpy oracle")
+    return flops, dt, desc
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------- arms
+def run_reference(args, w, rank, world):
+    """The reference arm: the fp64 CPU oracle, on rank 0 only, each step a
+    bounded sample of the workload."""
+    if rank != 0:
+        return None
+    docs = (inputs.make_doc_offsets(w.S, w.seed + 1, w.doc_min, w.doc_max)
+            if w.packed_docs else None)
+    cache = {}
+
+    def get_head(b, h):
+        # one head's Q/K/V drawn on the CPU with a per-head seed: the same
+        # shape and distribution as the workload, without drawing all heads
+        key = (b, h)
+        if key not in cache:
+            qh, kh, vh = inputs.make_qkv(1, w.S, 1, w.d, w.seed * 1000 + b * w.H + h,
+                                         w.torch_dtype, w.scale)
+            cache.clear()
+            cache[key] = tuple(t.float().numpy() for t in (qh, kh, vh))
+        return cache[key]
+
+    rows = max(8, min(256, int(2 ** 22 // max(1, w.S))))
+    for s in range(args.warmup):
+        oracle_sample(w, get_head, docs, budget_s=0.0, rows_per_head=rows, seed=s + 100,
+                      max_heads=1)
+    t_total, f_total = 0.0, 0
+    desc = ""
+    for s in range(args.steps):
+        f, dt, desc = oracle_sample(w, get_head, docs, budget_s=0.0, rows_per_head=rows,
+                                    seed=s + 1, max_heads=1)
+        t_total += dt
+        f_total += f
+    value = f_total / t_total / 1e12
+    ms = 1e3 * t_total / args.steps
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": _config(w, docs, world),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                         "sample": "each step: " + desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def _config(w, docs, world):
+    return {"workload": w.describe(), "name": w.name, "B": w.B, "S": w.S, "H": w.H, "d": w.d,
+            "n_shards": w.n_shards, "causal": w.causal,
+            "n_docs": None if docs is None else len(docs) - 1,
+            "replicas": world, "l2_flush": "none: inputs (3*B*S*H*d*2 bytes) exceed the 129 MB L2"}
+
+
+def run_ours(args, w, rank, world, local):
+    import context_ring_attention_fwd_gb300 as pkg
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pkg.lib()
+    q, k, v = inputs.make_qkv(w.B, w.S, w.H, w.d, w.seed, w.torch_dtype, w.scale, device=str(dev))
+    docs = (inputs.make_doc_offsets(w.S, w.seed + 1, w.doc_min, w.doc_max)
+            if w.packed_docs else None)
+    docs_t = pkg.doc_offsets_tensor(docs, dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    call = pkg.cp_ring_attn_fwd if w.dtype == "bf16" else pkg.cp_ring_attn_fwd_f32
+
+    def step():
+        call(q, k, v, out, lse, w.n_shards, w.causal, docs_t, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if pkg.cp_get_last_status(stream) != 0:
+        raise RuntimeError("device error during warm-up")
+
+    clocks = ClockSampler(gpu_index(local))
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = pkg.launch_counts()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    t_all0 = torch.cuda.Event(enable_timing=True)
+    t_all1 = torch.cuda.Event(enable_timing=True)
+    t_all0.record(stream)
+    for s in range(args.steps):
+        ev[s][0].record(stream)
+        step()
+        ev[s][1].record(stream)
+    t_all1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    launches1 = pkg.launch_counts()
+    clk = clocks.stop()
+    if pkg.cp_get_last_status(stream) != 0:
+        raise RuntimeError("device error during the timed region")
+    total_ms = t_all0.elapsed_time(t_all1)
+    per_launch_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = max_over_ranks(total_ms, world, dev)
+    ms = total_ms / args.steps
+    flops = effective_flops(w, docs)
+    value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
+    gpu_launches = int(sum(launches1) - sum(launches0))
+
+    # roofline of the dominant kernel (the fused attention kernel: one launch per step)
+    avg_launch_ms = statistics.mean(per_launch_ms)
+    achieved = flops / (avg_launch_ms * 1e-3) / 1e12
+    peak_burst, peak_sust, peak_src = measured_peaks()
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
+                "frac": achieved / peak_burst, "traffic": args.traffic,
+                "peak_kind": f"{peak_src} bf16 dense burst (cuBLAS)",
+                "frac_of_sustained": achieved / peak_sust if peak_sust else None}
+
+    # end to end through the public API from pinned host buffers
+    e2e = None
+    if args.e2e_steps > 0:
+        hq = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+        hk = torch.empty_like(hq, pin_memory=True)
+        hv = torch.empty_like(hq, pin_memory=True)
+        hq.copy_(q)
+        hk.copy_(k)
+        hv.copy_(v)
+        bufs = (q, k, v, out, lse, torch.empty(q.shape, dtype=q.dtype, pin_memory=True),
+                torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True))
+        pkg.ring_attn_fwd_host(hq, hk, hv, w.n_shards, w.causal, docs, buffers=bufs)
+        barrier(world, dev)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            pkg.ring_attn_fwd_host(hq, hk, hv, w.n_shards, w.causal, docs, buffers=bufs)
+        dt = time.perf_counter() - t0
+        dt = max_over_ranks(dt, world, dev)
+        elem = q.numel() * q.element_size()
+        e2e = {"value": flops * world * args.e2e_steps / dt / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": 3 * elem + (0 if docs is None else 4 * len(docs)),
+               "d2h_bytes_per_step": elem + lse.numel() * 4,
+               "ms_per_step": 1e3 * dt / args.e2e_steps, "steps": args.e2e_steps}
+        del hq, hk, hv, bufs
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        def get_head(b, h):
+            return tuple(t[b:b + 1, :, h:h + 1].float().cpu().numpy() for t in (q, k, v))
+
+        f, dt, desc = oracle_sample(w, get_head, docs, budget_s=args.cpu_budget,
+                                    rows_per_head=args.cpu_rows)
+        cpu = {"value": f / dt / 1e12, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+               "sample": desc, "seconds": dt}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": _config(w, docs, world),
+        "frac_of_peak": value / world / peak_burst,
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
+        "clocks": clk,
+        "effective_flops_per_step": flops * world,
+    }
+    return line
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.BY_NAME))
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--cpu-rows", type=int, default=128)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the attention kernel from an ncu capture")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    w = inputs.BY_NAME[args.workload]
+    if args.impl == "reference":
+        dist_init(world, "gloo")
+        line = run_reference(args, w, rank, world)
+    else:
+        dist_init(world, "nccl" if torch.cuda.is_available() else "gloo")
+        line = run_ours(args, w, rank, world, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
