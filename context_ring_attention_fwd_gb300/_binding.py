@@ -20,7 +20,7 @@ CP_OK = 0
 STATUS_NAMES = {
     0: "CP_OK", -1: "CP_ERR_NULL", -2: "CP_ERR_SHAPE", -3: "CP_ERR_UNSUPPORTED",
     -4: "CP_ERR_ALIGN", -5: "CP_ERR_CUDA", -6: "CP_ERR_BUFFER", -7: "CP_ERR_DOC_OFFSETS",
-    -8: "CP_ERR_TIMEOUT", -9: "CP_ERR_DEVICE",
+    -8: "CP_ERR_TIMEOUT", -9: "CP_ERR_DEVICE", -10: "CP_ERR_SCRATCH",
 }
 STATUS_CODES = {v: k for k, v in STATUS_NAMES.items()}
 
@@ -30,6 +30,7 @@ _lock = threading.Lock()
 _vp, _i, _i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
 _SIGS = {
     "cp_ring_attn_fwd": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp],
+    "cp_ring_attn_fwd_noalloc": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp],
     "cp_ring_attn_fwd_f32": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp],
     "cp_ring_step": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _vp, _vp],
     "cp_ring_step_f32": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _vp, _vp],
@@ -127,6 +128,22 @@ def cp_ring_attn_fwd(q, k, v, out, lse, n_shards: int, causal: bool = True,
     if doc_offsets is not None:
         _need(doc_offsets, "doc_offsets", torch.int32)
     _check("cp_ring_attn_fwd", lib().cp_ring_attn_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, H, d, int(n_shards),
+        int(bool(causal)), _ptr(doc_offsets), _stream(stream)))
+
+
+def cp_ring_attn_fwd_noalloc(q, k, v, out, lse, n_shards: int, causal: bool = True,
+                             doc_offsets: Optional[torch.Tensor] = None, stream=None) -> None:
+    """cp_ring_attn_fwd without any device allocation by the library, for
+    callers whose memory pool forbids it; at most 65,535 documents (more is
+    reported as CP_ERR_SCRATCH by cp_get_last_status)."""
+    B, S, H, d = q.shape
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _need(t, n, torch.bfloat16, (B, S, H, d))
+    _need(lse, "lse", torch.float32, (B, H, S))
+    if doc_offsets is not None:
+        _need(doc_offsets, "doc_offsets", torch.int32)
+    _check("cp_ring_attn_fwd_noalloc", lib().cp_ring_attn_fwd_noalloc(
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, H, d, int(n_shards),
         int(bool(causal)), _ptr(doc_offsets), _stream(stream)))
 

@@ -271,6 +271,7 @@ cp_status cp_get_last_status(cudaStream_t stream) {
     if (cudaMemcpy(word, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
       return CP_ERR_CUDA;
   }
+  if (bits & cpring::kErrScratch) return CP_ERR_SCRATCH;
   if (bits & cpring::kErrTimeout) return CP_ERR_TIMEOUT;
   if (bits & cpring::kErrDocOffsets) return CP_ERR_DOC_OFFSETS;
   return CP_OK;
@@ -288,6 +289,7 @@ const char* cp_status_string(cp_status s) {
     case CP_ERR_DOC_OFFSETS: return "malformed doc_offsets";
     case CP_ERR_TIMEOUT: return "device wait timed out";
     case CP_ERR_DEVICE: return "device is not sm_103";
+    case CP_ERR_SCRATCH: return "more documents than the fixed scratch of cp_ring_attn_fwd_noalloc holds";
     default: return "unknown status";
   }
 }

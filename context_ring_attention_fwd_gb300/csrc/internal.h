@@ -31,6 +31,7 @@ struct AttnArgs {
 // Sticky device error word (bits of kErr*), owned by merge.cu.
 constexpr int kErrDocOffsets = 1;
 constexpr int kErrTimeout = 2;
+constexpr int kErrScratch = 4;  // raised only by cp_ring_attn_fwd_noalloc
 int* device_error_word();   // device address for the current device, or null
 
 // Launchers: return cudaSuccess or the launch error.

@@ -63,7 +63,9 @@ enum {
   CP_ERR_BUFFER = -6,       /* an output buffer is too small                    */
   CP_ERR_DOC_OFFSETS = -7,  /* doc_offsets not 0 < ... < S terminated by S      */
   CP_ERR_TIMEOUT = -8,      /* a bounded device wait ran out; outputs invalid   */
-  CP_ERR_DEVICE = -9        /* current device is not an sm_103 GPU              */
+  CP_ERR_DEVICE = -9,       /* current device is not an sm_103 GPU              */
+  CP_ERR_SCRATCH = -10      /* problem too large for the fixed scratch of       */
+                            /* cp_ring_attn_fwd_noalloc (more than 65,535 docs) */
 };
 
 /*
@@ -86,6 +88,34 @@ enum {
 cp_status cp_ring_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
                            int B, int S, int H, int d, int n_shards, int causal,
                            const int32_t* doc_offsets, cudaStream_t stream);
+
+/*
+ * cp_ring_attn_fwd for callers that cannot let a library allocate device
+ * memory.  The pages have no counterpart: this is a deployment variant of the
+ * fused forward above, with the same arguments, layouts and result.
+ *
+ * cp_ring_attn_fwd allocates 16 bytes of stream-ordered scratch for every call
+ * that passes doc_offsets.  Processes that give nearly all GPU memory to their
+ * own pool at start-up and forbid later cudaMalloc/cudaMallocAsync, and loops
+ * that must never enter the driver's allocator, call this entry point instead:
+ * it allocates nothing and keeps its scratch in a fixed device array built into
+ * the library (262,208 bytes per GPU that loads the library, held until the
+ * process exits).
+ *
+ * Limit: doc_offsets may describe at most 65,535 documents.  A larger array
+ * is rejected on the device: nothing is written, and cp_get_last_status
+ * reports CP_ERR_SCRATCH.  Host-side checks are those of cp_ring_attn_fwd.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the array and it keeps the last
+ * call's contents; every call rewrites what it reads, so nothing needs
+ * clearing.  Calls whose GPU work can overlap (unordered streams) race on the
+ * array and must not be issued.
+ */
+cp_status cp_ring_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out,
+                                   float* lse, int B, int S, int H, int d, int n_shards,
+                                   int causal, const int32_t* doc_offsets, cudaStream_t stream);
 
 /* Same operation in true fp32 (CUDA-core FFMA, no TF32): q, k, v, out are
  * float [B,S,H,d]; d in [1, 128]; 4-byte alignment suffices. */
@@ -178,9 +208,9 @@ cp_status cp_ring_traffic(int64_t B, int64_t S, int64_t H, int64_t d, int dtype_
 
 /*
  * Synchronise `stream`, then read and clear the sticky device error word of
- * the current device: CP_OK, CP_ERR_DOC_OFFSETS or CP_ERR_TIMEOUT (the
- * lowest code wins when several were raised); CP_ERR_CUDA if the
- * synchronisation itself failed.
+ * the current device: CP_OK, CP_ERR_DOC_OFFSETS, CP_ERR_TIMEOUT or
+ * CP_ERR_SCRATCH (the lowest code wins when several were raised);
+ * CP_ERR_CUDA if the synchronisation itself failed.
  */
 cp_status cp_get_last_status(cudaStream_t stream);
 
