@@ -31,15 +31,38 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libcpring.so")
 
 
+# The tensor-core kernel moves registers between its warpgroups with
+# setmaxnreg; the split is sized for exactly this many registers per thread at
+# launch, so a build that comes out different is refused (the split would not
+# fit and the kernel would stall).
+SPLIT_KERNEL = "ring_attn_bf16_kernel"
+SPLIT_LAUNCH_REGS = 168
+
+
+def _check_split(src: str, ptxas_log: str) -> None:
+    entry = None
+    for line in ptxas_log.splitlines():
+        if "Compiling entry function" in line:
+            entry = line
+        elif "Used" in line and "registers" in line and entry and SPLIT_KERNEL in entry:
+            n = int(line.split("Used")[1].split("registers")[0])
+            if n != SPLIT_LAUNCH_REGS:
+                raise RuntimeError(f"{src}: {SPLIT_KERNEL} launches with {n} registers per "
+                                   f"thread, its register split needs {SPLIT_LAUNCH_REGS}")
+            entry = None
+
+
 def _compile(src: str, verbose: bool) -> str:
     obj = os.path.join(OBJDIR, os.path.splitext(src)[0] + ".o")
     cmd = [_nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
            "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj]
     if src.endswith(".cu"):
-        cmd[1:1] = ["-Xptxas", "-v"] if verbose else []
+        cmd[1:1] = ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
+    if src.endswith(".cu"):
+        _check_split(src, r.stdout + r.stderr)
     if verbose and (r.stdout or r.stderr):
         sys.stderr.write(r.stdout + r.stderr)
     return obj

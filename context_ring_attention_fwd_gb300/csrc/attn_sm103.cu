@@ -18,6 +18,8 @@
 //              each visited shard into a 2-stage shared-memory ring
 //              (the ring's send/receive becomes this double-buffered walk)
 //   warp  9    a single thread issues every tcgen05.mma
+//   warps 10-11 idle (they complete the third warpgroup, which gives its
+//              registers to the softmax warpgroups through setmaxnreg)
 // TMEM (512 columns): S_0 | S_1 | O_0 | O_1.  S_t = Q_t K^T lands in TMEM
 // (fp32); the softmax warps read it with tcgen05.ld, write P (bf16 pairs)
 // back over S_t, and the MMA thread issues O_t += P V with P taken from TMEM.
@@ -48,11 +50,36 @@ constexpr int kBM = 128;        // query rows per tile = TMEM lanes
 constexpr int kBN = 128;        // key rows per K/V tile
 constexpr int kQTiles = 2;      // query tiles per work item
 constexpr int kStages = 2;      // K/V ring depth
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;   // three warpgroups
+constexpr int kLaunchRegs = 168;  // registers per thread at launch (checked by the build)
+constexpr int kSoftmaxRegs = 200; // softmax warpgroups after setmaxnreg.inc
+constexpr int kControlRegs = 96;  // producer / MMA warpgroup after setmaxnreg.dec
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch's register pool");
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
+// Tuning switches (both give the same result up to rounding):
+//  CPRING_FUSED_NOMAX      fused forward only: after the first tile, skip the
+//                          row max and redo a tile only if its row sum shows
+//                          exponentials above 2^64 (the reference point never
+//                          affects P's relative precision, only its range).
+//  CPRING_PACKED_F32X2     fast pass: scale-and-shift and row sum with the
+//                          paired fp32 FMA / ADD (two elements per instruction).
+//  CPRING_SPLIT_LOAD       fast pass: read the second half of S from TMEM
+//                          while the first half's exponentials run.
+#ifndef CPRING_FUSED_NOMAX
+#define CPRING_FUSED_NOMAX 1
+#endif
+#ifndef CPRING_PACKED_F32X2
+#define CPRING_PACKED_F32X2 1
+#endif
+#ifndef CPRING_SPLIT_LOAD
+#define CPRING_SPLIT_LOAD 0
+#endif
+constexpr int kPReadyCount = 128;
+constexpr float kOverflowGuard = 18446744073709551616.0f;  // 2^64
 constexpr unsigned long long kTimeoutNs = 4000000000ull;  // per wait
 
 template <int D>
@@ -142,7 +169,7 @@ __device__ __forceinline__ void tile_keys(const KParams& p, int f, int& ks, int&
 // with h(q) = q (causal) or doc_end(q) - 1: every key of that interval is
 // seen by at least one row of the tile, so the K/V tiles it touches are
 // exactly the tiles holding a visible (q, k).
-__device__ void decode_item(const KParams& p, int n_docs, int w, Item& it) {
+__device__ __forceinline__ void decode_item(const KParams& p, int n_docs, int w, Item& it) {
   const int BH = p.B * p.H;
   const int slots = p.n_qshards * p.pairs_per_shard;
   const int g = slots - 1 - w / BH;
@@ -237,6 +264,159 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity,
   }
 }
 
+// ---------------------------------------------------------------- softmax pieces
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// This thread's 128 scores of the S tile (one TMEM lane), with columns
+// outside [c_lo, c_hi] set to -inf.
+__device__ __forceinline__ void load_scores(uint32_t tS, int c_lo, int c_hi,
+                                            uint32_t (&sv)[4][32]) {
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch) ptx::tmem_ld32(tS + ch * 32, sv[ch]);
+  ptx::tmem_wait_ld();
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch) ptx::reg_fence(sv[ch]);
+  if (c_lo > 0 || c_hi < kBN - 1) {
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+      for (int x = 0; x < 32; ++x) {
+        const int cc = ch * 32 + x;
+        if (cc < c_lo || cc > c_hi) sv[ch][x] = __float_as_uint(-INFINITY);
+      }
+  }
+}
+
+__device__ __forceinline__ float row_max(const uint32_t (&sv)[4][32]) {
+  float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+    for (int x = 0; x < 32; x += 2)
+      m[ch] = max3(m[ch], __uint_as_float(sv[ch][x]), __uint_as_float(sv[ch][x + 1]));
+  return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+}
+
+// P = 2^(s * sc - base) packed as bf16 pairs (P[2c] low, P[2c+1] high), its
+// row sum, and the raw row max of the scores.
+__device__ __forceinline__ void exponentials(const uint32_t (&sv)[4][32], float sc, float base,
+                                             uint32_t (&pk)[2][32], float& lsum, float& mx) {
+  float ls[4] = {0.f, 0.f, 0.f, 0.f};
+  float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+    for (int x = 0; x < 16; ++x) {
+      const float s0 = __uint_as_float(sv[ch][2 * x]);
+      const float s1 = __uint_as_float(sv[ch][2 * x + 1]);
+      m[ch] = max3(m[ch], s0, s1);
+      const float p0 = ptx::ex2(fmaf(s0, sc, -base));
+      const float p1 = ptx::ex2(fmaf(s1, sc, -base));
+      ls[ch] += p0 + p1;
+      pk[ch >> 1][(ch & 1) * 16 + x] = ptx::pack_bf16(p0, p1);
+    }
+  lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+  mx = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+}
+
+// Two exponent arguments s * sc - base at once (paired fp32 FMA).
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float sc,
+                                     float nb) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\tmov.b64 rc, {%5, %5};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(sc), "f"(nb));
+}
+// acc (two fp32 lanes) += (p0, p1) with one paired add.
+__device__ __forceinline__ void add2(uint64_t& acc, float p0, float p1) {
+  asm("{\n\t.reg .b64 rp;\n\tmov.b64 rp, {%1, %2};\n\tadd.rn.f32x2 %0, %0, rp;\n\t}"
+      : "+l"(acc)
+      : "f"(p0), "f"(p1));
+}
+__device__ __forceinline__ float sum2(uint64_t acc) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(acc));
+  return lo + hi;
+}
+
+// P for two 32-column chunks of S against `base`, into pk row `half`.
+__device__ __forceinline__ void exp_chunks(const uint32_t (&sv)[4][32], int half, float sc,
+                                           float base, uint32_t (&pk)[2][32], uint64_t& acc,
+                                           float& ls) {
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc) {
+    const int ch = 2 * half + cc;
+#pragma unroll
+    for (int x = 0; x < 16; ++x) {
+      const float s0 = __uint_as_float(sv[ch][2 * x]);
+      const float s1 = __uint_as_float(sv[ch][2 * x + 1]);
+      float e0, e1;
+      if (CPRING_PACKED_F32X2) {
+        fma2(e0, e1, s0, s1, sc, -base);
+      } else {
+        e0 = fmaf(s0, sc, -base);
+        e1 = fmaf(s1, sc, -base);
+      }
+      const float p0 = ptx::ex2(e0);
+      const float p1 = ptx::ex2(e1);
+      if (CPRING_PACKED_F32X2) {
+        add2(acc, p0, p1);
+      } else {
+        ls += p0 + p1;
+      }
+      pk[half][cc * 16 + x] = ptx::pack_bf16(p0, p1);
+    }
+  }
+}
+
+// Masks columns outside [c_lo, c_hi] of chunks 2*half, 2*half+1.
+__device__ __forceinline__ void mask_chunks(uint32_t (&sv)[4][32], int half, int c_lo, int c_hi) {
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+    for (int x = 0; x < 32; ++x) {
+      const int col = (2 * half + cc) * 32 + x;
+      if (col < c_lo || col > c_hi) sv[2 * half + cc][x] = __float_as_uint(-INFINITY);
+    }
+}
+
+// The common case of the fused kernel: load this lane's S row (in two
+// halves, the second in flight while the first is exponentiated), mask it,
+// and form P and its row sum against the current reference.  No row max.
+__device__ __forceinline__ void fast_pass(uint32_t tS, int c_lo, int c_hi, float sc, float base,
+                                          uint32_t (&sv)[4][32], uint32_t (&pk)[2][32],
+                                          float& lsum) {
+  const bool need_mask = (c_lo > 0 || c_hi < kBN - 1);
+  uint64_t acc = 0;  // two fp32 zeros
+  float ls = 0.f;
+  if (CPRING_SPLIT_LOAD) {
+    ptx::tmem_ld32(tS, sv[0]);
+    ptx::tmem_ld32(tS + 32, sv[1]);
+    ptx::tmem_wait_ld();
+    ptx::reg_fence(sv[0]);
+    ptx::reg_fence(sv[1]);
+    ptx::tmem_ld32(tS + 64, sv[2]);
+    ptx::tmem_ld32(tS + 96, sv[3]);
+    if (need_mask) mask_chunks(sv, 0, c_lo, c_hi);
+    exp_chunks(sv, 0, sc, base, pk, acc, ls);
+    ptx::tmem_wait_ld();
+    ptx::reg_fence(sv[2]);
+    ptx::reg_fence(sv[3]);
+    if (need_mask) mask_chunks(sv, 1, c_lo, c_hi);
+    exp_chunks(sv, 1, sc, base, pk, acc, ls);
+  } else {
+    load_scores(tS, c_lo, c_hi, sv);
+    exp_chunks(sv, 0, sc, base, pk, acc, ls);
+    exp_chunks(sv, 1, sc, base, pk, acc, ls);
+  }
+  lsum = CPRING_PACKED_F32X2 ? sum2(acc) : ls;
+}
+
 // ---------------------------------------------------------------- kernel
 template <int D, bool kPartial>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -274,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < kQTiles; ++t) {
       ptx::mbar_init(bar(kSFull + t), 1);
-      ptx::mbar_init(bar(kPReady + t), 128);
+      ptx::mbar_init(bar(kPReady + t), kPReadyCount);
       ptx::mbar_init(bar(kOBar + t), 1);
     }
     ptx::mbar_init(bar(kDrain), 1);
@@ -293,7 +473,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = gridDim.x;
   const int c = blockIdx.x;
 
-  if (warp == kProducerWarp) {
+  if (warp >= kProducerWarp) {
+   // the third warpgroup gives registers away, then splits into its roles
+   ptx::setmaxnreg_dec<kControlRegs>();
+   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       ptx::tma_prefetch_desc(&tmap_q);
@@ -309,7 +492,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it.F_lo > it.F_hi) continue;
         if (!wait1(bar(kQEmpty), (q_iter & 1u) ^ 1u, abort_flag, p)) { ok = false; break; }
         ptx::mbar_arrive_expect_tx(bar(kQFull), kQTiles * Lay::kTileBytes);
+#pragma unroll
         for (int t = 0; t < kQTiles; ++t)
+#pragma unroll
           for (int pn = 0; pn < Lay::kPanels; ++pn)
             ptx::tma_load_4d(sbase + Lay::kQOff + t * Lay::kTileBytes + pn * Lay::kPanelBytes,
                              &tmap_q, bar(kQFull), pn * 64, it.h, it.q0[t], it.b);
@@ -347,14 +532,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == kMmaWarp) {
+   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(kBM, kBN, false);
       constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kBM, D, true);
       uint32_t kv_iter = 0, q_iter = 0;
-      uint32_t p_cnt[kQTiles] = {0u, 0u};
+      uint32_t p_cnt0 = 0, p_cnt1 = 0;
       bool ok = true;
+      // O_t (+)= P_t V: P_t from TMEM, V (MN-major) from the given stage.
+      auto issue_pv = [&](int t, uint32_t st, bool first) {
+        const uint32_t vbase = sbase + Lay::kVOff + st * Lay::kTileBytes;
+#pragma unroll
+        for (int s = 0; s < kBN / 16; ++s) {
+          const uint64_t bdesc = ptx::smem_desc_sw128(vbase + s * 16 * 128, Lay::kPanelBytes, 1024);
+          ptx::mma_ts(tmem_base + 256 + t * D, tmem_base + t * 128 + s * 8, bdesc, kIdescPV,
+                      (first && s == 0) ? 0u : 1u);
+        }
+        ptx::mma_commit(bar(kOBar + t));
+      };
+      // S_t = Q_t K^T (both K-major, 128-byte swizzled panels of 64 columns).
+      auto issue_s = [&](int t, uint32_t st) {
+        const uint32_t qbase = sbase + Lay::kQOff + t * Lay::kTileBytes;
+        const uint32_t kbase = sbase + Lay::kKOff + st * Lay::kTileBytes;
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s) {
+          const uint32_t off = (s >> 2) * Lay::kPanelBytes + (s & 3) * 32;
+          const uint64_t adesc = ptx::smem_desc_sw128(qbase + off, 16, 1024);
+          const uint64_t bdesc = ptx::smem_desc_sw128(kbase + off, 16, 1024);
+          ptx::mma_ss(tmem_base + t * 128, adesc, bdesc, kIdescQK, s > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(bar(kSFull + t));
+      };
       for (int k = 0; ok; ++k) {
         const int w = item_of(k, c, G);
         if (w >= p.n_items) break;
@@ -364,53 +573,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait1(bar(kQFull), q_iter & 1u, abort_flag, p)) { ok = false; break; }
         ++q_iter;
         ptx::tc_fence_after();
-        int pend[kQTiles] = {-1, -1};
-        bool first_pv[kQTiles] = {true, true};
+        bool pend0 = false, pend1 = false;    // an S issued whose PV is still owed
+        bool first0 = true, first1 = true;    // next PV overwrites O
         uint32_t prev_st = 0, prev_ph = 0;
         bool have_prev = false, prev_v_ready = false;
-        for (int f = it.F_lo; f <= it.F_hi && ok; ++f) {
+        // Owed PV of tile t on the previous K/V stage: wait for V and P, issue.
+        auto flush = [&](int t, uint32_t& pc, bool& first) -> bool {
+          if (!prev_v_ready) {
+            if (!wait1(bar(kVFull + prev_st), prev_ph, abort_flag, p)) return false;
+            prev_v_ready = true;
+          }
+          if (!wait1(bar(kPReady + t), pc & 1u, abort_flag, p)) return false;
+          ++pc;
+          ptx::tc_fence_after();
+          issue_pv(t, prev_st, first);
+          first = false;
+          return true;
+        };
+        for (int f = it.F_lo; f <= it.F_hi; ++f) {
           const uint32_t st = kv_iter % kStages;
           const uint32_t ph = (kv_iter / kStages) & 1u;
+          if (pend0) {
+            if (!flush(0, p_cnt0, first0)) { ok = false; break; }
+            pend0 = false;
+          }
           if (!wait1(bar(kKFull + st), ph, abort_flag, p)) { ok = false; break; }
           ptx::tc_fence_after();
-          for (int t = 0; t < kQTiles && ok; ++t) {
-            if (pend[t] >= 0) {
-              // O_t += P_t V(previous tile): P_t from TMEM, V (MN-major) from smem
-              if (!prev_v_ready) {
-                if (!wait1(bar(kVFull + prev_st), prev_ph, abort_flag, p)) { ok = false; break; }
-                prev_v_ready = true;
-              }
-              if (!wait1(bar(kPReady + t), p_cnt[t] & 1u, abort_flag, p)) { ok = false; break; }
-              ++p_cnt[t];
-              ptx::tc_fence_after();
-              const uint32_t vbase = sbase + Lay::kVOff + prev_st * Lay::kTileBytes;
-#pragma unroll
-              for (int s = 0; s < kBN / 16; ++s) {
-                const uint64_t bdesc =
-                    ptx::smem_desc_sw128(vbase + s * 16 * 128, Lay::kPanelBytes, 1024);
-                ptx::mma_ts(tmem_base + 256 + t * D, tmem_base + t * 128 + s * 8, bdesc,
-                            kIdescPV, (first_pv[t] && s == 0) ? 0u : 1u);
-              }
-              first_pv[t] = false;
-              ptx::mma_commit(bar(kOBar + t));
-              pend[t] = -1;
-            }
-            if (f >= it.f_lo[t] && f <= it.f_hi[t]) {
-              // S_t = Q_t K^T (both K-major, 128-byte swizzled panels of 64 columns)
-              const uint32_t qbase = sbase + Lay::kQOff + t * Lay::kTileBytes;
-              const uint32_t kbase = sbase + Lay::kKOff + st * Lay::kTileBytes;
-#pragma unroll
-              for (int s = 0; s < D / 16; ++s) {
-                const uint32_t off = (s >> 2) * Lay::kPanelBytes + (s & 3) * 32;
-                const uint64_t adesc = ptx::smem_desc_sw128(qbase + off, 16, 1024);
-                const uint64_t bdesc = ptx::smem_desc_sw128(kbase + off, 16, 1024);
-                ptx::mma_ss(tmem_base + t * 128, adesc, bdesc, kIdescQK, s > 0 ? 1u : 0u);
-              }
-              ptx::mma_commit(bar(kSFull + t));
-              pend[t] = f;
-            }
+          if (f >= it.f_lo[0] && f <= it.f_hi[0]) {
+            issue_s(0, st);
+            pend0 = true;
           }
-          if (!ok) break;
+          if (pend1) {
+            if (!flush(1, p_cnt1, first1)) { ok = false; break; }
+            pend1 = false;
+          }
+          if (f >= it.f_lo[1] && f <= it.f_hi[1]) {
+            issue_s(1, st);
+            pend1 = true;
+          }
           ptx::mma_commit(bar(kKEmpty + st));                      // K(f) read by every S
           if (have_prev) ptx::mma_commit(bar(kVEmpty + prev_st));  // V(f-1) read by every PV
           prev_st = st;
@@ -421,34 +621,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         ptx::mma_commit(bar(kQEmpty));  // every S of this item has been issued
-        for (int t = 0; t < kQTiles && ok; ++t) {
-          if (pend[t] < 0) continue;
-          if (!prev_v_ready) {
-            if (!wait1(bar(kVFull + prev_st), prev_ph, abort_flag, p)) { ok = false; break; }
-            prev_v_ready = true;
-          }
-          if (!wait1(bar(kPReady + t), p_cnt[t] & 1u, abort_flag, p)) { ok = false; break; }
-          ++p_cnt[t];
-          ptx::tc_fence_after();
-          const uint32_t vbase = sbase + Lay::kVOff + prev_st * Lay::kTileBytes;
-#pragma unroll
-          for (int s = 0; s < kBN / 16; ++s) {
-            const uint64_t bdesc =
-                ptx::smem_desc_sw128(vbase + s * 16 * 128, Lay::kPanelBytes, 1024);
-            ptx::mma_ts(tmem_base + 256 + t * D, tmem_base + t * 128 + s * 8, bdesc, kIdescPV,
-                        (first_pv[t] && s == 0) ? 0u : 1u);
-          }
-          first_pv[t] = false;
-          ptx::mma_commit(bar(kOBar + t));
-          pend[t] = -1;
+        if (pend0) {
+          if (!flush(0, p_cnt0, first0)) { ok = false; break; }
         }
-        if (ok && have_prev) ptx::mma_commit(bar(kVEmpty + prev_st));
+        if (pend1) {
+          if (!flush(1, p_cnt1, first1)) { ok = false; break; }
+        }
+        if (have_prev) ptx::mma_commit(bar(kVEmpty + prev_st));
       }
       // Wait until every MMA this thread issued has finished.
       ptx::mma_commit(bar(kDrain));
       wait1(bar(kDrain), 0u, abort_flag, p, false);
     }
+   }
   } else {
+    ptx::setmaxnreg_inc<kSoftmaxRegs>();
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;  // query tile of this warpgroup
     const int wq = warp & 3;  // TMEM lane quarter
@@ -464,10 +651,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (w >= p.n_items) break;
       Item it;
       decode_item(p, n_docs, w, it);
-      const int rows = it.rows[t];
+      // this warpgroup's tile (selects keep the item in registers)
+      const int rows = t ? it.rows[1] : it.rows[0];
+      const int f_lo = t ? it.f_lo[1] : it.f_lo[0];
+      const int f_hi = t ? it.f_hi[1] : it.f_hi[0];
       if (rows == 0) continue;
       const bool row_valid = row_in_tile < rows;
-      const int r = it.q0[t] + row_in_tile;
+      const int r = (t ? it.q0[1] : it.q0[0]) + row_in_tile;
       int klo_r = 0, khi_r = -1;
       if (row_valid) {
         const int2 ds = doc_span(p, n_docs, r);
@@ -476,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int rloc = r - it.i * p.L;
       const size_t mrow = (static_cast<size_t>(it.b) * p.H + it.h) * p.L + rloc;
-      if (it.f_lo[t] > it.f_hi[t]) {
+      if (f_lo > f_hi) {
         // No visible key for the whole tile (a skipped step): empty partial.
         if (kPartial && row_valid) {
           float4* o4 = reinterpret_cast<float4*>(
@@ -489,61 +679,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       float m_used = -INFINITY, m_true = -INFINITY, l_run = 0.f;
-      for (int f = it.f_lo[t]; f <= it.f_hi[t]; ++f) {
+      for (int f = f_lo; f <= f_hi; ++f) {
         if (!wait_warp(bar(kSFull + t), s_cnt & 1u, abort_flag, p)) { ok = false; break; }
         ++s_cnt;
         ptx::tc_fence_after();
-        uint32_t sv[4][32];
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) ptx::tmem_ld32(tS + ch * 32, sv[ch]);
-        ptx::tmem_wait_ld();
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) ptx::reg_fence(sv[ch]);
         int ks, ke;
         tile_keys(p, f, ks, ke);
         const int c_lo = klo_r - ks;
         const int c_hi = min(khi_r, ke - 1) - ks;
-        if (c_lo > 0 || c_hi < kBN - 1) {
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch)
-#pragma unroll
-            for (int x = 0; x < 32; ++x) {
-              const int cc = ch * 32 + x;
-              if (cc < c_lo || cc > c_hi) sv[ch][x] = __float_as_uint(-INFINITY);
-            }
-        }
-        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          mx0 = fmaxf(mx0, __uint_as_float(sv[0][x]));
-          mx1 = fmaxf(mx1, __uint_as_float(sv[1][x]));
-          mx2 = fmaxf(mx2, __uint_as_float(sv[2][x]));
-          mx3 = fmaxf(mx3, __uint_as_float(sv[3][x]));
-        }
-        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sc;
-        m_true = fmaxf(m_true, m_tile);
+        uint32_t sv[4][32];
+        uint32_t pk[2][32];
+        float lsum, mx;
         float alpha = 1.f;
         bool rescale_o = false;
-        if (m_tile > m_used + kRescaleLog2) {
-          rescale_o = (m_used != -INFINITY);
-          alpha = rescale_o ? ptx::ex2(m_used - m_tile) : 0.f;
-          l_run *= alpha;
-          m_used = m_tile;
-        }
-        const float base = (m_used == -INFINITY) ? 0.f : m_used;
-        float ls0 = 0.f, ls1 = 0.f;
-        uint32_t pk[2][32];
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch)
-#pragma unroll
-          for (int x = 0; x < 16; ++x) {
-            const float p0 = ptx::ex2(fmaf(__uint_as_float(sv[ch][2 * x]), sc, -base));
-            const float p1 = ptx::ex2(fmaf(__uint_as_float(sv[ch][2 * x + 1]), sc, -base));
-            ls0 += p0;
-            ls1 += p1;
-            pk[ch >> 1][(ch & 1) * 16 + x] = ptx::pack_bf16(p0, p1);
+        const bool fast = CPRING_FUSED_NOMAX && !kPartial &&
+                          !__any_sync(0xffffffffu, m_used == -INFINITY);
+        if (fast) {
+          fast_pass(tS, c_lo, c_hi, sc, m_used, sv, pk, lsum);
+          const bool redo = !(lsum <= kOverflowGuard);
+          if (__any_sync(0xffffffffu, redo)) {
+            // Rare: exponentials ran past 2^64.  Reload S (P is not yet
+            // written), move the reference to this tile's max and let every
+            // lane recompute (lanes that keep their reference get the same P).
+            load_scores(tS, c_lo, c_hi, sv);
+            const float m_tile = row_max(sv) * sc;
+            if (redo && m_tile > m_used) {
+              rescale_o = true;
+              alpha = ptx::ex2(m_used - m_tile);
+              l_run *= alpha;
+              m_used = m_tile;
+            }
+            exponentials(sv, sc, m_used, pk, lsum, mx);
           }
-        l_run += ls0 + ls1;
+        } else {
+        load_scores(tS, c_lo, c_hi, sv);
+        if (__any_sync(0xffffffffu, m_used == -INFINITY)) {
+          // Some row of this warp has no reference yet: row max first.
+          mx = row_max(sv);
+          const float m_tile = mx * sc;
+          m_true = fmaxf(m_true, m_tile);
+          if (m_tile > m_used + kRescaleLog2) {
+            rescale_o = (m_used != -INFINITY);
+            alpha = rescale_o ? ptx::ex2(m_used - m_tile) : 0.f;
+            l_run *= alpha;
+            m_used = m_tile;
+          }
+          exponentials(sv, sc, (m_used == -INFINITY) ? 0.f : m_used, pk, lsum, mx);
+        } else {
+          // Exponentials against the current reference; the row max is
+          // taken in the same pass and only forces a redo (rare) when it
+          // moved more than 2^8 above the reference.
+          {
+            exponentials(sv, sc, m_used, pk, lsum, mx);
+            const float m_tile = mx * sc;
+            m_true = fmaxf(m_true, m_tile);
+            const bool redo = m_tile > m_used + kRescaleLog2;
+            if (__any_sync(0xffffffffu, redo)) {
+              if (redo) {
+                rescale_o = true;
+                alpha = ptx::ex2(m_used - m_tile);
+                l_run *= alpha;
+                m_used = m_tile;
+              }
+              load_scores(tS, c_lo, c_hi, sv);  // S is still in TMEM: P not yet written
+              exponentials(sv, sc, m_used, pk, lsum, mx);
+            }
+          }
+        }
+        }
+        l_run += lsum;
         ptx::tmem_st32(tS, pk[0]);
         ptx::tmem_st32(tS + 32, pk[1]);
         if (__any_sync(0xffffffffu, rescale_o)) {
