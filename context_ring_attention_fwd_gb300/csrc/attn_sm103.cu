@@ -53,7 +53,7 @@ constexpr int kStages = 2;      // K/V ring depth
 constexpr int kThreads = 384;   // three warpgroups
 constexpr int kLaunchRegs = 168;  // registers per thread at launch (checked by the build)
 constexpr int kSoftmaxRegs = 200; // softmax warpgroups after setmaxnreg.inc
-constexpr int kControlRegs = 96;  // producer / MMA warpgroup after setmaxnreg.dec
+constexpr int kControlRegs = 104; // producer / MMA warpgroup after setmaxnreg.dec
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch's register pool");
 constexpr int kProducerWarp = 8;
@@ -540,27 +540,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t kv_iter = 0, q_iter = 0;
       uint32_t p_cnt0 = 0, p_cnt1 = 0;
       bool ok = true;
+      // Shared-memory descriptors of every operand tile, built once.  A k-step
+      // moves the start address (bits 0-13, in 16-byte units) by a constant,
+      // so each MMA needs one add: this thread issues 32 MMAs per K/V tile
+      // while sharing its scheduler with two softmax warps.
+      // (Shared addresses stay below 2^18 bytes, so the 14-bit start field
+      // never carries into the offsets above it.)
+      const uint64_t d_qk = ptx::smem_desc_sw128(sbase, 16, 1024);
+      const uint64_t d_v = ptx::smem_desc_sw128(sbase, Lay::kPanelBytes, 1024);
       // O_t (+)= P_t V: P_t from TMEM, V (MN-major) from the given stage.
       auto issue_pv = [&](int t, uint32_t st, bool first) {
-        const uint32_t vbase = sbase + Lay::kVOff + st * Lay::kTileBytes;
+        const uint64_t dv = d_v + ((Lay::kVOff + st * Lay::kTileBytes) >> 4);
 #pragma unroll
         for (int s = 0; s < kBN / 16; ++s) {
-          const uint64_t bdesc = ptx::smem_desc_sw128(vbase + s * 16 * 128, Lay::kPanelBytes, 1024);
-          ptx::mma_ts(tmem_base + 256 + t * D, tmem_base + t * 128 + s * 8, bdesc, kIdescPV,
+          ptx::mma_ts(tmem_base + 256 + t * D, tmem_base + t * 128 + s * 8,
+                      dv + static_cast<uint64_t>((s * 16 * 128) >> 4), kIdescPV,
                       (first && s == 0) ? 0u : 1u);
         }
         ptx::mma_commit(bar(kOBar + t));
       };
       // S_t = Q_t K^T (both K-major, 128-byte swizzled panels of 64 columns).
       auto issue_s = [&](int t, uint32_t st) {
-        const uint32_t qbase = sbase + Lay::kQOff + t * Lay::kTileBytes;
-        const uint32_t kbase = sbase + Lay::kKOff + st * Lay::kTileBytes;
+        const uint64_t dq = d_qk + ((Lay::kQOff + t * Lay::kTileBytes) >> 4);
+        const uint64_t dk = d_qk + ((Lay::kKOff + st * Lay::kTileBytes) >> 4);
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
-          const uint32_t off = (s >> 2) * Lay::kPanelBytes + (s & 3) * 32;
-          const uint64_t adesc = ptx::smem_desc_sw128(qbase + off, 16, 1024);
-          const uint64_t bdesc = ptx::smem_desc_sw128(kbase + off, 16, 1024);
-          ptx::mma_ss(tmem_base + t * 128, adesc, bdesc, kIdescQK, s > 0 ? 1u : 0u);
+          const uint64_t step = static_cast<uint64_t>(((s >> 2) * Lay::kPanelBytes + (s & 3) * 32) >> 4);
+          ptx::mma_ss(tmem_base + t * 128, dq + step, dk + step, kIdescQK, s > 0 ? 1u : 0u);
         }
         ptx::mma_commit(bar(kSFull + t));
       };

@@ -44,8 +44,36 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
       : "memory");
 }
 
+// How a wait polls its mbarrier (a tuning switch; every mode is bounded by
+// the caller's loop):
+//   0  mbarrier.try_wait (the hardware may suspend the thread for a while)
+//   1  mbarrier.try_wait with a suspend-time hint of CPRING_WAIT_HINT_NS
+//   2  mbarrier.test_wait (never suspends)
+#ifndef CPRING_WAIT_MODE
+#define CPRING_WAIT_MODE 0
+#endif
+#ifndef CPRING_WAIT_HINT_NS
+#define CPRING_WAIT_HINT_NS 1000000
+#endif
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
+#if CPRING_WAIT_MODE == 1
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "n"(CPRING_WAIT_HINT_NS)
+      : "memory");
+#elif CPRING_WAIT_MODE == 2
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+#else
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
@@ -53,6 +81,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "=r"(ok)
       : "r"(bar), "r"(parity)
       : "memory");
+#endif
   return ok != 0;
 }
 
