@@ -41,6 +41,7 @@ _SIGS = {
     "cp_get_last_status": [_vp],
     "cp_status_string": [_i],
     "cp_launch_counts": [ctypes.POINTER(_i64)],
+    "cp_test_set_wait_fault": [_i, _i64],
 }
 
 
@@ -68,7 +69,7 @@ def lib() -> ctypes.CDLL:
                 fn.argtypes = argtypes
                 if name == "cp_status_string":
                     fn.restype = ctypes.c_char_p
-                elif name == "cp_launch_counts":
+                elif name in ("cp_launch_counts", "cp_test_set_wait_fault"):
                     fn.restype = None
                 else:
                     fn.restype = _i
@@ -246,6 +247,12 @@ def cp_get_last_status(stream=None) -> int:
 
 def cp_status_string(status: int) -> str:
     return lib().cp_status_string(int(status)).decode()
+
+
+def test_set_wait_fault(drop_first_k_tile: bool, wait_limit_ns: int = 0) -> None:
+    """Test hook: make CTA 0 of later tensor-core launches skip its first K
+    tile so that a bounded device wait runs out (see include/cpring.h)."""
+    lib().cp_test_set_wait_fault(int(bool(drop_first_k_tile)), int(wait_limit_ns))
 
 
 def launch_counts():

@@ -38,6 +38,7 @@
 #include <climits>
 #include <cmath>
 #include <cstdio>
+#include <atomic>
 #include <mutex>
 
 #include "internal.h"
@@ -130,6 +131,7 @@ struct KParams {
   float* l_part;
   int* err;
   unsigned long long timeout_ns;
+  int fault_drop_k;  // test hook: CTA 0 never loads its first K tile
 };
 
 struct Item {
@@ -482,7 +484,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tma_prefetch_desc(&tmap_q);
       ptx::tma_prefetch_desc(&tmap_k);
       ptx::tma_prefetch_desc(&tmap_v);
-      uint32_t kv_iter = 0, q_iter = 0, k_loads = 0, v_loads = 0;
+      uint32_t kv_iter = 0, q_iter = 0;
+      // Loads started into each stage: the n-th one completes phase n - 1.
+      uint32_t k_armed0 = 0, k_armed1 = 0, v_armed0 = 0, v_armed1 = 0;
+      bool dropped = false;
       bool ok = true;
       for (int k = 0; ok; ++k) {
         const int w = item_of(k, c, G);
@@ -505,32 +510,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           int ks, ke;
           tile_keys(p, f, ks, ke);
           if (!wait1(bar(kKEmpty + st), ph ^ 1u, abort_flag, p)) { ok = false; break; }
-          ptx::mbar_arrive_expect_tx(bar(kKFull + st), Lay::kTileBytes);
-          for (int pn = 0; pn < Lay::kPanels; ++pn)
-            ptx::tma_load_4d(sbase + Lay::kKOff + st * Lay::kTileBytes + pn * Lay::kPanelBytes,
-                             &tmap_k, bar(kKFull + st), pn * 64, it.h, ks, it.b);
-          ++k_loads;
+          if (p.fault_drop_k && c == 0 && !dropped) {
+            // Test hook: this K tile is never loaded, so the MMA thread's
+            // bounded wait for it runs out and the CTA takes its abort path.
+            dropped = true;
+          } else {
+            ptx::mbar_arrive_expect_tx(bar(kKFull + st), Lay::kTileBytes);
+            for (int pn = 0; pn < Lay::kPanels; ++pn)
+              ptx::tma_load_4d(sbase + Lay::kKOff + st * Lay::kTileBytes + pn * Lay::kPanelBytes,
+                               &tmap_k, bar(kKFull + st), pn * 64, it.h, ks, it.b);
+            if (st == 0) ++k_armed0; else ++k_armed1;
+          }
           if (!wait1(bar(kVEmpty + st), ph ^ 1u, abort_flag, p)) { ok = false; break; }
           ptx::mbar_arrive_expect_tx(bar(kVFull + st), Lay::kTileBytes);
           for (int pn = 0; pn < Lay::kPanels; ++pn)
             ptx::tma_load_4d(sbase + Lay::kVOff + st * Lay::kTileBytes + pn * Lay::kPanelBytes,
                              &tmap_v, bar(kVFull + st), pn * 64, it.h, ks, it.b);
-          ++v_loads;
+          if (st == 0) ++v_armed0; else ++v_armed1;
           ++kv_iter;
         }
       }
       // Let every copy this thread started land before the CTA can exit.
       if (q_iter > 0) wait1(bar(kQFull), (q_iter - 1) & 1u, abort_flag, p, false);
-      for (uint32_t s = 0; s < kStages; ++s) {
-        if (k_loads > s) {  // loads into stage s: (k_loads - 1 - s) / kStages + 1
-          const uint32_t uses = (k_loads - 1 - s) / kStages + 1;
-          wait1(bar(kKFull + s), (uses - 1) & 1u, abort_flag, p, false);
-        }
-        if (v_loads > s) {
-          const uint32_t uses = (v_loads - 1 - s) / kStages + 1;
-          wait1(bar(kVFull + s), (uses - 1) & 1u, abort_flag, p, false);
-        }
-      }
+      if (k_armed0 > 0) wait1(bar(kKFull + 0), (k_armed0 - 1) & 1u, abort_flag, p, false);
+      if (k_armed1 > 0) wait1(bar(kKFull + 1), (k_armed1 - 1) & 1u, abort_flag, p, false);
+      if (v_armed0 > 0) wait1(bar(kVFull + 0), (v_armed0 - 1) & 1u, abort_flag, p, false);
+      if (v_armed1 > 0) wait1(bar(kVFull + 1), (v_armed1 - 1) & 1u, abort_flag, p, false);
     }
    } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -884,6 +889,10 @@ bool make_map(CUtensorMap* m, const void* base, int B, int S, int H, int D) {
   return r == CUDA_SUCCESS;
 }
 
+// Test hook state (see cp_test_set_wait_fault).
+std::atomic<int> g_fault_drop_k{0};
+std::atomic<unsigned long long> g_wait_limit_ns{kTimeoutNs};
+
 template <int D, bool kPartial>
 cudaError_t launch_t(const AttnArgs& a, cudaStream_t stream) {
   using Lay = Layout<D>;
@@ -926,7 +935,8 @@ cudaError_t launch_t(const AttnArgs& a, cudaStream_t stream) {
   p.l_part = a.l_part;
   p.err = device_error_word();
   if (!p.err) return cudaErrorInvalidValue;
-  p.timeout_ns = kTimeoutNs;
+  p.timeout_ns = g_wait_limit_ns.load();
+  p.fault_drop_k = g_fault_drop_k.load();
   const int grid = static_cast<int>(std::min<long long>(items, sm_count()));
   if (grid <= 0) return cudaSuccess;
   kern<<<grid, kThreads, Lay::kAlloc, stream>>>(mq, mk, mv, p);
@@ -944,3 +954,9 @@ cudaError_t launch_attn_bf16(const AttnArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace cpring
+
+extern "C" void cp_test_set_wait_fault(int drop_first_k_tile, long long wait_limit_ns) {
+  cpring::g_fault_drop_k.store(drop_first_k_tile ? 1 : 0);
+  cpring::g_wait_limit_ns.store(wait_limit_ns > 0 ? static_cast<unsigned long long>(wait_limit_ns)
+                                                  : cpring::kTimeoutNs);
+}

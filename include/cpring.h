@@ -217,6 +217,17 @@ cp_status cp_get_last_status(cudaStream_t stream);
 /* A static, human-readable name for a status code. */
 const char* cp_status_string(cp_status status);
 
+/*
+ * TEST HOOK (failure detection without a GPU fault).  With drop_first_k_tile
+ * != 0, the next tensor-core launches have CTA 0 skip loading its first K
+ * tile, so one of its bounded device waits runs out: the CTA drains its own
+ * copies and MMAs, frees TMEM, leaves its outputs unwritten and raises
+ * CP_ERR_TIMEOUT in the device error word.  wait_limit_ns sets the per-wait
+ * limit of later launches (<= 0 restores the default of 4 s).  Call with
+ * (0, 0) to return to normal operation.  Not thread-safe; for tests only.
+ */
+void cp_test_set_wait_fault(int drop_first_k_tile, long long wait_limit_ns);
+
 /* Number of tcgen05 kernel launches, fp32 kernel launches, merge/finalize
  * launches and doc-scan launches made by this process so far (host-side
  * counters, for launch accounting in benchmarks). */

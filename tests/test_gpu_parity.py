@@ -229,6 +229,29 @@ def test_malformed_doc_offsets_reported():
     assert pkg.cp_get_last_status() == 0
 
 
+def test_bounded_wait_runs_out_and_context_recovers():
+    # A K tile that is never loaded (a flag nothing sets): the MMA thread's
+    # wait gives up after 0.3 s, the CTA drains and exits, the host reads
+    # CP_ERR_TIMEOUT, and the next call on the same context is correct.
+    B, S, H, d, N = 1, 1024, 2, 128, 2
+    q, k, v = inputs.make_qkv(B, S, H, d, seed=17, dtype=torch.bfloat16)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    assert pkg.cp_get_last_status() == 0
+    try:
+        pkg.test_set_wait_fault(True, 300_000_000)
+        out = torch.empty_like(qd)
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=DEV)
+        pkg.cp_ring_attn_fwd(qd, kd, vd, out, lse, N, True)
+        assert pkg.cp_get_last_status() == pkg.STATUS_CODES["CP_ERR_TIMEOUT"]
+    finally:
+        pkg.test_set_wait_fault(False, 0)
+    assert pkg.cp_get_last_status() == 0
+    out, lse = pkg.ring_attn_fwd(qd, kd, vd, N, True)
+    assert pkg.cp_get_last_status() == 0
+    want_o, want_l = ref.attention(_np(q), _np(k), _np(v), True, None)
+    _check_bf16(out, lse, want_o, want_l)
+
+
 def test_native_kernels_launch():
     before = pkg.launch_counts()
     q, k, v = (t.to(DEV) for t in inputs.make_qkv(1, 256, 1, 128, seed=1, dtype=torch.bfloat16))
