@@ -371,6 +371,56 @@ def run_ours(args, w, rank, world, local):
     return line
 
 
+def run_ring_emulation(args, w, local):
+    """Time the ring with explicit per-rank buffers: transfers overlapped on
+    a copy stream, transfers in order on the compute stream, and the fused
+    kernel, on the same inputs.  One JSON line (impl "ring_emulated")."""
+    import context_ring_attention_fwd_gb300 as pkg
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    q, k, v = inputs.make_qkv(w.B, w.S, w.H, w.d, w.seed, w.torch_dtype, w.scale, device=str(dev))
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
+    ws = torch.empty(pkg.cp_ring_emulated_workspace_bytes(w.B, w.S, w.H, w.d, w.n_shards),
+                     dtype=torch.uint8, device=dev)
+    cs = torch.cuda.Stream(device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / args.steps
+
+    recv = []
+    ms_ov = timed(lambda: recv.append(pkg.cp_ring_attn_fwd_emulated(
+        q, k, v, out, lse, w.n_shards, w.causal, ws, stream, cs)))
+    ms_ser = timed(lambda: pkg.cp_ring_attn_fwd_emulated(
+        q, k, v, out, lse, w.n_shards, w.causal, ws, stream, None))
+    ms_fused = timed(lambda: pkg.cp_ring_attn_fwd(q, k, v, out, lse, w.n_shards, w.causal, None,
+                                                  stream))
+    if pkg.cp_get_last_status(stream) != 0:
+        raise RuntimeError("device error in the ring emulation")
+    flops = effective_flops(w, None)
+    moved = int(sum(recv[-1]))
+    return {
+        "metric": METRIC, "impl": "ring_emulated", "unit": UNIT,
+        "value": flops / (ms_ov * 1e-3) / 1e12, "ms_per_step": ms_ov,
+        "ms_transfers_in_order": ms_ser, "ms_fused_kernel": ms_fused,
+        "transfer_time_hidden_ms": ms_ser - ms_ov,
+        "bytes_received_per_step": moved, "bytes_received_per_rank": recv[-1],
+        "steps": args.steps, "warmup": args.warmup, "n_gpus": 1, "dtype": w.dtype,
+        "data": "synthetic", "config": _config(w, None, 1),
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -382,6 +432,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--cpu-rows", type=int, default=128)
+    ap.add_argument("--ring-emulation", action="store_true",
+                    help="time the ring with explicit per-rank buffers instead")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the attention kernel from an ncu capture")
     args = ap.parse_args(argv)
@@ -389,6 +441,11 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_env()
     w = inputs.BY_NAME[args.workload]
+    if args.ring_emulation:
+        line = run_ring_emulation(args, w, local)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
     if args.impl == "reference":
         dist_init(world, "gloo")
         line = run_reference(args, w, rank, world)

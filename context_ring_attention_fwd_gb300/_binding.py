@@ -42,6 +42,9 @@ _SIGS = {
     "cp_status_string": [_i],
     "cp_launch_counts": [ctypes.POINTER(_i64)],
     "cp_test_set_wait_fault": [_i, _i64],
+    "cp_ring_emulated_workspace_bytes": [_i, _i, _i, _i, _i],
+    "cp_ring_attn_fwd_emulated": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _i64,
+                                  _vp, _vp, ctypes.POINTER(_i64)],
 }
 
 
@@ -71,6 +74,8 @@ def lib() -> ctypes.CDLL:
                     fn.restype = ctypes.c_char_p
                 elif name in ("cp_launch_counts", "cp_test_set_wait_fault"):
                     fn.restype = None
+                elif name == "cp_ring_emulated_workspace_bytes":
+                    fn.restype = _i64
                 else:
                     fn.restype = _i
             _lib = handle
@@ -147,6 +152,35 @@ def cp_ring_attn_fwd_noalloc(q, k, v, out, lse, n_shards: int, causal: bool = Tr
     _check("cp_ring_attn_fwd_noalloc", lib().cp_ring_attn_fwd_noalloc(
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, H, d, int(n_shards),
         int(bool(causal)), _ptr(doc_offsets), _stream(stream)))
+
+
+def cp_ring_attn_fwd_emulated(q, k, v, out, lse, n_shards: int, causal: bool = True,
+                              workspace: Optional[torch.Tensor] = None, stream=None,
+                              copy_stream=None):
+    """The ring with explicit per-rank K/V buffers and copy-engine transfers
+    (overlapped on copy_stream, or in order when copy_stream is None).
+    Returns the bytes each rank received.  workspace: a uint8 device tensor
+    of at least cp_ring_emulated_workspace_bytes(...) bytes (allocated here
+    if None)."""
+    B, S, H, d = q.shape
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _need(t, n, torch.bfloat16, (B, S, H, d))
+    _need(lse, "lse", torch.float32, (B, H, S))
+    need = int(lib().cp_ring_emulated_workspace_bytes(B, S, H, d, int(n_shards)))
+    if need < 0:
+        raise CpError("cp_ring_emulated_workspace_bytes", STATUS_CODES["CP_ERR_SHAPE"])
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    recv = (ctypes.c_int64 * int(n_shards))()
+    cs = None if copy_stream is None else _stream(copy_stream)
+    _check("cp_ring_attn_fwd_emulated", lib().cp_ring_attn_fwd_emulated(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, H, d, int(n_shards),
+        int(bool(causal)), _ptr(workspace), int(workspace.numel()), _stream(stream), cs, recv))
+    return list(recv)
+
+
+def cp_ring_emulated_workspace_bytes(B: int, S: int, H: int, d: int, n_shards: int) -> int:
+    return int(lib().cp_ring_emulated_workspace_bytes(B, S, H, d, n_shards))
 
 
 def cp_ring_attn_fwd_f32(q, k, v, out, lse, n_shards: int, causal: bool = True,

@@ -132,6 +132,7 @@ struct KParams {
   int* err;
   unsigned long long timeout_ns;
   int fault_drop_k;  // test hook: CTA 0 never loads its first K tile
+  int kv_row0;       // key index of row 0 of the K/V tensors (0 unless a block)
 };
 
 struct Item {
@@ -518,14 +519,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_arrive_expect_tx(bar(kKFull + st), Lay::kTileBytes);
             for (int pn = 0; pn < Lay::kPanels; ++pn)
               ptx::tma_load_4d(sbase + Lay::kKOff + st * Lay::kTileBytes + pn * Lay::kPanelBytes,
-                               &tmap_k, bar(kKFull + st), pn * 64, it.h, ks, it.b);
+                               &tmap_k, bar(kKFull + st), pn * 64, it.h, ks - p.kv_row0, it.b);
             if (st == 0) ++k_armed0; else ++k_armed1;
           }
           if (!wait1(bar(kVEmpty + st), ph ^ 1u, abort_flag, p)) { ok = false; break; }
           ptx::mbar_arrive_expect_tx(bar(kVFull + st), Lay::kTileBytes);
           for (int pn = 0; pn < Lay::kPanels; ++pn)
             ptx::tma_load_4d(sbase + Lay::kVOff + st * Lay::kTileBytes + pn * Lay::kPanelBytes,
-                             &tmap_v, bar(kVFull + st), pn * 64, it.h, ks, it.b);
+                             &tmap_v, bar(kVFull + st), pn * 64, it.h, ks - p.kv_row0, it.b);
           if (st == 0) ++v_armed0; else ++v_armed1;
           ++kv_iter;
         }
@@ -906,8 +907,9 @@ cudaError_t launch_t(const AttnArgs& a, cudaStream_t stream) {
   if (attr_err != cudaSuccess) return attr_err;
 
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, a.q, a.B, a.S, a.H, D) || !make_map(&mk, a.k, a.B, a.S, a.H, D) ||
-      !make_map(&mv, a.v, a.B, a.S, a.H, D))
+  const int kv_rows = a.kv_rows > 0 ? a.kv_rows : a.S;
+  if (!make_map(&mq, a.q, a.B, a.S, a.H, D) || !make_map(&mk, a.k, a.B, kv_rows, a.H, D) ||
+      !make_map(&mv, a.v, a.B, kv_rows, a.H, D))
     return cudaErrorInvalidValue;
 
   KParams p{};
@@ -918,6 +920,7 @@ cudaError_t launch_t(const AttnArgs& a, cudaStream_t stream) {
   p.L = a.S / a.n_shards;
   p.q_shard = a.q_shard;
   p.k_shard = a.k_shard;
+  p.kv_row0 = a.kv_rows > 0 ? a.kv_row0 : 0;
   p.causal = a.causal;
   p.doc_offsets = a.doc_offsets;
   p.doc_info = a.doc_info;

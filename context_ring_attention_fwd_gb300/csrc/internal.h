@@ -19,6 +19,11 @@ struct AttnArgs {
   int causal;
   const int32_t* doc_offsets;  // device or null
   const int32_t* doc_info;     // device scratch written by the doc scan, or null
+  // K/V layout: by default k and v are the whole sequence [B, S, H, d].  With
+  // kv_rows > 0 they are one block [B, kv_rows, H, d] whose row 0 is the key
+  // kv_row0 of the sequence (a rank's receive buffer in the ring emulation).
+  int kv_rows;
+  int kv_row0;
   // fused outputs
   void* out;
   float* lse;
@@ -45,6 +50,12 @@ cudaError_t launch_merge(float* o_acc, float* m_acc, float* l_acc, const float* 
 cudaError_t launch_finalize(const float* o_acc, const float* m_acc, const float* l_acc, void* out,
                             float* lse, int B, int rows, int H, int d, int out_is_bf16,
                             cudaStream_t stream);
+// Finalize into strided outputs: out row (b, r, h) at b*out_bstride +
+// (r*H + h)*d elements; lse (b, h, r) at b*lse_bstride + h*lse_hstride + r.
+cudaError_t launch_finalize_strided(const float* o_acc, const float* m_acc, const float* l_acc,
+                                    void* out, float* lse, int B, int rows, int H, int d,
+                                    int out_is_bf16, long long out_bstride, long long lse_bstride,
+                                    long long lse_hstride, cudaStream_t stream);
 
 // Host launch counters (index: 0 tcgen05 attention, 1 fp32 attention,
 // 2 merge/finalize, 3 doc scan).

@@ -87,7 +87,8 @@ template <bool kBf16>
 __global__ void __launch_bounds__(kMergeThreads)
     lse_finalize_kernel(const float* __restrict__ o_acc, const float* __restrict__ m_acc,
                         const float* __restrict__ l_acc, void* __restrict__ out,
-                        float* __restrict__ lse, int B, int rows, int H, int d, bool vec4) {
+                        float* __restrict__ lse, int B, int rows, int H, int d, bool vec4,
+                        long long out_bstride, long long lse_bstride, long long lse_hstride) {
   const int lane = threadIdx.x & 31;
   const long long n = static_cast<long long>(B) * rows * H;
   const long long wstride = static_cast<long long>(gridDim.x) * (kMergeThreads / 32);
@@ -101,8 +102,9 @@ __global__ void __launch_bounds__(kMergeThreads)
     const float l = l_acc[mi];
     const float inv = (l > 0.f) ? 1.f / l : 0.f;
     const float* o = o_acc + static_cast<size_t>(w) * d;
+    const size_t orow = static_cast<size_t>(b) * out_bstride + (static_cast<size_t>(row) * H + h) * d;
     if (kBf16) {
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(out) + static_cast<size_t>(w) * d;
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(out) + orow;
       if (vec4) {
         for (int x = lane; x < d / 4; x += 32) {
           const float4 u = reinterpret_cast<const float4*>(o)[x];
@@ -115,7 +117,7 @@ __global__ void __launch_bounds__(kMergeThreads)
         for (int x = lane; x < d; x += 32) dst[x] = __float2bfloat16_rn(o[x] * inv);
       }
     } else {
-      float* dst = static_cast<float*>(out) + static_cast<size_t>(w) * d;
+      float* dst = static_cast<float*>(out) + orow;
       if (vec4) {
         for (int x = lane; x < d / 4; x += 32) {
           float4 u = reinterpret_cast<const float4*>(o)[x];
@@ -129,7 +131,9 @@ __global__ void __launch_bounds__(kMergeThreads)
         for (int x = lane; x < d; x += 32) dst[x] = o[x] * inv;
       }
     }
-    if (lane == 0) lse[mi] = (l > 0.f) ? m_acc[mi] + logf(l) : -INFINITY;
+    if (lane == 0)
+      lse[static_cast<size_t>(b) * lse_bstride + static_cast<size_t>(h) * lse_hstride + row] =
+          (l > 0.f) ? m_acc[mi] + logf(l) : -INFINITY;
   }
 }
 
@@ -236,21 +240,33 @@ cudaError_t launch_merge(float* o_acc, float* m_acc, float* l_acc, const float* 
   return cudaGetLastError();
 }
 
+cudaError_t launch_finalize_strided(const float* o_acc, const float* m_acc, const float* l_acc,
+                                    void* out, float* lse, int B, int rows, int H, int d,
+                                    int out_is_bf16, long long out_bstride, long long lse_bstride,
+                                    long long lse_hstride, cudaStream_t stream) {
+  const long long n = static_cast<long long>(B) * rows * H;
+  const size_t esz = out_is_bf16 ? 2 : 4;
+  const bool vec4 = (d % 4 == 0) &&
+                    ((reinterpret_cast<uintptr_t>(o_acc) | reinterpret_cast<uintptr_t>(out)) % 16 == 0) &&
+                    ((static_cast<size_t>(out_bstride) * esz) % 16 == 0) &&
+                    ((static_cast<size_t>(d) * esz) % (out_is_bf16 ? 8 : 16) == 0);
+  if (out_is_bf16)
+    lse_finalize_kernel<true><<<grid_for(n), kMergeThreads, 0, stream>>>(
+        o_acc, m_acc, l_acc, out, lse, B, rows, H, d, vec4 && d % 8 == 0, out_bstride, lse_bstride,
+        lse_hstride);
+  else
+    lse_finalize_kernel<false><<<grid_for(n), kMergeThreads, 0, stream>>>(
+        o_acc, m_acc, l_acc, out, lse, B, rows, H, d, vec4, out_bstride, lse_bstride, lse_hstride);
+  count_launch(2);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_finalize(const float* o_acc, const float* m_acc, const float* l_acc, void* out,
                             float* lse, int B, int rows, int H, int d, int out_is_bf16,
                             cudaStream_t stream) {
-  const long long n = static_cast<long long>(B) * rows * H;
-  const bool vec4 = (d % 4 == 0) && ((reinterpret_cast<uintptr_t>(o_acc) |
-                                       reinterpret_cast<uintptr_t>(out)) % 16 == 0);
-  if (out_is_bf16)
-    lse_finalize_kernel<true><<<grid_for(n), kMergeThreads, 0, stream>>>(o_acc, m_acc, l_acc, out,
-                                                                         lse, B, rows, H, d,
-                                                                         vec4 && d % 8 == 0);
-  else
-    lse_finalize_kernel<false><<<grid_for(n), kMergeThreads, 0, stream>>>(o_acc, m_acc, l_acc, out,
-                                                                          lse, B, rows, H, d, vec4);
-  count_launch(2);
-  return cudaGetLastError();
+  return launch_finalize_strided(o_acc, m_acc, l_acc, out, lse, B, rows, H, d, out_is_bf16,
+                                 static_cast<long long>(rows) * H * d,
+                                 static_cast<long long>(H) * rows, rows, stream);
 }
 
 }  // namespace cpring

@@ -218,6 +218,34 @@ cp_status cp_get_last_status(cudaStream_t stream);
 const char* cp_status_string(cp_status status);
 
 /*
+ * The ring with explicit per-rank buffers ("上下文並行（Context Parallelism,
+ * CP）", 線上 Softmax: compute against the held K/V block, then pass it to the
+ * next GPU; "大语言模型并行策略（五）：上下文并行", 通信模式: double-buffered so
+ * the transfer overlaps the computation; 因果掩碼的特殊處理: under causality a
+ * block goes only to the ranks that need it).  Every virtual rank owns a
+ * two-slot K/V receive buffer in `workspace`; at step t rank i holds the block
+ * of rank (i - t) mod N, runs cp_ring_step on it and merges the partial, while
+ * the copy engine moves each held block into the next rank's other slot for
+ * step t + 1.  Same arguments and result as cp_ring_attn_fwd (bf16, d 64 or
+ * 128, no doc_offsets), plus:
+ *  workspace        device, >= cp_ring_emulated_workspace_bytes(...) bytes,
+ *                   256-byte aligned; owned by the caller; contents undefined
+ *                   after the call.
+ *  stream           compute stream.
+ *  copy_stream      stream for the block transfers; NULL runs them in order
+ *                   on `stream` (no overlap).  The call leaves `stream`
+ *                   waiting for every transfer it issued.
+ *  recv_bytes_per_rank  host int64 [n_shards] or NULL: bytes each rank
+ *                   received from its predecessor (K and V).
+ */
+int64_t cp_ring_emulated_workspace_bytes(int B, int S, int H, int d, int n_shards);
+cp_status cp_ring_attn_fwd_emulated(const void* q, const void* k, const void* v, void* out,
+                                    float* lse, int B, int S, int H, int d, int n_shards,
+                                    int causal, void* workspace, int64_t workspace_bytes,
+                                    cudaStream_t stream, cudaStream_t copy_stream,
+                                    int64_t* recv_bytes_per_rank);
+
+/*
  * TEST HOOK (failure detection without a GPU fault).  With drop_first_k_tile
  * != 0, the next tensor-core launches have CTA 0 skip loading its first K
  * tile, so one of its bounded device waits runs out: the CTA drains its own

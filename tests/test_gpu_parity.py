@@ -252,6 +252,34 @@ def test_bounded_wait_runs_out_and_context_recovers():
     _check_bf16(out, lse, want_o, want_l)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("overlap", [True, False])
+@pytest.mark.parametrize("B,S,H,d,N", [(2, 1024, 2, 128, 4), (1, 768, 3, 64, 3)])
+def test_ring_emulation_explicit_buffers(causal, overlap, B, S, H, d, N):
+    # The ring with per-rank K/V buffers and copy-engine transfers gives the
+    # fused result, and each rank receives exactly the blocks the traffic
+    # count says: i blocks under causality, N - 1 otherwise.
+    q, k, v = inputs.make_qkv(B, S, H, d, seed=S + N, dtype=torch.bfloat16)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    out = torch.full_like(qd, 9.0)
+    lse = torch.full((B, H, S), 9.0, dtype=torch.float32, device=DEV)
+    cs = torch.cuda.Stream() if overlap else None
+    recv = pkg.cp_ring_attn_fwd_emulated(qd, kd, vd, out, lse, N, causal, copy_stream=cs)
+    torch.cuda.synchronize()
+    assert pkg.cp_get_last_status() == 0
+    want_o, want_l = ref.attention(_np(q), _np(k), _np(v), causal, None)
+    _check_bf16(out, lse, want_o, want_l)
+    fo, fl = pkg.ring_attn_fwd(qd, kd, vd, N, causal)
+    e = (out.float() - fo.float()).abs()
+    assert e.max().item() <= BF16_MAX and e.mean().item() <= BF16_MEAN
+    L = S // N
+    block = 2 * B * L * H * d * 2  # K and V of one shard, bf16
+    want_recv = [i * block for i in range(N)] if causal else [(N - 1) * block] * N
+    assert recv == want_recv
+    sent = [recv[(i + 1) % N] if (not causal or i < N - 1) else 0 for i in range(N)]
+    assert [s_ + r_ for s_, r_ in zip(sent, recv)] == pkg.cp_ring_traffic(B, S, H, d, 2, N, causal)
+
+
 def test_native_kernels_launch():
     before = pkg.launch_counts()
     q, k, v = (t.to(DEV) for t in inputs.make_qkv(1, 256, 1, 128, seed=1, dtype=torch.bfloat16))

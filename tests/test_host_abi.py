@@ -45,6 +45,20 @@ def test_exports_every_declared_symbol(lib):
     assert set(names) <= set(_binding._SIGS)
 
 
+def test_ring_emulation_workspace_and_checks(lib):
+    n = pkg.cp_ring_emulated_workspace_bytes(2, 1024, 2, 128, 4)
+    # 4 ranks x 2 slots x (K, V) blocks of 2*256*2*128 bf16, plus 5 fp32 states
+    blk = 2 * 256 * 2 * 128
+    assert n >= 4 * 2 * 2 * blk * 2 + 5 * blk * 4
+    assert pkg.cp_ring_emulated_workspace_bytes(2, 1000, 2, 128, 3) == -1
+    f = lib.cp_ring_attn_fwd_emulated
+    assert f(None, FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 128, 4, 1, FAKE, 1 << 30, None, None,
+             None) == -1
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 96, 4, 1, FAKE, 1 << 30, None, None,
+             None) == -3
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 128, 4, 1, FAKE, 16, None, None, None) == -6
+
+
 def test_status_strings(lib):
     for code, name in pkg.STATUS_NAMES.items():
         s = pkg.cp_status_string(code)
