@@ -421,6 +421,67 @@ def run_ring_emulation(args, w, local):
     }
 
 
+def run_ulysses(args, w, local):
+    """Time the all-to-all (Ulysses) form against the fused ring kernel on the
+    same inputs; the permutations are HBM-bound, so their achieved bandwidth
+    is reported against the measured copy peak.  One JSON line."""
+    import context_ring_attention_fwd_gb300 as pkg
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    q, k, v = inputs.make_qkv(w.B, w.S, w.H, w.d, w.seed, w.torch_dtype, w.scale, device=str(dev))
+    docs = (inputs.make_doc_offsets(w.S, w.seed + 1, w.doc_min, w.doc_max)
+            if w.packed_docs else None)
+    dd = pkg.doc_offsets_tensor(docs, dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
+    ws = torch.empty(pkg.cp_ulysses_workspace_bytes(w.B, w.S, w.H, w.d, w.n_shards),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / args.steps
+
+    moved = []
+    ms_u = timed(lambda: moved.append(pkg.cp_ulysses_attn_fwd(q, k, v, out, lse, w.n_shards,
+                                                              w.causal, dd, ws, stream)))
+    ms_f = timed(lambda: pkg.cp_ring_attn_fwd(q, k, v, out, lse, w.n_shards, w.causal, dd, stream))
+    if pkg.cp_get_last_status(stream) != 0:
+        raise RuntimeError("device error in the Ulysses form")
+    flops = effective_flops(w, docs)
+    tensor_bytes = q.numel() * q.element_size()
+    perm_bytes = 8 * tensor_bytes  # Q, K, V in and O out, each read once and written once
+    hbm, _, _ = measured_peaks_hbm()
+    perm_ms = max(ms_u - ms_f, 1e-9)
+    return {
+        "metric": METRIC, "impl": "ulysses_all_to_all", "unit": UNIT,
+        "value": flops / (ms_u * 1e-3) / 1e12, "ms_per_step": ms_u, "ms_fused_ring": ms_f,
+        "a2a_bytes_counted": moved[-1], "permutation_bytes_in_hbm": perm_bytes,
+        "permutation_ms_estimate": ms_u - ms_f,
+        "permutation_GBps_estimate": perm_bytes / (perm_ms * 1e-3) / 1e9,
+        "hbm_peak_GBps": hbm,
+        "steps": args.steps, "warmup": args.warmup, "n_gpus": 1, "dtype": w.dtype,
+        "data": "synthetic", "config": _config(w, docs, 1),
+    }
+
+
+def measured_peaks_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f).get("hbm_gbs"), None, "measured"
+    return 6800.0, None, "fallback"
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -434,6 +495,8 @@ def main(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=128)
     ap.add_argument("--ring-emulation", action="store_true",
                     help="time the ring with explicit per-rank buffers instead")
+    ap.add_argument("--ulysses", action="store_true",
+                    help="time the all-to-all (Ulysses) form instead")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the attention kernel from an ncu capture")
     args = ap.parse_args(argv)
@@ -441,8 +504,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_env()
     w = inputs.BY_NAME[args.workload]
-    if args.ring_emulation:
-        line = run_ring_emulation(args, w, local)
+    if args.ring_emulation or args.ulysses:
+        line = run_ring_emulation(args, w, local) if args.ring_emulation else run_ulysses(args, w, local)
         if rank == 0:
             print(json.dumps(line), flush=True)
         return

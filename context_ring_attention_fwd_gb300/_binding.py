@@ -43,6 +43,9 @@ _SIGS = {
     "cp_launch_counts": [ctypes.POINTER(_i64)],
     "cp_test_set_wait_fault": [_i, _i64],
     "cp_ring_emulated_workspace_bytes": [_i, _i, _i, _i, _i],
+    "cp_ulysses_workspace_bytes": [_i, _i, _i, _i, _i],
+    "cp_ulysses_attn_fwd": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _i64, _vp,
+                            ctypes.POINTER(_i64)],
     "cp_ring_attn_fwd_emulated": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _i64,
                                   _vp, _vp, ctypes.POINTER(_i64)],
 }
@@ -74,7 +77,7 @@ def lib() -> ctypes.CDLL:
                     fn.restype = ctypes.c_char_p
                 elif name in ("cp_launch_counts", "cp_test_set_wait_fault"):
                     fn.restype = None
-                elif name == "cp_ring_emulated_workspace_bytes":
+                elif name in ("cp_ring_emulated_workspace_bytes", "cp_ulysses_workspace_bytes"):
                     fn.restype = _i64
                 else:
                     fn.restype = _i
@@ -177,6 +180,34 @@ def cp_ring_attn_fwd_emulated(q, k, v, out, lse, n_shards: int, causal: bool = T
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, H, d, int(n_shards),
         int(bool(causal)), _ptr(workspace), int(workspace.numel()), _stream(stream), cs, recv))
     return list(recv)
+
+
+def cp_ulysses_attn_fwd(q, k, v, out, lse, n_shards: int, causal: bool = True,
+                        doc_offsets: Optional[torch.Tensor] = None,
+                        workspace: Optional[torch.Tensor] = None, stream=None) -> int:
+    """All-to-all (Ulysses) form: head-split attention between two layout
+    permutations.  Returns the bytes the two all-to-alls would move."""
+    B, S, H, d = q.shape
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _need(t, n, torch.bfloat16, (B, S, H, d))
+    _need(lse, "lse", torch.float32, (B, H, S))
+    if doc_offsets is not None:
+        _need(doc_offsets, "doc_offsets", torch.int32)
+    need = int(lib().cp_ulysses_workspace_bytes(B, S, H, d, int(n_shards)))
+    if need < 0:
+        raise CpError("cp_ulysses_workspace_bytes", STATUS_CODES["CP_ERR_SHAPE"])
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    moved = ctypes.c_int64(0)
+    _check("cp_ulysses_attn_fwd", lib().cp_ulysses_attn_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, H, d, int(n_shards),
+        int(bool(causal)), _ptr(doc_offsets), _ptr(workspace), int(workspace.numel()),
+        _stream(stream), ctypes.byref(moved)))
+    return int(moved.value)
+
+
+def cp_ulysses_workspace_bytes(B: int, S: int, H: int, d: int, n_shards: int) -> int:
+    return int(lib().cp_ulysses_workspace_bytes(B, S, H, d, n_shards))
 
 
 def cp_ring_emulated_workspace_bytes(B: int, S: int, H: int, d: int, n_shards: int) -> int:

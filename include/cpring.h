@@ -246,6 +246,27 @@ cp_status cp_ring_attn_fwd_emulated(const void* q, const void* k, const void* v,
                                     int64_t* recv_bytes_per_rank);
 
 /*
+ * The all-to-all form of context parallelism ("上下文並行（Context
+ * Parallelism, CP）", 方案二 All-to-All (DeepSpeed Ulysses)): an all-to-all
+ * turns the sequence-split Q/K/V into head-split ones, every rank attends
+ * over the whole sequence for its H/N heads, and an all-to-all turns the
+ * output back.  On one GPU both all-to-alls are layout permutations run by a
+ * bandwidth-bound kernel; the attention is the fused kernel.  Same arguments
+ * and result as cp_ring_attn_fwd (bf16, d 64 or 128, doc_offsets allowed),
+ * with H % n_shards == 0, plus:
+ *  workspace  device, >= cp_ulysses_workspace_bytes(...) bytes, 256-byte
+ *             aligned, owned by the caller, contents undefined afterwards.
+ *  a2a_bytes  host int64 or NULL: bytes the two all-to-alls would move,
+ *             sent plus received, summed over the ranks (8 * shard bytes *
+ *             (N - 1) with shard = B*(S/N)*H*d*2).
+ */
+int64_t cp_ulysses_workspace_bytes(int B, int S, int H, int d, int n_shards);
+cp_status cp_ulysses_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                              int B, int S, int H, int d, int n_shards, int causal,
+                              const int32_t* doc_offsets, void* workspace,
+                              int64_t workspace_bytes, cudaStream_t stream, int64_t* a2a_bytes);
+
+/*
  * TEST HOOK (failure detection without a GPU fault).  With drop_first_k_tile
  * != 0, the next tensor-core launches have CTA 0 skip loading its first K
  * tile, so one of its bounded device waits runs out: the CTA drains its own

@@ -280,6 +280,28 @@ def test_ring_emulation_explicit_buffers(causal, overlap, B, S, H, d, N):
     assert [s_ + r_ for s_, r_ in zip(sent, recv)] == pkg.cp_ring_traffic(B, S, H, d, 2, N, causal)
 
 
+@pytest.mark.parametrize("causal,docs", [(True, None), (False, None),
+                                         (True, [0, 300, 301, 777, 1024])])
+def test_ulysses_all_to_all_form(causal, docs):
+    # Head-split attention between two all-to-all permutations gives the
+    # ring's result; with shards of whole 256-row tile pairs the same tiles
+    # meet in the same order, so it is bit-identical to the fused kernel.
+    B, S, H, d, N = 2, 1024, 8, 128, 4
+    q, k, v = inputs.make_qkv(B, S, H, d, seed=55, dtype=torch.bfloat16)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    out = torch.full_like(qd, 9.0)
+    lse = torch.full((B, H, S), 9.0, dtype=torch.float32, device=DEV)
+    dd = pkg.doc_offsets_tensor(docs, DEV)
+    moved = pkg.cp_ulysses_attn_fwd(qd, kd, vd, out, lse, N, causal, dd)
+    assert pkg.cp_get_last_status() == 0
+    fo, fl = pkg.ring_attn_fwd(qd, kd, vd, N, causal, docs)
+    assert torch.equal(out, fo) and torch.equal(lse, fl)
+    want_o, want_l = ref.attention(_np(q), _np(k), _np(v), causal, docs)
+    _check_bf16(out, lse, want_o, want_l)
+    shard = B * (S // N) * H * d * 2
+    assert moved == 8 * shard * (N - 1)
+
+
 def test_native_kernels_launch():
     before = pkg.launch_counts()
     q, k, v = (t.to(DEV) for t in inputs.make_qkv(1, 256, 1, 128, seed=1, dtype=torch.bfloat16))

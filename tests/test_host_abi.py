@@ -59,6 +59,17 @@ def test_ring_emulation_workspace_and_checks(lib):
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 128, 4, 1, FAKE, 16, None, None, None) == -6
 
 
+def test_ulysses_checks(lib):
+    assert pkg.cp_ulysses_workspace_bytes(1, 1024, 6, 128, 4) == -1   # 6 heads over 4 ranks
+    n = pkg.cp_ulysses_workspace_bytes(1, 1024, 8, 128, 4)
+    assert n >= 4 * 1024 * 8 * 128 * 2 + 8 * 1024 * 4
+    f = lib.cp_ulysses_attn_fwd
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1024, 6, 128, 4, 1, None, FAKE, 1 << 30, None,
+             None) == -2
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1024, 8, 128, 4, 1, None, FAKE, 16, None,
+             None) == -6
+
+
 def test_status_strings(lib):
     for code, name in pkg.STATUS_NAMES.items():
         s = pkg.cp_status_string(code)
