@@ -61,7 +61,11 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
-// Tuning switches (both give the same result up to rounding):
+// Tuning switches (all give the same result up to rounding):
+//  CPRING_BALANCE          items are dealt in groups of heads holding at least
+//                          this many rounds of the grid (see head_group) ...
+//  CPRING_GROUP_MIN_ROUNDS ... when the launch has at least this many rounds;
+//                          shorter launches deal every item from one pool.
 //  CPRING_FUSED_NOMAX      fused forward only: after the first tile, skip the
 //                          row max and redo a tile only if its row sum shows
 //                          exponentials above 2^64 (the reference point never
@@ -70,6 +74,12 @@ constexpr float kRescaleLog2 = 8.0f;
 //                          paired fp32 FMA / ADD (two elements per instruction).
 //  CPRING_SPLIT_LOAD       fast pass: read the second half of S from TMEM
 //                          while the first half's exponentials run.
+#ifndef CPRING_BALANCE
+#define CPRING_BALANCE 2
+#endif
+#ifndef CPRING_GROUP_MIN_ROUNDS
+#define CPRING_GROUP_MIN_ROUNDS 16
+#endif
 #ifndef CPRING_FUSED_NOMAX
 #define CPRING_FUSED_NOMAX 1
 #endif
@@ -133,6 +143,7 @@ struct KParams {
   unsigned long long timeout_ns;
   int fault_drop_k;  // test hook: CTA 0 never loads its first K tile
   int kv_row0;       // key index of row 0 of the K/V tensors (0 unless a block)
+  int head_group;    // (b, h) heads whose items are dealt out together
 };
 
 struct Item {
@@ -167,7 +178,10 @@ __device__ __forceinline__ void tile_keys(const KParams& p, int f, int& ks, int&
   ke = min(ks + kBN, (j + 1) * p.L);
 }
 
-// Work item w (heaviest first): (b, h, query shard, pair of 128-row tiles).
+// Work item w: (b, h, query shard, pair of 128-row tiles).  Items are dealt
+// head group by head group (p.head_group (b, h) heads at a time), and inside
+// a group heaviest first, so that the CTAs running at any moment stream the
+// K/V of few heads and reuse each K/V tile from L2.
 // A tile's visible keys are [max(doc_start(q_first), klo), min(h(q_last), khi)]
 // with h(q) = q (causal) or doc_end(q) - 1: every key of that interval is
 // seen by at least one row of the tile, so the K/V tiles it touches are
@@ -175,8 +189,12 @@ __device__ __forceinline__ void tile_keys(const KParams& p, int f, int& ks, int&
 __device__ __forceinline__ void decode_item(const KParams& p, int n_docs, int w, Item& it) {
   const int BH = p.B * p.H;
   const int slots = p.n_qshards * p.pairs_per_shard;
-  const int g = slots - 1 - w / BH;
-  const int bh = w % BH;
+  const int HG = p.head_group;
+  const int gi = w / (HG * slots);                  // head group
+  const int r = w - gi * HG * slots;
+  const int hg = min(HG, BH - gi * HG);             // heads in this group
+  const int g = slots - 1 - r / hg;
+  const int bh = gi * HG + r % hg;
   it.b = bh / p.H;
   it.h = bh - it.b * p.H;
   const int ii = g / p.pairs_per_shard;
@@ -941,6 +959,23 @@ cudaError_t launch_t(const AttnArgs& a, cudaStream_t stream) {
   p.timeout_ns = g_wait_limit_ns.load();
   p.fault_drop_k = g_fault_drop_k.load();
   const int grid = static_cast<int>(std::min<long long>(items, sm_count()));
+  // Head groups: fewer heads in flight reuse each K/V tile from L2.  A long
+  // launch (many rounds of the grid) takes the smallest group whose items
+  // fill CPRING_BALANCE rounds; a short one keeps a single pool, because the
+  // heaviest-first deal only balances the tail when every item is in it.
+  // With documents the live work per item depends on the layout, which stays
+  // on the device, so the item count says nothing about the rounds: one pool.
+  {
+    const int BH = a.B * a.H;
+    const long long slots = static_cast<long long>(p.n_qshards) * p.pairs_per_shard;
+    long long hg = BH;
+    if (a.doc_offsets == nullptr &&
+        items >= static_cast<long long>(CPRING_GROUP_MIN_ROUNDS) * grid) {
+      hg = (static_cast<long long>(CPRING_BALANCE) * grid + slots - 1) / slots;
+      hg = std::max<long long>(1, std::min<long long>(hg, BH));
+    }
+    p.head_group = static_cast<int>(hg);
+  }
   if (grid <= 0) return cudaSuccess;
   kern<<<grid, kThreads, Lay::kAlloc, stream>>>(mq, mk, mv, p);
   count_launch(0);
