@@ -37,6 +37,14 @@ from context_ring_attention_fwd_gb300 import inputs  # noqa: E402
 METRIC = "effective causal TFLOP/s of ring-attention fwd (1 GB300) and % of bf16 dense peak"
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "bf16_causal_128k"
+# DRAM bytes (read + write) per launch of the fused attention kernel, from one
+# ncu capture of dram__bytes_read.sum + dram__bytes_write.sum on this bench
+# command with that workload.  They hold for the kernel they were taken on:
+# re-take them whenever the kernel changes.
+NCU_TRAFFIC_BYTES = {
+    "bf16_causal_128k": 37.405e9 + 1.0835e9,
+    "bf16_full_32k": 1.6020e9 + 0.2578e9,
+}
 
 
 # ------------------------------------------------------------------ helpers
@@ -318,7 +326,9 @@ def run_ours(args, w, rank, world, local):
     achieved = flops / (avg_launch_ms * 1e-3) / 1e12
     peak_burst, peak_sust, peak_src = measured_peaks()
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
-                "frac": achieved / peak_burst, "traffic": args.traffic,
+                "frac": achieved / peak_burst,
+                "traffic": args.traffic if args.traffic is not None
+                else NCU_TRAFFIC_BYTES.get(w.name),
                 "peak_kind": f"{peak_src} bf16 dense burst (cuBLAS)",
                 "frac_of_sustained": achieved / peak_sust if peak_sust else None}
 
