@@ -12,9 +12,10 @@
 // rank g's head group is the contiguous run of H/N heads g*H/N .. (g+1)*H/N-1
 // of every token, so [B, S, H, d] becomes N tensors [B, S, H/N, d] (one per
 // rank, stored back to back) and back.  The permutation kernel moves 16-byte
-// vectors; it is bound by HBM bandwidth.
+// vectors with no per-element division; it is bound by HBM bandwidth.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "internal.h"
@@ -23,40 +24,61 @@ namespace cpring {
 namespace {
 
 constexpr int kPermThreads = 256;
+constexpr int kPermUnroll = 4;            // 16-byte vectors in flight per thread
+constexpr int kPermBlockVecs = 4096;      // about 64 KB moved per block
 
-// Chunk (row, g) of C = (H/N) * d elements: in[row][g*C + c] <-> out[g][row][c].
-// to_heads: in = [R rows][N*C] (sequence layout), out = [N][R][C] (head groups).
-// otherwise the inverse.  Elements are moved as 16-byte vectors (C*2 % 16 == 0).
+// Chunk (row, g) of cv 16-byte vectors: in[row][g][c] <-> out[g][row][c].
+// to_heads: src = [rows][N][cv] (sequence layout), dst = [N][rows][cv] (head
+// groups); otherwise the inverse.  Block (x, y) moves rows
+// [x * rows_per_block, ...) of head group g = y.  Each thread splits its first
+// vector index into (row, c) once and then steps by the block size with a
+// carry, so the loop does no division.
 __global__ void __launch_bounds__(kPermThreads)
     a2a_permute_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, long long rows,
-                       int n_groups, int chunk_vec, bool to_heads) {
-  const long long total = rows * n_groups * chunk_vec;
-  for (long long x = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; x < total;
-       x += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int c = static_cast<int>(x % chunk_vec);
-    const long long rg = x / chunk_vec;
-    // x walks the destination in order for coalesced writes
-    if (to_heads) {
-      const long long row = rg % rows;
-      const int g = static_cast<int>(rg / rows);
-      dst[x] = src[(row * n_groups + g) * chunk_vec + c];
-    } else {
-      const int g = static_cast<int>(rg % n_groups);
-      const long long row = rg / n_groups;
-      dst[x] = src[(static_cast<long long>(g) * rows + row) * chunk_vec + c];
+                       int n_groups, int cv, int rows_per_block, bool to_heads) {
+  const int g = blockIdx.y;
+  const long long row0 = static_cast<long long>(blockIdx.x) * rows_per_block;
+  const int nr = static_cast<int>(min(static_cast<long long>(rows_per_block), rows - row0));
+  const int dr = kPermThreads / cv, dc = kPermThreads % cv;
+  int r = threadIdx.x / cv, c = threadIdx.x % cv;
+  const long long src_row_stride = to_heads ? static_cast<long long>(n_groups) * cv : cv;
+  const long long dst_row_stride = to_heads ? cv : static_cast<long long>(n_groups) * cv;
+  const long long src_base = to_heads ? (row0 * n_groups + g) * cv : (g * rows + row0) * cv;
+  const long long dst_base = to_heads ? (g * rows + row0) * cv : (row0 * n_groups + g) * cv;
+  while (r < nr) {
+    uint4 val[kPermUnroll];
+    long long di[kPermUnroll];
+    int n = 0;
+#pragma unroll
+    for (int u = 0; u < kPermUnroll; ++u) {
+      if (r < nr) {
+        val[u] = src[src_base + r * src_row_stride + c];
+        di[u] = dst_base + r * dst_row_stride + c;
+        n = u + 1;
+        c += dc;
+        r += dr;
+        if (c >= cv) {
+          c -= cv;
+          ++r;
+        }
+      }
     }
+#pragma unroll
+    for (int u = 0; u < kPermUnroll; ++u)
+      if (u < n) dst[di[u]] = val[u];
   }
 }
 
 cudaError_t permute(const void* src, void* dst, long long rows, int n_groups, int chunk_bytes,
                     bool to_heads, cudaStream_t stream) {
-  const int chunk_vec = chunk_bytes / 16;
-  const long long total = rows * n_groups * chunk_vec;
-  const long long want = (total + kPermThreads - 1) / kPermThreads;
-  const int grid = static_cast<int>(std::min<long long>(want, 8LL * sm_count()));
+  const int cv = chunk_bytes / 16;
+  const int rows_per_block = std::max(1, kPermBlockVecs / cv);
+  const long long blocks = (rows + rows_per_block - 1) / rows_per_block;
+  if (blocks > 0x7fffffffLL || n_groups > 65535) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(n_groups));
   a2a_permute_kernel<<<grid, kPermThreads, 0, stream>>>(static_cast<const uint4*>(src),
                                                         static_cast<uint4*>(dst), rows, n_groups,
-                                                        chunk_vec, to_heads);
+                                                        cv, rows_per_block, to_heads);
   count_launch(2);
   return cudaGetLastError();
 }
