@@ -28,6 +28,12 @@ Sources (page title, site, section):
       - §常见失败模式 / §配置关注点: packed samples keep their document
         boundaries across shards; a wrong causal or document mask leaks the
         future or mixes samples.
+  * FP8 K/V: the communication-volume note of §通訊量分析 on the first page
+    says the bytes moved depend on whether K/V travel in FP8; its timeline
+    ties FP8 to FlashAttention-3.  Nothing more is given, so the FP8 form
+    here is the plainest one: OCP E4M3 (bias 7, 3 mantissa bits, largest
+    finite 448, no infinities) with one scale per (b, h), and attention over
+    the dequantized values.
 
 Readings where the pages are silent (each is listed in the design notes):
   * causal mask: key k is visible to query q iff k <= q (a token sees
@@ -41,6 +47,11 @@ Readings where the pages are silent (each is listed in the design notes):
     returned as [B, H, S].
   * a row with no visible key inside one step has m = -inf, l = 0, O = 0;
     the merge treats such a partial as the identity.
+  * FP8 quantisation of a [B, S, H, d] tensor: amax = max |x| over (S, d) of
+    each (b, h), in fp32; inv = 448 / amax and x8 = E4M3(x * inv), both fp32
+    operations rounded to nearest, then rounded to the nearest E4M3 value
+    (ties to even) and saturated at +-448; descale = amax / 448 (fp32).  An
+    all-zero (b, h) gets inv = descale = 1.
 
 Array conventions: q, k, v are [B, S, H, d] (any real dtype, upcast exactly
 to float64); per-step partial state is O [B, L, H, d], m and l [B, H, L].
@@ -416,3 +427,52 @@ def zero_query_closed_form(v, causal: bool = True, doc_offsets=None):
 def all_orders(n_shards: int) -> Iterable[Tuple[int, ...]]:
     """Every visiting order of n_shards shards."""
     return itertools.permutations(range(n_shards))
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) storage of Q, K, V
+# ---------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+def e4m3_round(x) -> np.ndarray:
+    """Nearest OCP E4M3 value to each element (ties to even), saturated at
+    +-448, as float64.  The grid: in the binade [2^e, 2^(e+1)) with e >= -6
+    three mantissa bits give a spacing of 2^(e-3); below 2^-6 the subnormals
+    are the multiples of 2^-9.  Inputs are float32 or float64; NaN stays NaN."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, e = np.frexp(a)                       # a = f * 2^e, f in [0.5, 1)
+    quantum = np.ldexp(1.0, np.maximum(e - 4, -9))
+    r = np.rint(a / quantum) * quantum       # np.rint rounds halves to even
+    r = np.minimum(r, E4M3_MAX)
+    return np.copysign(r, x)
+
+
+def fp8_quantize(x):
+    """Per-(b, h) E4M3 quantisation of x [B, S, H, d] (read as float32).
+    Returns (x8, descale): x8 [B, S, H, d] float64 holding E4M3 values and
+    descale [B, H] float32, so that x ~ x8 * descale."""
+    x32 = np.asarray(x, dtype=np.float32)
+    amax = np.abs(x32).max(axis=(1, 3)).astype(np.float32)      # [B, H]
+    nz = amax > 0
+    safe = np.where(nz, amax, np.float32(1.0)).astype(np.float32)
+    inv = np.where(nz, np.float32(E4M3_MAX) / safe, np.float32(1.0)).astype(np.float32)
+    descale = np.where(nz, safe / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    scaled = (x32 * inv[:, None, :, None]).astype(np.float32)
+    return e4m3_round(scaled), descale
+
+
+def fp8_dequantize(x8, descale) -> np.ndarray:
+    """x8 * descale in float64 (exact: an E4M3 value times an fp32 scale)."""
+    x8 = np.asarray(x8, dtype=np.float64)
+    return x8 * np.asarray(descale, dtype=np.float64)[:, None, :, None]
+
+
+def attention_fp8(q8, k8, v8, q_descale, k_descale, v_descale, causal: bool = True,
+                  doc_offsets=None):
+    """The forward over FP8-stored inputs: the exact masked softmax attention
+    of the dequantized Q, K, V.  Returns (out [B,S,H,d], lse [B,H,S])."""
+    return attention(fp8_dequantize(q8, q_descale), fp8_dequantize(k8, k_descale),
+                     fp8_dequantize(v8, v_descale), causal, doc_offsets)

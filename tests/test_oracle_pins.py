@@ -338,3 +338,81 @@ def test_effective_flops():
     w = inputs.BY_NAME["bf16_causal_128k"]
     pairs = ref.visible_pair_count(4096, True)
     assert pairs == 4096 * 4097 // 2
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) storage: rounding, quantisation, attention over dequantized values
+# ---------------------------------------------------------------------------
+
+def _torch_e4m3(x32: np.ndarray) -> np.ndarray:
+    """torch's float32 -> float8_e4m3fn conversion, decoded back to float64."""
+    return torch.from_numpy(x32).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def test_e4m3_round_matches_torch_conversion():
+    rng = np.random.default_rng(7)
+    mag = np.exp2(rng.uniform(-13, 8.8, 200_000)).astype(np.float32)     # subnormals..448
+    x = (mag * rng.choice([-1.0, 1.0], mag.size)).astype(np.float32)
+    np.testing.assert_array_equal(ref.e4m3_round(x), _torch_e4m3(x))
+
+
+def test_e4m3_round_fixed_points_and_ties():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    vals = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    finite = vals[np.isfinite(vals)]
+    assert finite.size == 254 and finite.max() == 448.0 and finite.min() == -448.0
+    np.testing.assert_array_equal(ref.e4m3_round(finite), finite)
+    # every midpoint between neighbouring positive codes rounds to the even one
+    grid = np.unique(finite[finite >= 0])
+    mids = (grid[:-1] + grid[1:]) / 2
+    got = ref.e4m3_round(mids)
+    even_code = lambda v: int(torch.tensor([v]).to(torch.float8_e4m3fn).view(torch.uint8)) % 2 == 0
+    for lo, hi, g in zip(grid[:-1], grid[1:], got):
+        assert g == (lo if even_code(lo) else hi)
+        assert even_code(g)
+
+
+def test_e4m3_round_closed_forms():
+    cases = {448.0: 448.0, 460.0: 448.0, 1e6: 448.0, -1e6: -448.0,   # saturation
+             2.0 ** -10: 0.0, 1.5 * 2.0 ** -10: 2.0 ** -9,            # below the subnormals
+             1.0625: 1.0, 1.1875: 1.25, 3.0 * 2 ** -8: 3.0 * 2 ** -8,  # ties to even; a subnormal
+             0.0: 0.0, 2.0 ** -6: 2.0 ** -6, 240.0: 240.0, 250.0: 256.0}
+    for x, want in cases.items():
+        assert ref.e4m3_round(np.float32(x)) == want, x
+    assert np.isnan(ref.e4m3_round(np.float32("nan")))
+
+
+def test_fp8_quantize_scales_and_range():
+    B, S, H, d = 2, 96, 3, 64
+    x = torch.randn(B, S, H, d, generator=torch.Generator().manual_seed(11), dtype=torch.float32)
+    x[1, :, 2, :] = 0.0                                # an all-zero (b, h)
+    x[0, 17, 1, 5] = -9.5                              # a known extreme
+    x8, desc = ref.fp8_quantize(x.numpy())
+    assert desc.dtype == np.float32 and desc.shape == (B, H)
+    assert desc[1, 2] == 1.0 and np.all(x8[1, :, 2, :] == 0.0)
+    assert x8[0, 17, 1, 5] == -448.0                   # amax maps to the largest code
+    assert desc[0, 1] == np.float32(9.5) / np.float32(448.0)
+    np.testing.assert_array_equal(ref.e4m3_round(x8), x8)            # on the grid
+    assert np.abs(x8).max() <= 448.0
+    # dequantisation error: within half a quantum of the E4M3 grid, scaled
+    deq = ref.fp8_dequantize(x8, desc)
+    a = np.abs(x.numpy().astype(np.float64) / desc[:, None, :, None].astype(np.float64))
+    half_q = np.ldexp(1.0, np.maximum(np.frexp(a)[1] - 5, -10))
+    assert np.all(np.abs(deq - x.numpy()) <= (half_q * 1.0001 + 1e-7) * desc[:, None, :, None])
+
+
+@pytest.mark.parametrize("causal,docs", [(True, None), (False, [0, 40, 41, 128]),
+                                         (True, [0, 70, 128])])
+def test_attention_fp8_is_attention_of_dequantized_inputs(causal, docs):
+    B, S, H, d = 1, 128, 2, 64
+    q, k, v = _qkv(B, S, H, d, 23)
+    (q8, qd), (k8, kd), (v8, vd) = (ref.fp8_quantize(t) for t in (q, k, v))
+    o, lse = ref.attention_fp8(q8, k8, v8, qd, kd, vd, causal, docs)
+    deq = [torch.from_numpy(ref.fp8_dequantize(a, s)) for a, s in ((q8, qd), (k8, kd), (v8, vd))]
+    want = _sdpa(*(t.numpy() for t in deq), causal, docs)
+    np.testing.assert_allclose(o, want, atol=1e-12, rtol=0)
+    # Q = 0: each query averages the dequantized V over its visible keys
+    o0, lse0 = ref.attention_fp8(np.zeros_like(q8), k8, v8, qd, kd, vd, causal, docs)
+    c_o, c_l = ref.zero_query_closed_form(ref.fp8_dequantize(v8, vd), causal, docs)
+    np.testing.assert_allclose(o0, c_o, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(lse0, c_l, atol=1e-12, rtol=0)
