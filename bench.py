@@ -499,6 +499,67 @@ def run_ulysses(args, w, local):
     }
 
 
+def run_fp8(args, w, local):
+    """Time the FP8 (E4M3) form on the workload's inputs stored as FP8: the
+    quantisation of Q, K, V and the FP8 forward, each with CUDA events, and
+    the bf16 forward on the same bf16 inputs beside them.  The roofline of
+    the FP8 forward is taken against the FP8 dense peak: the measured bf16
+    burst figure times the nominal FP8 / bf16 ratio (4.5 / 2.25 PFLOP/s).
+    One JSON line."""
+    import context_ring_attention_fwd_gb300 as pkg
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    q, k, v = inputs.make_qkv(w.B, w.S, w.H, w.d, w.seed, w.torch_dtype, w.scale, device=str(dev))
+    docs = (inputs.make_doc_offsets(w.S, w.seed + 1, w.doc_min, w.doc_max)
+            if w.packed_docs else None)
+    dd = pkg.doc_offsets_tensor(docs, dev)
+    stream = torch.cuda.current_stream(dev)
+    fp8 = pkg.fp8_quantize_qkv(q, k, v, stream)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / args.steps
+
+    clocks = ClockSampler(gpu_index(local))
+    clocks.start()
+    time.sleep(0.3)
+    ms_8 = timed(lambda: pkg.cp_ring_attn_fwd_fp8(*fp8, out, lse, w.n_shards, w.causal, dd,
+                                                  stream))
+    clk = clocks.stop()
+    ms_q = timed(lambda: pkg.fp8_quantize_qkv(q, k, v, stream))
+    ms_b = timed(lambda: pkg.cp_ring_attn_fwd(q, k, v, out, lse, w.n_shards, w.causal, dd,
+                                              stream))
+    if pkg.cp_get_last_status(stream) != 0:
+        raise RuntimeError("device error in the FP8 form")
+    flops = effective_flops(w, docs)
+    achieved = flops / (ms_8 * 1e-3) / 1e12
+    peak_burst, peak_sust, peak_src = measured_peaks()
+    g8 = pkg.cp_ring_traffic(w.B, w.S, w.H, w.d, 1, w.n_shards, w.causal)
+    g16 = pkg.cp_ring_traffic(w.B, w.S, w.H, w.d, 2, w.n_shards, w.causal)
+    return {
+        "metric": METRIC, "impl": "fp8_e4m3", "unit": UNIT, "value": achieved,
+        "ms_per_step": ms_8, "ms_quantize_qkv": ms_q, "ms_bf16_fused": ms_b,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": 2 * peak_burst,
+                     "unit": "TFLOP/s", "frac": achieved / (2 * peak_burst), "traffic": None,
+                     "peak_kind": f"{peak_src} bf16 dense burst (cuBLAS) x 2 (nominal FP8/bf16)"},
+        "ring_send_plus_recv_bytes_fp8": int(sum(g8)),
+        "ring_send_plus_recv_bytes_bf16": int(sum(g16)),
+        "clocks": clk, "steps": args.steps, "warmup": args.warmup, "n_gpus": 1,
+        "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic", "config": _config(w, docs, 1),
+    }
+
+
 def measured_peaks_hbm():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -522,6 +583,8 @@ def main(argv=None):
                     help="time the ring with explicit per-rank buffers instead")
     ap.add_argument("--ulysses", action="store_true",
                     help="time the all-to-all (Ulysses) form instead")
+    ap.add_argument("--fp8", action="store_true",
+                    help="time the FP8 (E4M3) form instead")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the attention kernel from an ncu capture")
     args = ap.parse_args(argv)
@@ -529,8 +592,9 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_env()
     w = inputs.BY_NAME[args.workload]
-    if args.ring_emulation or args.ulysses:
-        line = run_ring_emulation(args, w, local) if args.ring_emulation else run_ulysses(args, w, local)
+    if args.ring_emulation or args.ulysses or args.fp8:
+        line = (run_ring_emulation(args, w, local) if args.ring_emulation
+                else run_ulysses(args, w, local) if args.ulysses else run_fp8(args, w, local))
         if rank == 0:
             print(json.dumps(line), flush=True)
         return

@@ -18,8 +18,9 @@ from typing import Optional, Sequence
 import torch
 
 from ._binding import (  # noqa: F401
-    CP_OK, STATUS_CODES, STATUS_NAMES, CpError, LIB_PATH, cp_get_last_status, cp_lse_finalize,
-    cp_lse_merge, cp_ring_attn_fwd, cp_ring_attn_fwd_emulated, cp_ring_attn_fwd_f32,
+    CP_OK, STATUS_CODES, STATUS_NAMES, CpError, LIB_PATH, cp_fp8_quantize, cp_get_last_status,
+    cp_lse_finalize, cp_lse_merge, cp_ring_attn_fwd, cp_ring_attn_fwd_emulated,
+    cp_ring_attn_fwd_f32, cp_ring_attn_fwd_fp8,
     cp_ring_emulated_workspace_bytes, cp_ring_schedule, cp_ring_step, cp_ulysses_attn_fwd,
     cp_ulysses_workspace_bytes,
     cp_ring_traffic, cp_status_string, doc_offsets_tensor, launch_counts, lib,
@@ -29,6 +30,7 @@ __all__ = [
     "cp_ring_attn_fwd", "cp_ring_attn_fwd_f32", "cp_ring_step", "cp_lse_merge",
     "cp_lse_finalize", "cp_ring_schedule", "cp_ring_traffic", "cp_get_last_status",
     "cp_status_string", "ring_attn_fwd", "ring_attn_fwd_host", "ring_attn_composed",
+    "cp_fp8_quantize", "cp_ring_attn_fwd_fp8", "fp8_quantize_qkv", "ring_attn_fwd_fp8",
     "CpError", "lib",
 ]
 
@@ -127,4 +129,33 @@ def ring_attn_composed(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, n_shar
         cp_lse_finalize(o_acc, m_acc, l_acc, o_fin, lse_fin, stream)
         out[:, i * L:(i + 1) * L].copy_(o_fin)
         lse[:, :, i * L:(i + 1) * L].copy_(lse_fin)
+    return out, lse
+
+
+def fp8_quantize_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, stream=None):
+    """E4M3 storage of bf16 Q, K, V [B,S,H,d]: returns (q8, k8, v8t, q_descale,
+    k_descale, v_descale) with q8, k8 [B,S,H,d], v8t [B,H,d,S] (uint8) and the
+    descales [B,H] fp32."""
+    B, S, H, d = q.shape
+    dev = q.device
+    q8 = torch.empty((B, S, H, d), dtype=torch.uint8, device=dev)
+    k8 = torch.empty_like(q8)
+    v8t = torch.empty((B, H, d, S), dtype=torch.uint8, device=dev)
+    desc = [torch.empty((B, H), dtype=torch.float32, device=dev) for _ in range(3)]
+    cp_fp8_quantize(q, q8, desc[0], False, stream)
+    cp_fp8_quantize(k, k8, desc[1], False, stream)
+    cp_fp8_quantize(v, v8t, desc[2], True, stream)
+    return q8, k8, v8t, desc[0], desc[1], desc[2]
+
+
+def ring_attn_fwd_fp8(fp8_inputs, n_shards: int = 1, causal: bool = True, doc_offsets=None,
+                      stream=None):
+    """The FP8 fused forward on the output of fp8_quantize_qkv; allocates and
+    returns (out [B,S,H,d] bf16, lse [B,H,S] fp32)."""
+    q8, k8, v8t, qd, kd, vd = fp8_inputs
+    B, S, H, d = q8.shape
+    out = torch.empty((B, S, H, d), dtype=torch.bfloat16, device=q8.device)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=q8.device)
+    docs = doc_offsets_tensor(doc_offsets, q8.device)
+    cp_ring_attn_fwd_fp8(q8, k8, v8t, qd, kd, vd, out, lse, n_shards, causal, docs, stream)
     return out, lse

@@ -48,6 +48,9 @@ _SIGS = {
                             ctypes.POINTER(_i64)],
     "cp_ring_attn_fwd_emulated": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _i64,
                                   _vp, _vp, ctypes.POINTER(_i64)],
+    "cp_fp8_quantize": [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp],
+    "cp_ring_attn_fwd_fp8": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp,
+                             _vp],
 }
 
 
@@ -139,6 +142,38 @@ def cp_ring_attn_fwd(q, k, v, out, lse, n_shards: int, causal: bool = True,
     _check("cp_ring_attn_fwd", lib().cp_ring_attn_fwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, H, d, int(n_shards),
         int(bool(causal)), _ptr(doc_offsets), _stream(stream)))
+
+
+def cp_fp8_quantize(x, x8, descale, transpose: bool = False, stream=None) -> None:
+    """Per-(b, h) E4M3 quantisation of x [B,S,H,d] bf16 into x8 (uint8,
+    [B,S,H,d], or [B,H,d,S] with transpose) and descale [B,H] fp32."""
+    B, S, H, d = x.shape
+    _need(x, "x", torch.bfloat16)
+    _need(x8, "x8", torch.uint8, (B, H, d, S) if transpose else (B, S, H, d))
+    _need(descale, "descale", torch.float32, (B, H))
+    _check("cp_fp8_quantize", lib().cp_fp8_quantize(
+        _ptr(x), _ptr(x8), _ptr(descale), B, S, H, d, int(bool(transpose)), _stream(stream)))
+
+
+def cp_ring_attn_fwd_fp8(q8, k8, v8t, q_descale, k_descale, v_descale, out, lse, n_shards: int,
+                         causal: bool = True, doc_offsets: Optional[torch.Tensor] = None,
+                         stream=None) -> None:
+    """FP8 fused forward: q8, k8 uint8 E4M3 [B,S,H,d], v8t uint8 E4M3
+    [B,H,d,S], descales fp32 [B,H]; out [B,S,H,d] bf16, lse [B,H,S] fp32."""
+    B, S, H, d = q8.shape
+    _need(q8, "q8", torch.uint8, (B, S, H, d))
+    _need(k8, "k8", torch.uint8, (B, S, H, d))
+    _need(v8t, "v8t", torch.uint8, (B, H, d, S))
+    for t, n in ((q_descale, "q_descale"), (k_descale, "k_descale"), (v_descale, "v_descale")):
+        _need(t, n, torch.float32, (B, H))
+    _need(out, "out", torch.bfloat16, (B, S, H, d))
+    _need(lse, "lse", torch.float32, (B, H, S))
+    if doc_offsets is not None:
+        _need(doc_offsets, "doc_offsets", torch.int32)
+    _check("cp_ring_attn_fwd_fp8", lib().cp_ring_attn_fwd_fp8(
+        _ptr(q8), _ptr(k8), _ptr(v8t), _ptr(q_descale), _ptr(k_descale), _ptr(v_descale),
+        _ptr(out), _ptr(lse), B, S, H, d, int(n_shards), int(bool(causal)), _ptr(doc_offsets),
+        _stream(stream)))
 
 
 def cp_ring_attn_fwd_noalloc(q, k, v, out, lse, n_shards: int, causal: bool = True,

@@ -21,7 +21,7 @@ LIB = os.path.join(LIBDIR, "libcpring.so")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 
 SOURCES = ["attn_sm103.cu", "attn_f32.cu", "merge.cu", "noalloc.cu", "ring_emulation.cpp",
-           "ulysses.cu", "api.cpp"]
+           "ulysses.cu", "fp8.cu", "api.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -36,7 +36,7 @@ def _nvcc() -> str:
 # setmaxnreg; the split is sized for exactly this many registers per thread at
 # launch, so a build that comes out different is refused (the split would not
 # fit and the kernel would stall).
-SPLIT_KERNEL = "ring_attn_bf16_kernel"
+SPLIT_KERNELS = ("ring_attn_bf16_kernel", "ring_attn_fp8_kernel")
 SPLIT_LAUNCH_REGS = 168
 
 
@@ -45,10 +45,11 @@ def _check_split(src: str, ptxas_log: str) -> None:
     for line in ptxas_log.splitlines():
         if "Compiling entry function" in line:
             entry = line
-        elif "Used" in line and "registers" in line and entry and SPLIT_KERNEL in entry:
+        elif "Used" in line and "registers" in line and entry and \
+                any(k in entry for k in SPLIT_KERNELS):
             n = int(line.split("Used")[1].split("registers")[0])
             if n != SPLIT_LAUNCH_REGS:
-                raise RuntimeError(f"{src}: {SPLIT_KERNEL} launches with {n} registers per "
+                raise RuntimeError(f"{src}: {entry.strip()} launches with {n} registers per "
                                    f"thread, its register split needs {SPLIT_LAUNCH_REGS}")
             entry = None
 

@@ -30,7 +30,8 @@ cp_status check_device() {
   return CP_OK;
 }
 
-cp_status run_attn(AttnArgs a, bool bf16, cudaStream_t stream) {
+// kind: 0 fp32 CUDA-core kernel, 1 bf16 tcgen05 kernel, 2 FP8 tcgen05 kernel.
+cp_status run_attn(AttnArgs a, int kind, cudaStream_t stream) {
   cp_status st = check_device();
   if (st != CP_OK) return st;
   int32_t* info = nullptr;
@@ -43,7 +44,9 @@ cp_status run_attn(AttnArgs a, bool bf16, cudaStream_t stream) {
     }
     a.doc_info = info;
   }
-  const cudaError_t e = bf16 ? cpring::launch_attn_bf16(a, stream) : cpring::launch_attn_f32(a, stream);
+  const cudaError_t e = kind == 2   ? cpring::launch_attn_fp8(a, stream)
+                        : kind == 1 ? cpring::launch_attn_bf16(a, stream)
+                                    : cpring::launch_attn_f32(a, stream);
   if (info) cudaFreeAsync(info, stream);
   return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
@@ -91,6 +94,33 @@ cp_status cp_ring_attn_fwd(const void* q, const void* k, const void* v, void* ou
   a.doc_offsets = doc_offsets;
   a.out = out; a.lse = lse;
   return run_attn(a, true, stream);
+}
+
+cp_status cp_ring_attn_fwd_fp8(const void* q8, const void* k8, const void* v8t,
+                               const float* q_descale, const float* k_descale,
+                               const float* v_descale, void* out, float* lse, int B, int S, int H,
+                               int d, int n_shards, int causal, const int32_t* doc_offsets,
+                               cudaStream_t stream) {
+  if (!q8 || !k8 || !v8t || !q_descale || !k_descale || !v_descale || !out || !lse)
+    return CP_ERR_NULL;
+  cp_status st = check_shape(B, S, H, d, n_shards);
+  if (st != CP_OK) return st;
+  if (d != 128) return CP_ERR_UNSUPPORTED;
+  if (causal != 0 && causal != 1) return CP_ERR_SHAPE;
+  if ((S / n_shards) % 16 != 0) return CP_ERR_SHAPE;
+  if (!aligned(q8, 16) || !aligned(k8, 16) || !aligned(v8t, 16) || !aligned(out, 16) ||
+      !aligned(q_descale, 4) || !aligned(k_descale, 4) || !aligned(v_descale, 4) ||
+      !aligned(lse, 4) || !aligned(doc_offsets, 4))
+    return CP_ERR_ALIGN;
+  AttnArgs a{};
+  a.q = q8; a.k = k8; a.v = v8t;
+  a.q_descale = q_descale; a.k_descale = k_descale; a.v_descale = v_descale;
+  a.B = B; a.S = S; a.H = H; a.d = d; a.n_shards = n_shards;
+  a.q_shard = -1; a.k_shard = -1;
+  a.causal = causal;
+  a.doc_offsets = doc_offsets;
+  a.out = out; a.lse = lse;
+  return run_attn(a, 2, stream);
 }
 
 cp_status cp_ring_attn_fwd_f32(const float* q, const float* k, const float* v, float* out,

@@ -1,4 +1,5 @@
-// Ring-attention forward for bf16 inputs on sm_103a tensor cores (tcgen05).
+// Ring-attention forward on sm_103a tensor cores (tcgen05): bf16 inputs, and
+// E4M3 (FP8) inputs with per-(b, h) scales.
 //
 // What is computed ("上下文並行（Context Parallelism, CP）", compassingai.com,
 // section 線上 Softmax, algorithm "Ring Attention + FlashAttention 分塊計算"):
@@ -11,7 +12,7 @@
 // computed (section 因果掩碼的特殊處理).  The inner tile loop that the page
 // leaves out is this kernel's main loop.
 //
-// GB300 mapping.  One persistent CTA per SM (320 threads):
+// GB300 mapping.  One persistent CTA per SM (384 threads, three warpgroups):
 //   warps 0-3  softmax + merge + epilogue for query tile 0 (128 rows)
 //   warps 4-7  the same for query tile 1 (the next 128 rows)
 //   warp  8    TMA producer: Q tiles once per work item, then K/V tiles of
@@ -31,6 +32,15 @@
 // only when the row max grows by more than 2^8 (so most tiles need no
 // rescale of O); the exact row max is tracked separately and the result is
 // converted to the pages' (O, m, l) with m the true row max at the end.
+//
+// FP8 form (ring_attn_fp8_kernel).  Q and K arrive as E4M3 [B, S, H, d] and
+// V as E4M3 [B, H, d, S] (keys contiguous, so V is K-major for the PV MMA),
+// each with one fp32 descale per (b, h).  Both MMAs run as kind::f8f6f4; the
+// softmax writes P as E4M3 (four per TMEM column) and always keeps P <= 2^8
+// (the row max is taken every tile), inside E4M3's range of 448.  The
+// descales enter as the score scale (q_descale * k_descale) and the output
+// scale (v_descale).  The communication-volume note of the first page ties
+// the bytes moved to FP8 transfer; this form halves the K/V bytes.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -93,11 +103,12 @@ constexpr int kPReadyCount = 128;
 constexpr float kOverflowGuard = 18446744073709551616.0f;  // 2^64
 constexpr unsigned long long kTimeoutNs = 4000000000ull;  // per wait
 
-template <int D>
+template <int D, int E>  // E = bytes per element (2 bf16, 1 E4M3)
 struct Layout {
-  static constexpr int kTileBytes = kBM * D * 2;    // 128 rows x D bf16
-  static constexpr int kPanelBytes = kBM * 64 * 2;  // 128 rows x 64 cols (one swizzle panel)
-  static constexpr int kPanels = D / 64;
+  static constexpr int kTileBytes = kBM * D * E;    // 128 rows x D elements
+  static constexpr int kPanelBytes = kBM * 128;     // 128 rows x 128 bytes (one swizzle panel)
+  static constexpr int kPanelCols = 128 / E;        // elements per panel row
+  static constexpr int kPanels = D * E / 128;
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + kQTiles * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
@@ -144,6 +155,9 @@ struct KParams {
   int fault_drop_k;  // test hook: CTA 0 never loads its first K tile
   int kv_row0;       // key index of row 0 of the K/V tensors (0 unless a block)
   int head_group;    // (b, h) heads whose items are dealt out together
+  const float* q_descale;  // FP8 form: [B * H] each
+  const float* k_descale;
+  const float* v_descale;
 };
 
 struct Item {
@@ -322,24 +336,45 @@ __device__ __forceinline__ float row_max(const uint32_t (&sv)[4][32]) {
   return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
 }
 
-// P = 2^(s * sc - base) packed as bf16 pairs (P[2c] low, P[2c+1] high), its
-// row sum, and the raw row max of the scores.
+// P = 2^(s * sc - base), its row sum, and the raw row max of the scores.  P is
+// packed as bf16 pairs (P[2c] low, P[2c+1] high) into pk[0..1][32], or for
+// the FP8 form as E4M3 quads (P[4c] lowest byte) into pk[0][32].
+template <bool kFp8 = false>
 __device__ __forceinline__ void exponentials(const uint32_t (&sv)[4][32], float sc, float base,
                                              uint32_t (&pk)[2][32], float& lsum, float& mx) {
   float ls[4] = {0.f, 0.f, 0.f, 0.f};
   float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  if constexpr (kFp8) {
 #pragma unroll
-  for (int ch = 0; ch < 4; ++ch)
+    for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
-    for (int x = 0; x < 16; ++x) {
-      const float s0 = __uint_as_float(sv[ch][2 * x]);
-      const float s1 = __uint_as_float(sv[ch][2 * x + 1]);
-      m[ch] = max3(m[ch], s0, s1);
-      const float p0 = ptx::ex2(fmaf(s0, sc, -base));
-      const float p1 = ptx::ex2(fmaf(s1, sc, -base));
-      ls[ch] += p0 + p1;
-      pk[ch >> 1][(ch & 1) * 16 + x] = ptx::pack_bf16(p0, p1);
-    }
+      for (int x = 0; x < 8; ++x) {
+        const float s0 = __uint_as_float(sv[ch][4 * x]);
+        const float s1 = __uint_as_float(sv[ch][4 * x + 1]);
+        const float s2 = __uint_as_float(sv[ch][4 * x + 2]);
+        const float s3 = __uint_as_float(sv[ch][4 * x + 3]);
+        m[ch] = max3(m[ch], max3(s0, s1, s2), s3);
+        const float p0 = ptx::ex2(fmaf(s0, sc, -base));
+        const float p1 = ptx::ex2(fmaf(s1, sc, -base));
+        const float p2 = ptx::ex2(fmaf(s2, sc, -base));
+        const float p3 = ptx::ex2(fmaf(s3, sc, -base));
+        ls[ch] += (p0 + p1) + (p2 + p3);
+        pk[0][ch * 8 + x] = ptx::pack_e4m3x4(p0, p1, p2, p3);
+      }
+  } else {
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+      for (int x = 0; x < 16; ++x) {
+        const float s0 = __uint_as_float(sv[ch][2 * x]);
+        const float s1 = __uint_as_float(sv[ch][2 * x + 1]);
+        m[ch] = max3(m[ch], s0, s1);
+        const float p0 = ptx::ex2(fmaf(s0, sc, -base));
+        const float p1 = ptx::ex2(fmaf(s1, sc, -base));
+        ls[ch] += p0 + p1;
+        pk[ch >> 1][(ch & 1) * 16 + x] = ptx::pack_bf16(p0, p1);
+      }
+  }
   lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
   mx = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
 }
@@ -439,12 +474,12 @@ __device__ __forceinline__ void fast_pass(uint32_t tS, int c_lo, int c_hi, float
 }
 
 // ---------------------------------------------------------------- kernel
-template <int D, bool kPartial>
-__global__ void __launch_bounds__(kThreads, 1)
-    ring_attn_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q,
-                          const __grid_constant__ CUtensorMap tmap_k,
-                          const __grid_constant__ CUtensorMap tmap_v, const KParams p) {
-  using Lay = Layout<D>;
+// The body shared by the bf16 and the FP8 kernels (see the wrappers below).
+template <int D, bool kPartial, bool kFp8>
+__device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
+                                          const CUtensorMap& tmap_v, const KParams& p) {
+  static_assert(!(kFp8 && kPartial), "the FP8 form has no step epilogue");
+  using Lay = Layout<D, kFp8 ? 1 : 2>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -521,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int pn = 0; pn < Lay::kPanels; ++pn)
             ptx::tma_load_4d(sbase + Lay::kQOff + t * Lay::kTileBytes + pn * Lay::kPanelBytes,
-                             &tmap_q, bar(kQFull), pn * 64, it.h, it.q0[t], it.b);
+                             &tmap_q, bar(kQFull), pn * Lay::kPanelCols, it.h, it.q0[t], it.b);
         ++q_iter;
         for (int f = it.F_lo; f <= it.F_hi; ++f) {
           const uint32_t st = kv_iter % kStages;
@@ -537,14 +572,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_arrive_expect_tx(bar(kKFull + st), Lay::kTileBytes);
             for (int pn = 0; pn < Lay::kPanels; ++pn)
               ptx::tma_load_4d(sbase + Lay::kKOff + st * Lay::kTileBytes + pn * Lay::kPanelBytes,
-                               &tmap_k, bar(kKFull + st), pn * 64, it.h, ks - p.kv_row0, it.b);
+                               &tmap_k, bar(kKFull + st), pn * Lay::kPanelCols, it.h,
+                               ks - p.kv_row0, it.b);
             if (st == 0) ++k_armed0; else ++k_armed1;
           }
           if (!wait1(bar(kVEmpty + st), ph ^ 1u, abort_flag, p)) { ok = false; break; }
           ptx::mbar_arrive_expect_tx(bar(kVFull + st), Lay::kTileBytes);
-          for (int pn = 0; pn < Lay::kPanels; ++pn)
-            ptx::tma_load_4d(sbase + Lay::kVOff + st * Lay::kTileBytes + pn * Lay::kPanelBytes,
-                             &tmap_v, bar(kVFull + st), pn * 64, it.h, ks - p.kv_row0, it.b);
+          if constexpr (kFp8) {
+            // V^T [B, H, d, S]: one box of 128 keys x D rows (keys contiguous)
+            ptx::tma_load_4d(sbase + Lay::kVOff + st * Lay::kTileBytes, &tmap_v,
+                             bar(kVFull + st), ks - p.kv_row0, 0, it.h, it.b);
+          } else {
+            for (int pn = 0; pn < Lay::kPanels; ++pn)
+              ptx::tma_load_4d(sbase + Lay::kVOff + st * Lay::kTileBytes + pn * Lay::kPanelBytes,
+                               &tmap_v, bar(kVFull + st), pn * Lay::kPanelCols, it.h,
+                               ks - p.kv_row0, it.b);
+          }
           if (st == 0) ++v_armed0; else ++v_armed1;
           ++kv_iter;
         }
@@ -559,8 +602,11 @@ __global__ void __launch_bounds__(kThreads, 1)
    } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(kBM, kBN, false);
-      constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kBM, D, true);
+      constexpr uint32_t kIdescQK =
+          kFp8 ? ptx::idesc_e4m3_f32(kBM, kBN) : ptx::idesc_bf16_f32(kBM, kBN, false);
+      constexpr uint32_t kIdescPV =
+          kFp8 ? ptx::idesc_e4m3_f32(kBM, D) : ptx::idesc_bf16_f32(kBM, D, true);
+      constexpr int kKStep = 32 / (kFp8 ? 1 : 2);  // K elements per MMA (32 bytes)
       uint32_t kv_iter = 0, q_iter = 0;
       uint32_t p_cnt0 = 0, p_cnt1 = 0;
       bool ok = true;
@@ -572,25 +618,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       // never carries into the offsets above it.)
       const uint64_t d_qk = ptx::smem_desc_sw128(sbase, 16, 1024);
       const uint64_t d_v = ptx::smem_desc_sw128(sbase, Lay::kPanelBytes, 1024);
-      // O_t (+)= P_t V: P_t from TMEM, V (MN-major) from the given stage.
+      // O_t (+)= P_t V: P_t from TMEM (8 columns per K step in both forms),
+      // V MN-major (bf16) or V^T K-major (FP8) from the given stage.
       auto issue_pv = [&](int t, uint32_t st, bool first) {
-        const uint64_t dv = d_v + ((Lay::kVOff + st * Lay::kTileBytes) >> 4);
+        if constexpr (kFp8) {
+          const uint64_t dv = d_qk + ((Lay::kVOff + st * Lay::kTileBytes) >> 4);
 #pragma unroll
-        for (int s = 0; s < kBN / 16; ++s) {
-          ptx::mma_ts(tmem_base + 256 + t * D, tmem_base + t * 128 + s * 8,
-                      dv + static_cast<uint64_t>((s * 16 * 128) >> 4), kIdescPV,
-                      (first && s == 0) ? 0u : 1u);
+          for (int s = 0; s < kBN / kKStep; ++s)
+            ptx::mma_ts_f8(tmem_base + 256 + t * D, tmem_base + t * 128 + s * 8,
+                           dv + static_cast<uint64_t>((s * 32) >> 4), kIdescPV,
+                           (first && s == 0) ? 0u : 1u);
+        } else {
+          const uint64_t dv = d_v + ((Lay::kVOff + st * Lay::kTileBytes) >> 4);
+#pragma unroll
+          for (int s = 0; s < kBN / 16; ++s) {
+            ptx::mma_ts(tmem_base + 256 + t * D, tmem_base + t * 128 + s * 8,
+                        dv + static_cast<uint64_t>((s * 16 * 128) >> 4), kIdescPV,
+                        (first && s == 0) ? 0u : 1u);
+          }
         }
         ptx::mma_commit(bar(kOBar + t));
       };
-      // S_t = Q_t K^T (both K-major, 128-byte swizzled panels of 64 columns).
+      // S_t = Q_t K^T (both K-major, 128-byte swizzled panels; a K step is
+      // 32 bytes, four steps per panel).
       auto issue_s = [&](int t, uint32_t st) {
         const uint64_t dq = d_qk + ((Lay::kQOff + t * Lay::kTileBytes) >> 4);
         const uint64_t dk = d_qk + ((Lay::kKOff + st * Lay::kTileBytes) >> 4);
 #pragma unroll
-        for (int s = 0; s < D / 16; ++s) {
+        for (int s = 0; s < D / kKStep; ++s) {
           const uint64_t step = static_cast<uint64_t>(((s >> 2) * Lay::kPanelBytes + (s & 3) * 32) >> 4);
-          ptx::mma_ss(tmem_base + t * 128, dq + step, dk + step, kIdescQK, s > 0 ? 1u : 0u);
+          if constexpr (kFp8)
+            ptx::mma_ss_f8(tmem_base + t * 128, dq + step, dk + step, kIdescQK, s > 0 ? 1u : 0u);
+          else
+            ptx::mma_ss(tmem_base + t * 128, dq + step, dk + step, kIdescQK, s > 0 ? 1u : 0u);
         }
         ptx::mma_commit(bar(kSFull + t));
       };
@@ -673,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem_base + lane_off + static_cast<uint32_t>(t * 128);
     const uint32_t tO = tmem_base + lane_off + 256u + static_cast<uint32_t>(t * D);
-    const float sc = p.scale_log2;
+    float sc = p.scale_log2;
     uint32_t s_cnt = 0, pv_cnt = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -686,6 +746,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int f_lo = t ? it.f_lo[1] : it.f_lo[0];
       const int f_hi = t ? it.f_hi[1] : it.f_hi[0];
       if (rows == 0) continue;
+      const int bh = it.b * p.H + it.h;
+      if constexpr (kFp8) sc = p.scale_log2 * __ldg(p.q_descale + bh) * __ldg(p.k_descale + bh);
       const bool row_valid = row_in_tile < rows;
       const int r = (t ? it.q0[1] : it.q0[0]) + row_in_tile;
       int klo_r = 0, khi_r = -1;
@@ -722,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float lsum, mx;
         float alpha = 1.f;
         bool rescale_o = false;
-        const bool fast = CPRING_FUSED_NOMAX && !kPartial &&
+        const bool fast = CPRING_FUSED_NOMAX && !kPartial && !kFp8 &&
                           !__any_sync(0xffffffffu, m_used == -INFINITY);
         if (fast) {
           fast_pass(tS, c_lo, c_hi, sc, m_used, sv, pk, lsum);
@@ -739,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               l_run *= alpha;
               m_used = m_tile;
             }
-            exponentials(sv, sc, m_used, pk, lsum, mx);
+            exponentials<kFp8>(sv, sc, m_used, pk, lsum, mx);
           }
         } else {
         load_scores(tS, c_lo, c_hi, sv);
@@ -754,13 +816,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             l_run *= alpha;
             m_used = m_tile;
           }
-          exponentials(sv, sc, (m_used == -INFINITY) ? 0.f : m_used, pk, lsum, mx);
+          exponentials<kFp8>(sv, sc, (m_used == -INFINITY) ? 0.f : m_used, pk, lsum, mx);
         } else {
           // Exponentials against the current reference; the row max is
           // taken in the same pass and only forces a redo (rare) when it
           // moved more than 2^8 above the reference.
           {
-            exponentials(sv, sc, m_used, pk, lsum, mx);
+            exponentials<kFp8>(sv, sc, m_used, pk, lsum, mx);
             const float m_tile = mx * sc;
             m_true = fmaxf(m_true, m_tile);
             const bool redo = m_tile > m_used + kRescaleLog2;
@@ -772,14 +834,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_used = m_tile;
               }
               load_scores(tS, c_lo, c_hi, sv);  // S is still in TMEM: P not yet written
-              exponentials(sv, sc, m_used, pk, lsum, mx);
+              exponentials<kFp8>(sv, sc, m_used, pk, lsum, mx);
             }
           }
         }
         }
         l_run += lsum;
         ptx::tmem_st32(tS, pk[0]);
-        ptx::tmem_st32(tS + 32, pk[1]);
+        if constexpr (!kFp8) ptx::tmem_st32(tS + 32, pk[1]);
         if (__any_sync(0xffffffffu, rescale_o)) {
           // O_t holds the sum up to the previous tile once that PV is done.
           if (!wait_warp(bar(kOBar + t), (pv_cnt - 1u) & 1u, abort_flag, p)) { ok = false; break; }
@@ -805,7 +867,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait_warp(bar(kOBar + t), (pv_cnt - 1u) & 1u, abort_flag, p)) { ok = false; break; }
       ptx::tc_fence_after();
       if (!kPartial) {
-        const float inv_l = 1.f / l_run;
+        const float inv_l = (kFp8 ? __ldg(p.v_descale + bh) : 1.f) / l_run;
         uint4* dst = reinterpret_cast<uint4*>(
             p.out + ((static_cast<size_t>(it.b) * p.S + r) * p.H + it.h) * D);
 #pragma unroll
@@ -872,6 +934,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+template <int D, bool kPartial>
+__global__ void __launch_bounds__(kThreads, 1)
+    ring_attn_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                          const __grid_constant__ CUtensorMap tmap_k,
+                          const __grid_constant__ CUtensorMap tmap_v, const KParams p) {
+  attn_body<D, kPartial, false>(tmap_q, tmap_k, tmap_v, p);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    ring_attn_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                         const __grid_constant__ CUtensorMap tmap_k,
+                         const __grid_constant__ CUtensorMap tmap_v, const KParams p) {
+  attn_body<D, false, true>(tmap_q, tmap_k, tmap_v, p);
+}
+
 // ---------------------------------------------------------------- host side
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -892,17 +970,37 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [B, S, H, D] bf16 viewed as a 4-D tensor (D, H, S, B); box = 64 x 1 x 128 x 1.
-bool make_map(CUtensorMap* m, const void* base, int B, int S, int H, int D) {
+// [B, S, H, D] viewed as a 4-D tensor (D, H, S, B) of E-byte elements;
+// box = one 128-byte panel x 1 x 128 rows x 1.
+bool make_map(CUtensorMap* m, const void* base, int B, int S, int H, int D, int E = 2) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
+  const cuuint64_t e = static_cast<cuuint64_t>(E);
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
                         static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
-                           static_cast<cuuint64_t>(S) * H * D * 2};
-  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kBM), 1};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * e, static_cast<cuuint64_t>(H) * D * e,
+                           static_cast<cuuint64_t>(S) * H * D * e};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / E), 1, static_cast<cuuint32_t>(kBM), 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+  CUresult r = fn(m, E == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
+                  const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// V^T [B, H, D, S] of bytes viewed as (S, D, H, B); box = 128 keys x D rows.
+// Needs S % 16 == 0 (row stride a multiple of 16 bytes).
+bool make_map_vt8(CUtensorMap* m, const void* base, int B, int S, int H, int D) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(D),
+                        static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(D) * S,
+                           static_cast<cuuint64_t>(H) * D * S};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(kBN), static_cast<cuuint32_t>(D), 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides,
                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -912,11 +1010,15 @@ bool make_map(CUtensorMap* m, const void* base, int B, int S, int H, int D) {
 std::atomic<int> g_fault_drop_k{0};
 std::atomic<unsigned long long> g_wait_limit_ns{kTimeoutNs};
 
-template <int D, bool kPartial>
+template <int D, bool kPartial, bool kFp8 = false>
 cudaError_t launch_t(const AttnArgs& a, cudaStream_t stream) {
-  using Lay = Layout<D>;
+  using Lay = Layout<D, kFp8 ? 1 : 2>;
   static_assert(Lay::kAlloc <= 232448, "shared memory budget");
-  auto kern = ring_attn_bf16_kernel<D, kPartial>;
+  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, KParams);
+  if constexpr (kFp8)
+    kern = ring_attn_fp8_kernel<D>;
+  else
+    kern = ring_attn_bf16_kernel<D, kPartial>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
@@ -926,9 +1028,16 @@ cudaError_t launch_t(const AttnArgs& a, cudaStream_t stream) {
 
   CUtensorMap mq, mk, mv;
   const int kv_rows = a.kv_rows > 0 ? a.kv_rows : a.S;
-  if (!make_map(&mq, a.q, a.B, a.S, a.H, D) || !make_map(&mk, a.k, a.B, kv_rows, a.H, D) ||
-      !make_map(&mv, a.v, a.B, kv_rows, a.H, D))
-    return cudaErrorInvalidValue;
+  if constexpr (kFp8) {
+    if (a.kv_rows > 0) return cudaErrorInvalidValue;  // the FP8 form reads whole tensors
+    if (!make_map(&mq, a.q, a.B, a.S, a.H, D, 1) || !make_map(&mk, a.k, a.B, a.S, a.H, D, 1) ||
+        !make_map_vt8(&mv, a.v, a.B, a.S, a.H, D))
+      return cudaErrorInvalidValue;
+  } else {
+    if (!make_map(&mq, a.q, a.B, a.S, a.H, D) || !make_map(&mk, a.k, a.B, kv_rows, a.H, D) ||
+        !make_map(&mv, a.v, a.B, kv_rows, a.H, D))
+      return cudaErrorInvalidValue;
+  }
 
   KParams p{};
   p.B = a.B;
@@ -954,6 +1063,9 @@ cudaError_t launch_t(const AttnArgs& a, cudaStream_t stream) {
   p.o_part = a.o_part;
   p.m_part = a.m_part;
   p.l_part = a.l_part;
+  p.q_descale = a.q_descale;
+  p.k_descale = a.k_descale;
+  p.v_descale = a.v_descale;
   p.err = device_error_word();
   if (!p.err) return cudaErrorInvalidValue;
   p.timeout_ns = g_wait_limit_ns.load();
@@ -989,6 +1101,13 @@ cudaError_t launch_attn_bf16(const AttnArgs& a, cudaStream_t stream) {
   if (a.d == 128) return partial ? launch_t<128, true>(a, stream) : launch_t<128, false>(a, stream);
   if (a.d == 64) return partial ? launch_t<64, true>(a, stream) : launch_t<64, false>(a, stream);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attn_fp8(const AttnArgs& a, cudaStream_t stream) {
+  if (a.d != 128 || a.k_shard >= 0 || a.q_shard >= 0 || !a.q_descale || !a.k_descale ||
+      !a.v_descale)
+    return cudaErrorInvalidValue;
+  return launch_t<128, false, true>(a, stream);
 }
 
 }  // namespace cpring

@@ -31,6 +31,10 @@ struct AttnArgs {
   float* o_part;
   float* m_part;
   float* l_part;
+  // FP8 form: per-(b, h) descales [B * H] (q, k, v = E4M3 Q, K and V^T)
+  const float* q_descale;
+  const float* k_descale;
+  const float* v_descale;
 };
 
 // Sticky device error word (bits of kErr*), owned by merge.cu.
@@ -42,6 +46,9 @@ int* device_error_word();   // device address for the current device, or null
 // Launchers: return cudaSuccess or the launch error.
 cudaError_t launch_attn_bf16(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_attn_f32(const AttnArgs& a, cudaStream_t stream);
+// FP8 form: q, k E4M3 [B, S, H, 128], v E4M3 [B, H, 128, S]; the fused
+// forward only (q_shard = k_shard = -1).
+cudaError_t launch_attn_fp8(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_doc_scan(const int32_t* doc_offsets, int S, int32_t* doc_info,
                             cudaStream_t stream);
 cudaError_t launch_merge(float* o_acc, float* m_acc, float* l_acc, const float* o_part,

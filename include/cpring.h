@@ -277,10 +277,55 @@ cp_status cp_ulysses_attn_fwd(const void* q, const void* k, const void* v, void*
  */
 void cp_test_set_wait_fault(int drop_first_k_tile, long long wait_limit_ns);
 
-/* Number of tcgen05 kernel launches, fp32 kernel launches, merge/finalize
- * launches and doc-scan launches made by this process so far (host-side
- * counters, for launch accounting in benchmarks). */
+/* Number of tcgen05 kernel launches, fp32 kernel launches, auxiliary
+ * launches (merge, finalize, all-to-all permutation, FP8 quantisation) and
+ * doc-scan launches made by this process so far (host-side counters, for
+ * launch accounting in benchmarks). */
 void cp_launch_counts(int64_t* counts4);
+
+/*
+ * FP8 (E4M3) quantisation of one bf16 tensor, per (b, h).
+ * "上下文並行（Context Parallelism, CP）" (compassingai.com), section
+ * 通訊量分析: the bytes moved depend on whether K/V travel in FP8.  Format:
+ * OCP E4M3 (largest finite 448), one fp32 scale per (b, h):
+ *   amax = max |x| over (S, d);  inv = 448 / amax;  x8 = E4M3(x * inv)
+ *   (each an fp32 operation rounded to nearest, then rounded to the nearest
+ *   E4M3 value, ties to even, saturated at +-448);  descale = amax / 448;
+ *   an all-zero head gets inv = descale = 1.
+ *  x          device, bf16 [B,S,H,d], read only (finite values).
+ *  x8         device, bytes: [B,S,H,d] if transpose == 0 (Q, K), or
+ *             [B,H,d,S] if transpose == 1 (V^T for cp_ring_attn_fwd_fp8).
+ *  descale    device, fp32 [B,H], written (used as scratch during the call).
+ *  B, H       1 .. 65535; S >= 1 (transpose: S % 16 == 0); d 64 or 128.
+ *  Alignment  x, x8 16 bytes; descale 4 bytes.
+ * Four launches on `stream` (a memset and three kernels); no allocation.
+ */
+cp_status cp_fp8_quantize(const void* x, void* x8, float* descale, int B, int S, int H, int d,
+                          int transpose, cudaStream_t stream);
+
+/*
+ * Fused ring-attention forward over FP8 inputs.  Same computation, masks,
+ * sharding and outputs as cp_ring_attn_fwd, applied to the dequantized
+ * inputs q8 * q_descale, k8 * k_descale, v8 * v_descale ("上下文並行", section
+ * 線上 Softmax; FP8 transfer per section 通訊量分析).
+ *  q8, k8     device, E4M3 [B,S,H,d] (cp_fp8_quantize, transpose 0).
+ *  v8t        device, E4M3 [B,H,d,S] (cp_fp8_quantize, transpose 1).
+ *  q_descale, k_descale, v_descale   device, fp32 [B,H].
+ *  out        device, bf16 [B,S,H,d];  lse  device, fp32 [B,H,S].
+ *  d          128 only (others: CP_ERR_UNSUPPORTED).
+ *  Shapes     as cp_ring_attn_fwd, and (S / n_shards) % 16 == 0 so that every
+ *             K/V tile starts on a 16-byte boundary of v8t (else CP_ERR_SHAPE).
+ *  Alignment  q8, k8, v8t, out 16 bytes; descales, lse, doc_offsets 4 bytes.
+ * Both products run on tcgen05 as kind::f8f6f4 with fp32 accumulation; P is
+ * rounded to E4M3 before the PV product (relative error <= 2^-4 per entry),
+ * so the result differs from the exact attention of the dequantized inputs
+ * by up to about 2^-4 max|v| (peaked rows come closest).
+ */
+cp_status cp_ring_attn_fwd_fp8(const void* q8, const void* k8, const void* v8t,
+                               const float* q_descale, const float* k_descale,
+                               const float* v_descale, void* out, float* lse, int B, int S, int H,
+                               int d, int n_shards, int causal, const int32_t* doc_offsets,
+                               cudaStream_t stream);
 
 #ifdef __cplusplus
 }

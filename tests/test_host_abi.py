@@ -113,6 +113,25 @@ def test_rejects_before_any_launch(lib):
     assert z(FAKE, FAKE, FAKE, FAKE, ODD, 1, 8, 2, 64, 1, None) == -4
 
 
+def test_fp8_entry_points_reject_before_any_launch(lib):
+    f = lib.cp_ring_attn_fwd_fp8
+    ok = (FAKE,) * 8
+    assert f(None, *ok[1:], 1, 1024, 2, 128, 4, 1, None, None) == -1
+    assert f(*ok[:4], None, *ok[5:], 1, 1024, 2, 128, 4, 1, None, None) == -1   # a descale
+    assert f(*ok, 1, 1024, 2, 64, 4, 1, None, None) == -3            # d = 128 only
+    assert f(*ok, 1, 1000, 2, 128, 4, 1, None, None) == -2           # S % N != 0
+    assert f(*ok, 1, 1000, 2, 128, 5, 1, None, None) == -2           # 200-row shards: % 16
+    assert f(*ok, 1, 1024, 2, 128, 4, 3, None, None) == -2           # causal flag
+    assert f(ODD, *ok[1:], 1, 1024, 2, 128, 4, 1, None, None) == -4
+    assert f(*ok[:3], V(0x10001), *ok[4:], 1, 1024, 2, 128, 4, 1, None, None) == -4
+    g = lib.cp_fp8_quantize
+    assert g(None, FAKE, FAKE, 1, 64, 2, 128, 0, None) == -1
+    assert g(FAKE, FAKE, FAKE, 1, 64, 2, 96, 0, None) == -3
+    assert g(FAKE, FAKE, FAKE, 1, 40, 2, 128, 1, None) == -2          # V^T needs S % 16 == 0
+    assert g(FAKE, FAKE, FAKE, 1, 64, 2, 128, 2, None) == -2
+    assert g(FAKE, ODD, FAKE, 1, 64, 2, 128, 0, None) == -4
+
+
 @pytest.mark.parametrize("S,N,T", [(64, 4, 16), (96, 3, 8), (48, 4, 5), (40, 2, 7), (32, 8, 4)])
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("ndocs", [0, 1, 3, 6])
