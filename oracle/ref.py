@@ -476,3 +476,110 @@ def attention_fp8(q8, k8, v8, q_descale, k_descale, v_descale, causal: bool = Tr
     of the dequantized Q, K, V.  Returns (out [B,S,H,d], lse [B,H,S])."""
     return attention(fp8_dequantize(q8, q_descale), fp8_dequantize(k8, k_descale),
                      fp8_dequantize(v8, v_descale), causal, doc_offsets)
+
+
+# ---------------------------------------------------------------------------
+# Backward
+# ---------------------------------------------------------------------------
+#
+# "上下文並行" (§反向傳播) says only that the backward walks the K/V blocks of
+# the ring again, with about 2-3x the forward's traffic; "大语言模型并行策略（五）"
+# adds that dK/dV travel with their blocks.  The plainest reading: the exact
+# gradient of the forward, accumulated block by block over the same shard
+# pairs, with the forward's log-sum-exp saved (so P is recomputed, never
+# stored).  With L = sum(out * dout) and, per (b, h), P = softmax of the
+# visible scores S = Q K^T / sqrt(d):
+#   dV = P^T dO;  dP = dO V^T;  D = rowsum(P * dP) = rowsum(dO * O);
+#   dS = P * (dP - D);  dQ = dS K / sqrt(d);  dK = dS^T Q / sqrt(d).
+
+def attention_bwd(q, k, v, dout, causal: bool = True, doc_offsets=None):
+    """(dq, dk, dv), each [B,S,H,d] float64: the gradient of sum(out * dout)
+    for out = attention(q, k, v).  Dense per (b, h): for small S."""
+    q, k, v, dout = (np.asarray(x, dtype=np.float64) for x in (q, k, v, dout))
+    B, S, H, d = q.shape
+    doc = doc_of(S, doc_offsets)
+    mask = visible(np.arange(S), np.arange(S), causal, doc)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for b in range(B):
+        for h in range(H):
+            s = np.where(mask, q[b, :, h] @ k[b, :, h].T / math.sqrt(d), NEG_INF)
+            m = s.max(axis=1, keepdims=True)
+            p = np.where(mask, np.exp(s - m), 0.0)
+            p /= p.sum(axis=1, keepdims=True)
+            do = dout[b, :, h]
+            dv[b, :, h] = p.T @ do
+            dp = do @ v[b, :, h].T
+            ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+            dq[b, :, h] = ds @ k[b, :, h] / math.sqrt(d)
+            dk[b, :, h] = ds.T @ q[b, :, h] / math.sqrt(d)
+    return dq, dk, dv
+
+
+def attention_bwd_rows(q, k, v, dout, b: int, h: int, rows, causal: bool = True,
+                       doc_offsets=None):
+    """dq [len(rows), d] of one (b, h): row q of dQ needs only row q of P and
+    D_q = dO_q . O_q, so this is O(S d) per row."""
+    qf, kf, vf, dof = (np.asarray(x[b, :, h, :], dtype=np.float64) for x in (q, k, v, dout))
+    S, d = qf.shape
+    doc = doc_of(S, doc_offsets)
+    rows = np.asarray(rows)
+    mask = visible(rows, np.arange(S), causal, doc)
+    s = np.where(mask, qf[rows] @ kf.T / math.sqrt(d), NEG_INF)
+    p = np.where(mask, np.exp(s - s.max(axis=1, keepdims=True)), 0.0)
+    p /= p.sum(axis=1, keepdims=True)
+    dp = dof[rows] @ vf.T
+    ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+    return ds @ kf / math.sqrt(d)
+
+
+def ring_backward(q, k, v, dout, n_shards: int, causal: bool = True, doc_offsets=None,
+                  order="ascending"):
+    """The backward walked over the ring's shard pairs: rank i holds Q_i, dO_i
+    and the forward's O_i, lse_i; for every needed j in its visiting order it
+    recomputes P_ij = exp(S_ij - lse_i), adds P_ij^T dO_i to dV_j and
+    dS_ij^T Q_i / sqrt(d) to dK_j (the accumulators that travel with K_j, V_j)
+    and dS_ij K_j / sqrt(d) to dQ_i, with dS_ij = P_ij (dO_i V_j^T - D_i) and
+    D_i = rowsum(dO_i * O_i).  Returns (dq, dk, dv) [B,S,H,d]."""
+    q, k, v, dout = (np.asarray(x, dtype=np.float64) for x in (q, k, v, dout))
+    B, S, H, d = q.shape
+    bounds = shard_bounds(S, n_shards)
+    out, lse = ring_forward(q, k, v, n_shards, causal, doc_offsets)
+    doc = doc_of(S, doc_offsets)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for i in range(n_shards):
+        qa, qb = bounds[i]
+        for j in ring_order(i, n_shards, order):
+            if not shard_needed(i, j, S, n_shards, causal, doc_offsets):
+                continue
+            ka, kb = bounds[j]
+            mask = visible(np.arange(qa, qb), np.arange(ka, kb), causal, doc)
+            for b in range(B):
+                for h in range(H):
+                    s = q[b, qa:qb, h] @ k[b, ka:kb, h].T / math.sqrt(d)
+                    p = np.where(mask, np.exp(np.where(mask, s, 0.0) - lse[b, h, qa:qb, None]), 0.0)
+                    do = dout[b, qa:qb, h]
+                    D = (do * out[b, qa:qb, h]).sum(axis=1, keepdims=True)
+                    ds = p * (do @ v[b, ka:kb, h].T - D)
+                    dv[b, ka:kb, h] += p.T @ do
+                    dk[b, ka:kb, h] += ds.T @ q[b, qa:qb, h] / math.sqrt(d)
+                    dq[b, qa:qb, h] += ds @ k[b, ka:kb, h] / math.sqrt(d)
+    return dq, dk, dv
+
+
+def zero_query_dv_closed_form(dout, causal: bool = True, doc_offsets=None):
+    """With Q = 0, P is uniform over each query's visible keys, so
+    dV_k = sum over the queries q that see k of dO_q / count_q.  Causal: the
+    queries of k's document from k on (a suffix sum); otherwise the whole
+    document.  O(S d) per (b, h).  Returns dv [B,S,H,d]."""
+    dout = np.asarray(dout, dtype=np.float64)
+    B, S, H, d = dout.shape
+    doc = doc_of(S, doc_offsets)
+    offs = [0, S] if doc_offsets is None else [int(x) for x in doc_offsets]
+    start = np.asarray(offs)[doc]
+    end = np.asarray(offs)[doc + 1]
+    pos = np.arange(S)
+    cnt = ((pos + 1 if causal else end) - start).astype(np.float64)
+    w = dout / cnt[None, :, None, None]
+    csum = np.concatenate([np.zeros((B, 1, H, d)), np.cumsum(w, axis=1)], axis=1)
+    lo = pos if causal else start
+    return csum[:, end] - csum[:, lo]

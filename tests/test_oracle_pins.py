@@ -416,3 +416,88 @@ def test_attention_fp8_is_attention_of_dequantized_inputs(causal, docs):
     c_o, c_l = ref.zero_query_closed_form(ref.fp8_dequantize(v8, vd), causal, docs)
     np.testing.assert_allclose(o0, c_o, atol=1e-12, rtol=0)
     np.testing.assert_allclose(lse0, c_l, atol=1e-12, rtol=0)
+
+
+# ---------------------------------------------------------------------------
+# Backward
+# ---------------------------------------------------------------------------
+
+def _autograd_bwd(q, k, v, dout, causal, docs):
+    """torch autograd of SDPA in fp64 ([B,S,H,d] in/out)."""
+    tq, tk, tv = (torch.from_numpy(x).permute(0, 2, 1, 3).clone().requires_grad_(True)
+                  for x in (q, k, v))
+    B, S, H, d = q.shape
+    if docs is None:
+        o = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=causal)
+    else:
+        doc = torch.zeros(S, dtype=torch.long)
+        for t, (a, b) in enumerate(zip(docs[:-1], docs[1:])):
+            doc[a:b] = t
+        mask = doc[:, None] == doc[None, :]
+        if causal:
+            mask &= torch.ones(S, S, dtype=torch.bool).tril()
+        o = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask)
+    (o * torch.from_numpy(dout).permute(0, 2, 1, 3)).sum().backward()
+    return tuple(t.grad.permute(0, 2, 1, 3).numpy() for t in (tq, tk, tv))
+
+
+BWD_CASES = [(True, None), (False, None), (True, [0, 9, 10, 31, 48]), (False, [0, 20, 48])]
+
+
+@pytest.mark.parametrize("causal,docs", BWD_CASES)
+def test_attention_bwd_matches_autograd(causal, docs):
+    q, k, v = _qkv(2, 48, 2, 16, 31)
+    dout = _qkv(2, 48, 2, 16, 32)[0]
+    got = ref.attention_bwd(q, k, v, dout, causal, docs)
+    want = _autograd_bwd(q, k, v, dout, causal, docs)
+    for g, w_ in zip(got, want):
+        np.testing.assert_allclose(g, w_, atol=1e-12, rtol=0)
+
+
+def test_attention_bwd_finite_differences():
+    q, k, v = _qkv(1, 6, 1, 3, 33)
+    dout = _qkv(1, 6, 1, 3, 34)[0]
+    grads = ref.attention_bwd(q, k, v, dout, True, [0, 4, 6])
+    eps = 1e-6
+    for which, g in enumerate(grads):
+        for idx in itertools.product(range(6), range(3)):
+            arrs = [q.copy(), k.copy(), v.copy()]
+            arrs[which][0, idx[0], 0, idx[1]] += eps
+            up = (ref.attention(*arrs, True, [0, 4, 6])[0] * dout).sum()
+            arrs[which][0, idx[0], 0, idx[1]] -= 2 * eps
+            dn = (ref.attention(*arrs, True, [0, 4, 6])[0] * dout).sum()
+            assert abs((up - dn) / (2 * eps) - g[0, idx[0], 0, idx[1]]) < 1e-7
+
+
+@pytest.mark.parametrize("causal,docs", BWD_CASES)
+@pytest.mark.parametrize("N,order", [(1, "ascending"), (4, "ascending"), (4, "ring"),
+                                     (3, [2, 0, 1])])
+def test_ring_backward_equals_the_gradient(causal, docs, N, order):
+    q, k, v = _qkv(1, 48, 2, 8, 35)
+    dout = _qkv(1, 48, 2, 8, 36)[0]
+    got = ref.ring_backward(q, k, v, dout, N, causal, docs, order)
+    want = ref.attention_bwd(q, k, v, dout, causal, docs)
+    for g, w_ in zip(got, want):
+        np.testing.assert_allclose(g, w_, atol=1e-12, rtol=0)
+
+
+@pytest.mark.parametrize("causal,docs", BWD_CASES)
+def test_attention_bwd_closed_forms_and_invariants(causal, docs):
+    q, k, v = _qkv(1, 48, 2, 8, 37)
+    dout = _qkv(1, 48, 2, 8, 38)[0]
+    # constant V: out is constant, so dQ = dK = 0 (dS vanishes)
+    vc = np.broadcast_to(v[:, :1], v.shape).copy()
+    dq, dk, _ = ref.attention_bwd(q, k, vc, dout, causal, docs)
+    assert np.abs(dq).max() < 1e-12 and np.abs(dk).max() < 1e-12
+    # Q = 0: dV is the suffix (causal) or document sum of dO / count
+    _, _, dv0 = ref.attention_bwd(np.zeros_like(q), k, v, dout, causal, docs)
+    np.testing.assert_allclose(dv0, ref.zero_query_dv_closed_form(dout, causal, docs),
+                               atol=1e-12, rtol=0)
+    # rows of P sum to 1 and rows of dS sum to 0
+    dq, dk, dv = ref.attention_bwd(q, k, v, dout, causal, docs)
+    np.testing.assert_allclose(dv.sum(axis=1), dout.sum(axis=1), atol=1e-12)
+    assert np.abs(dk.sum(axis=1)).max() < 1e-12
+    # the row form of dQ
+    rows = np.array([0, 5, 17, 47])
+    np.testing.assert_allclose(ref.attention_bwd_rows(q, k, v, dout, 0, 1, rows, causal, docs),
+                               dq[0, rows, 1], atol=1e-12, rtol=0)
