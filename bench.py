@@ -560,6 +560,68 @@ def run_fp8(args, w, local):
     }
 
 
+def run_bwd(args, w, local):
+    """Time the backward (cp_ring_attn_bwd: the row sums D, the dK/dV kernel
+    and the dQ kernel) on the workload, after one forward for its out and
+    lse.  Algorithmic work: 10 d FLOPs per visible pair (dP, dV, dK, dQ and
+    the recomputed S, 2 d each); the two kernels execute 14 d (S and dP are
+    formed in both).  Roofline against the bf16 dense peak.  One JSON line."""
+    import context_ring_attention_fwd_gb300 as pkg
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    q, k, v = inputs.make_qkv(w.B, w.S, w.H, w.d, w.seed, w.torch_dtype, w.scale, device=str(dev))
+    dout = inputs.make_qkv(w.B, w.S, w.H, w.d, w.seed + 50, w.torch_dtype, device=str(dev))[0]
+    docs = (inputs.make_doc_offsets(w.S, w.seed + 1, w.doc_min, w.doc_max)
+            if w.packed_docs else None)
+    dd = pkg.doc_offsets_tensor(docs, dev)
+    stream = torch.cuda.current_stream(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
+    pkg.cp_ring_attn_fwd(q, k, v, out, lse, w.n_shards, w.causal, dd, stream)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    ws = torch.empty(pkg.cp_ring_attn_bwd_workspace_bytes(w.B, w.S, w.H, w.d, w.n_shards),
+                     dtype=torch.uint8, device=dev)
+
+    def step():
+        pkg.cp_ring_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, w.n_shards, w.causal, dd, ws,
+                             stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(gpu_index(local))
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = pkg.launch_counts()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    launches1 = pkg.launch_counts()
+    clk = clocks.stop()
+    if pkg.cp_get_last_status(stream) != 0:
+        raise RuntimeError("device error in the backward")
+    ms = e0.elapsed_time(e1) / args.steps
+    fwd_flops = effective_flops(w, docs)        # 4 d per visible pair
+    flops = fwd_flops * 10 // 4
+    achieved = flops / (ms * 1e-3) / 1e12
+    peak_burst, peak_sust, peak_src = measured_peaks()
+    return {
+        "metric": "effective TFLOP/s of the ring-attention backward (1 GB300)", "impl": "bwd",
+        "unit": UNIT, "value": achieved, "ms_per_step": ms, "higher_is_better": True,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_burst,
+                     "unit": "TFLOP/s", "frac": achieved / peak_burst, "traffic": None,
+                     "peak_kind": f"{peak_src} bf16 dense burst (cuBLAS)",
+                     "executed_tflops": achieved * 14 / 10},
+        "gpu_launches": int(sum(launches1) - sum(launches0)),
+        "clocks": clk, "steps": args.steps, "warmup": args.warmup, "n_gpus": 1,
+        "dtype": w.dtype, "data": "synthetic", "config": _config(w, docs, 1),
+    }
+
+
 def measured_peaks_hbm():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -585,6 +647,7 @@ def main(argv=None):
                     help="time the all-to-all (Ulysses) form instead")
     ap.add_argument("--fp8", action="store_true",
                     help="time the FP8 (E4M3) form instead")
+    ap.add_argument("--bwd", action="store_true", help="time the backward instead")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the attention kernel from an ncu capture")
     args = ap.parse_args(argv)
@@ -592,9 +655,10 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_env()
     w = inputs.BY_NAME[args.workload]
-    if args.ring_emulation or args.ulysses or args.fp8:
+    if args.ring_emulation or args.ulysses or args.fp8 or args.bwd:
         line = (run_ring_emulation(args, w, local) if args.ring_emulation
-                else run_ulysses(args, w, local) if args.ulysses else run_fp8(args, w, local))
+                else run_ulysses(args, w, local) if args.ulysses
+                else run_fp8(args, w, local) if args.fp8 else run_bwd(args, w, local))
         if rank == 0:
             print(json.dumps(line), flush=True)
         return

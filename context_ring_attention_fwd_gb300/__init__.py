@@ -19,7 +19,8 @@ import torch
 
 from ._binding import (  # noqa: F401
     CP_OK, STATUS_CODES, STATUS_NAMES, CpError, LIB_PATH, cp_fp8_quantize, cp_get_last_status,
-    cp_lse_finalize, cp_lse_merge, cp_ring_attn_fwd, cp_ring_attn_fwd_emulated,
+    cp_lse_finalize, cp_lse_merge, cp_ring_attn_bwd, cp_ring_attn_bwd_workspace_bytes,
+    cp_ring_attn_fwd, cp_ring_attn_fwd_emulated,
     cp_ring_attn_fwd_f32, cp_ring_attn_fwd_fp8,
     cp_ring_emulated_workspace_bytes, cp_ring_schedule, cp_ring_step, cp_ulysses_attn_fwd,
     cp_ulysses_workspace_bytes,
@@ -31,6 +32,7 @@ __all__ = [
     "cp_lse_finalize", "cp_ring_schedule", "cp_ring_traffic", "cp_get_last_status",
     "cp_status_string", "ring_attn_fwd", "ring_attn_fwd_host", "ring_attn_composed",
     "cp_fp8_quantize", "cp_ring_attn_fwd_fp8", "fp8_quantize_qkv", "ring_attn_fwd_fp8",
+    "cp_ring_attn_bwd", "ring_attn_bwd",
     "CpError", "lib",
 ]
 
@@ -159,3 +161,14 @@ def ring_attn_fwd_fp8(fp8_inputs, n_shards: int = 1, causal: bool = True, doc_of
     docs = doc_offsets_tensor(doc_offsets, q8.device)
     cp_ring_attn_fwd_fp8(q8, k8, v8t, qd, kd, vd, out, lse, n_shards, causal, docs, stream)
     return out, lse
+
+
+def ring_attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor,
+                  lse: torch.Tensor, dout: torch.Tensor, n_shards: int = 1, causal: bool = True,
+                  doc_offsets=None, stream=None):
+    """The bf16 backward for the forward's (out, lse): allocates and returns
+    (dq, dk, dv) [B,S,H,d] bf16."""
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    docs = doc_offsets_tensor(doc_offsets, q.device)
+    cp_ring_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, n_shards, causal, docs, None, stream)
+    return dq, dk, dv

@@ -49,6 +49,9 @@ _SIGS = {
     "cp_ring_attn_fwd_emulated": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _i64,
                                   _vp, _vp, ctypes.POINTER(_i64)],
     "cp_fp8_quantize": [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp],
+    "cp_ring_attn_bwd_workspace_bytes": [_i, _i, _i, _i, _i],
+    "cp_ring_attn_bwd": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp,
+                         _vp, _i64, _vp],
     "cp_ring_attn_fwd_fp8": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp,
                              _vp],
 }
@@ -80,7 +83,8 @@ def lib() -> ctypes.CDLL:
                     fn.restype = ctypes.c_char_p
                 elif name in ("cp_launch_counts", "cp_test_set_wait_fault"):
                     fn.restype = None
-                elif name in ("cp_ring_emulated_workspace_bytes", "cp_ulysses_workspace_bytes"):
+                elif name in ("cp_ring_emulated_workspace_bytes", "cp_ulysses_workspace_bytes",
+                              "cp_ring_attn_bwd_workspace_bytes"):
                     fn.restype = _i64
                 else:
                     fn.restype = _i
@@ -174,6 +178,34 @@ def cp_ring_attn_fwd_fp8(q8, k8, v8t, q_descale, k_descale, v_descale, out, lse,
         _ptr(q8), _ptr(k8), _ptr(v8t), _ptr(q_descale), _ptr(k_descale), _ptr(v_descale),
         _ptr(out), _ptr(lse), B, S, H, d, int(n_shards), int(bool(causal)), _ptr(doc_offsets),
         _stream(stream)))
+
+
+def cp_ring_attn_bwd_workspace_bytes(B: int, S: int, H: int, d: int, n_shards: int) -> int:
+    return int(lib().cp_ring_attn_bwd_workspace_bytes(B, S, H, d, n_shards))
+
+
+def cp_ring_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, n_shards: int, causal: bool = True,
+                     doc_offsets: Optional[torch.Tensor] = None, workspace=None,
+                     stream=None) -> None:
+    """bf16 backward: q, k, v, out, dout, dq, dk, dv [B,S,H,d] bf16, lse
+    [B,H,S] fp32; workspace a uint8 device tensor of at least
+    cp_ring_attn_bwd_workspace_bytes bytes (allocated here if None)."""
+    B, S, H, d = q.shape
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"),
+                 (dk, "dk"), (dv, "dv")):
+        _need(t, n, torch.bfloat16, (B, S, H, d))
+    _need(lse, "lse", torch.float32, (B, H, S))
+    if doc_offsets is not None:
+        _need(doc_offsets, "doc_offsets", torch.int32)
+    need = cp_ring_attn_bwd_workspace_bytes(B, S, H, d, int(n_shards))
+    if need < 0:
+        raise CpError("cp_ring_attn_bwd_workspace_bytes", STATUS_CODES["CP_ERR_SHAPE"])
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check("cp_ring_attn_bwd", lib().cp_ring_attn_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+        _ptr(dv), B, S, H, d, int(n_shards), int(bool(causal)), _ptr(doc_offsets),
+        _ptr(workspace), int(workspace.numel()), _stream(stream)))
 
 
 def cp_ring_attn_fwd_noalloc(q, k, v, out, lse, n_shards: int, causal: bool = True,

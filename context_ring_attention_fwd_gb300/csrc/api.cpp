@@ -123,6 +123,46 @@ cp_status cp_ring_attn_fwd_fp8(const void* q8, const void* k8, const void* v8t,
   return run_attn(a, 2, stream);
 }
 
+int64_t cp_ring_attn_bwd_workspace_bytes(int B, int S, int H, int d, int n_shards) {
+  if (check_shape(B, S, H, d, n_shards) != CP_OK) return -1;
+  const int64_t delta = static_cast<int64_t>(B) * H * S * 4;
+  return (delta + 255) / 256 * 256 + 256;  // D, then the doc-scan word
+}
+
+cp_status cp_ring_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                           const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                           int B, int S, int H, int d, int n_shards, int causal,
+                           const int32_t* doc_offsets, void* workspace, int64_t workspace_bytes,
+                           cudaStream_t stream) {
+  if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || !workspace)
+    return CP_ERR_NULL;
+  cp_status st = check_shape(B, S, H, d, n_shards);
+  if (st != CP_OK) return st;
+  if (d != 64 && d != 128) return CP_ERR_UNSUPPORTED;
+  if (causal != 0 && causal != 1) return CP_ERR_SHAPE;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(lse, 4) || !aligned(doc_offsets, 4) || !aligned(workspace, 256))
+    return CP_ERR_ALIGN;
+  const int64_t need = cp_ring_attn_bwd_workspace_bytes(B, S, H, d, n_shards);
+  if (workspace_bytes < need) return CP_ERR_BUFFER;
+  st = check_device();
+  if (st != CP_OK) return st;
+  cpring::BwdArgs a{};
+  a.q = q; a.k = k; a.v = v; a.out = out; a.lse = lse; a.dout = dout;
+  a.dq = dq; a.dk = dk; a.dv = dv;
+  a.delta = static_cast<float*>(workspace);
+  a.B = B; a.S = S; a.H = H; a.d = d; a.n_shards = n_shards;
+  a.causal = causal;
+  a.doc_offsets = doc_offsets;
+  if (doc_offsets) {
+    int32_t* info = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + need - 256);
+    if (cpring::launch_doc_scan(doc_offsets, S, info, stream) != cudaSuccess) return CP_ERR_CUDA;
+    a.doc_info = info;
+  }
+  return cpring::launch_attn_bwd(a, stream) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+}
+
 cp_status cp_ring_attn_fwd_f32(const float* q, const float* k, const float* v, float* out,
                                float* lse, int B, int S, int H, int d, int n_shards, int causal,
                                const int32_t* doc_offsets, cudaStream_t stream) {

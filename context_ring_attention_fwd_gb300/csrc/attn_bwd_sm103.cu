@@ -1,0 +1,562 @@
+// Ring-attention backward for bf16 inputs on sm_103a tensor cores (tcgen05).
+//
+// What is computed.  "上下文並行（Context Parallelism, CP）" (compassingai.com),
+// section 反向傳播: the backward walks the ring's K/V blocks again;
+// "大语言模型并行策略（五）：上下文并行" (wangyu.me): the gradients of K and V
+// travel with their blocks.  For L = sum(out * dout), per (b, h), with P the
+// forward's softmax recomputed from its saved log-sum-exp:
+//   D = rowsum(dO * O);  dP = dO V^T;  dS = P * (dP - D);
+//   dV = P^T dO;  dK = dS^T Q / sqrt(d);  dQ = dS K / sqrt(d),
+// summed over the visible shard pairs and tiles of the forward (tiles are
+// laid from each shard's first row; pairs with no visible (q, k) are never
+// loaded).
+//
+// Two kernels share one body:
+//   kDKDV  a CTA owns a 128-key tile of one (b, h) - the dK_j / dV_j
+//          accumulators that travel with K_j, V_j around the ring - and walks
+//          the query tiles that see it: S^T = K Q^T and dP^T = V dO^T on the
+//          tensor cores with both operands in shared memory, P^T and dS^T in
+//          the softmax warps, then dV += P^T dO and dK += dS^T Q with the A
+//          operand taken from TMEM.
+//   kDQ    a CTA owns a 128-query tile and walks the key tiles it sees:
+//          S = Q K^T, dP = dO V^T, dS, then dQ += dS K.
+// Every CTA finishes its own output tile, so no atomics are needed; the price
+// is that S and dP are formed by both kernels (7 tile products where the
+// gradient needs 5).
+//
+// CTA (320 threads): warps 0-3 and 4-7 split the 128 columns of each S / dP
+// tile (64 each) over the same 128 rows, one thread per TMEM lane; warp 8
+// is the TMA producer (the two fixed tiles once per item, the two streamed
+// tiles of every step into a 2-stage ring); one thread of warp 9 issues every
+// tcgen05.mma.
+// TMEM (512 columns): S | dP | acc0 | acc1 (acc0 = dV or dQ, acc1 = dK).
+// Warpgroup w writes its packed bf16 P / dS into the first 32 columns of its
+// own 64-column half of S / dP, so no half is overwritten before its owner
+// has read it; the TS products gather their A operand from the two halves.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <mutex>
+
+#include "attn_common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace cpring {
+namespace {
+
+constexpr int kT = kTileRows;       // rows of every tile
+constexpr int kStages = 2;          // streamed ring depth
+constexpr int kThreads = 320;
+constexpr int kSoftmaxThreads = 256;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kTmemCols = 512;
+constexpr unsigned long long kTimeoutNs = 4000000000ull;  // per wait
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BLayout {
+  static constexpr int kTileBytes = kT * D * 2;
+  static constexpr int kPanelBytes = kT * 128;   // 128 rows x 64 bf16 columns
+  static constexpr int kPanels = D / 64;
+  static constexpr int kF0 = 0;                  // fixed tiles
+  static constexpr int kF1 = kTileBytes;
+  static constexpr int kX = 2 * kTileBytes;      // streamed: [stage][X0, X1]
+  static constexpr int kVec = kX + kStages * 2 * kTileBytes;  // [2][lse2, delta][128] fp32
+  static constexpr int kBar = kVec + 2 * 2 * kT * 4;
+  static constexpr int kBytes = kBar + 256;
+  static constexpr int kAlloc = kBytes + 1024;
+  __host__ __device__ static constexpr int x0(int st) { return kX + st * 2 * kTileBytes; }
+  __host__ __device__ static constexpr int x1(int st) { return kX + st * 2 * kTileBytes + kTileBytes; }
+};
+
+enum BBar : int {
+  kFixFull = 0,
+  kFixEmpty = 1,
+  kX0Full = 2,   // + stage
+  kX1Full = 4,   // + stage
+  kXEmpty = 6,   // + stage: both streamed tiles consumed
+  kSFull = 8,    // S and dP of the current step are in TMEM
+  kPReady = 9,   // P / dS written by all 256 softmax threads
+  kAccFull = 10, // the item's accumulators are final
+  kVecFull = 11, // + buffer: per-column lse / delta of a query tile written (kDKDV)
+  kVecFree = 13, // + buffer: every softmax thread is done reading it
+  kDrain = 15,
+  kNumBars = 16
+};
+constexpr int kTmemSlot = kNumBars * 8;
+constexpr int kAbortSlot = kNumBars * 8 + 4;
+
+struct BParams {
+  int B, S, H, L, n_shards, causal;
+  const int32_t* doc_offsets;
+  const int32_t* doc_info;
+  int tiles_per_shard, n_tiles, n_items;
+  float scale_log2;     // log2(e) / sqrt(d)
+  float scale;          // 1 / sqrt(d)
+  const float* lse;     // [B, H, S], natural log
+  const float* delta;   // [B, H, S]
+  __nv_bfloat16* g0;    // dQ (kDQ) or dV (kDKDV)
+  __nv_bfloat16* g1;    // dK (kDKDV)
+  int* err;
+  unsigned long long timeout_ns;
+};
+
+struct BItem {
+  int b, h;
+  int r0, r1;        // fixed rows [r0, r1)
+  int x_lo, x_hi;    // flattened streamed tile range
+};
+
+// Item w: fixed tile slot w / (B H) of head w % (B H), heaviest slot first
+// (under causality the last query tiles see the most keys and the first key
+// tiles are seen by the most queries).
+template <bool kDKDV>
+__device__ __forceinline__ void decode_bitem(const BParams& p, int n_docs, int w, BItem& it) {
+  const int BH = p.B * p.H;
+  const int slot = w / BH;
+  const int bh = w - slot * BH;
+  it.b = bh / p.H;
+  it.h = bh - it.b * p.H;
+  const int g = kDKDV ? slot : p.n_tiles - 1 - slot;
+  tile_keys(p, g, it.r0, it.r1);
+  int lo, hi;
+  if (kDKDV) {  // queries that see a key of [r0, r1)
+    lo = p.causal ? it.r0 : doc_span(p, n_docs, it.r0).x;
+    hi = doc_span(p, n_docs, it.r1 - 1).y - 1;
+  } else {      // keys seen by a query of [r0, r1)
+    lo = doc_span(p, n_docs, it.r0).x;
+    hi = p.causal ? it.r1 - 1 : doc_span(p, n_docs, it.r1 - 1).y - 1;
+  }
+  it.x_lo = flat_tile(p, lo);
+  it.x_hi = flat_tile(p, hi);
+}
+
+template <int D, bool kDKDV>
+__global__ void __launch_bounds__(kThreads, 1)
+    ring_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0,
+                         const __grid_constant__ CUtensorMap tm_f1,
+                         const __grid_constant__ CUtensorMap tm_x0,
+                         const __grid_constant__ CUtensorMap tm_x1, const BParams p) {
+  using Lay = BLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_u32(smem);
+  const uint32_t bars = sbase + Lay::kBar;
+  auto bar = [&](int idx) -> uint32_t { return bars + 8u * static_cast<uint32_t>(idx); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kBar + kTmemSlot);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Lay::kBar + kAbortSlot);
+  float* vec = reinterpret_cast<float*>(smem + Lay::kVec);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  int n_docs = 1;
+  if (p.doc_offsets != nullptr) {
+    n_docs = __ldg(p.doc_info);
+    if (n_docs <= 0) return;  // malformed doc_offsets: the scan already flagged it
+  }
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar(kFixFull), 1);
+    ptx::mbar_init(bar(kFixEmpty), 1);
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(bar(kX0Full + s), 1);
+      ptx::mbar_init(bar(kX1Full + s), 1);
+      ptx::mbar_init(bar(kXEmpty + s), 1);
+    }
+    ptx::mbar_init(bar(kSFull), 1);
+    ptx::mbar_init(bar(kPReady), kSoftmaxThreads);
+    ptx::mbar_init(bar(kAccFull), 1);
+    for (int b2 = 0; b2 < 2; ++b2) {
+      ptx::mbar_init(bar(kVecFull + b2), kT);
+      ptx::mbar_init(bar(kVecFree + b2), kSoftmaxThreads);
+    }
+    ptx::mbar_init(bar(kDrain), 1);
+    *abort_flag = 0u;
+    ptx::fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int G = gridDim.x;
+  const int c = blockIdx.x;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      ptx::tma_prefetch_desc(&tm_f0);
+      ptx::tma_prefetch_desc(&tm_f1);
+      ptx::tma_prefetch_desc(&tm_x0);
+      ptx::tma_prefetch_desc(&tm_x1);
+      uint32_t x_iter = 0, fix_iter = 0;
+      uint32_t armed[kStages] = {0u, 0u};  // loads started into each stage
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int w = item_of(k, c, G);
+        if (w >= p.n_items) break;
+        BItem it;
+        decode_bitem<kDKDV>(p, n_docs, w, it);
+        if (!wait1(bar(kFixEmpty), (fix_iter & 1u) ^ 1u, abort_flag, p)) { ok = false; break; }
+        ptx::mbar_arrive_expect_tx(bar(kFixFull), 2 * Lay::kTileBytes);
+        for (int pn = 0; pn < Lay::kPanels; ++pn) {
+          ptx::tma_load_4d(sbase + Lay::kF0 + pn * Lay::kPanelBytes, &tm_f0, bar(kFixFull),
+                           pn * 64, it.h, it.r0, it.b);
+          ptx::tma_load_4d(sbase + Lay::kF1 + pn * Lay::kPanelBytes, &tm_f1, bar(kFixFull),
+                           pn * 64, it.h, it.r0, it.b);
+        }
+        ++fix_iter;
+        for (int f = it.x_lo; f <= it.x_hi; ++f) {
+          const uint32_t st = x_iter % kStages;
+          const uint32_t ph = (x_iter / kStages) & 1u;
+          int xs, xe;
+          tile_keys(p, f, xs, xe);
+          if (!wait1(bar(kXEmpty + st), ph ^ 1u, abort_flag, p)) { ok = false; break; }
+          ptx::mbar_arrive_expect_tx(bar(kX0Full + st), Lay::kTileBytes);
+          ptx::mbar_arrive_expect_tx(bar(kX1Full + st), Lay::kTileBytes);
+          for (int pn = 0; pn < Lay::kPanels; ++pn) {
+            ptx::tma_load_4d(sbase + Lay::x0(st) + pn * Lay::kPanelBytes, &tm_x0,
+                             bar(kX0Full + st), pn * 64, it.h, xs, it.b);
+            ptx::tma_load_4d(sbase + Lay::x1(st) + pn * Lay::kPanelBytes, &tm_x1,
+                             bar(kX1Full + st), pn * 64, it.h, xs, it.b);
+          }
+          ++armed[st];
+          ++x_iter;
+        }
+      }
+      // Let every copy this thread started land before the CTA can exit.
+      if (fix_iter > 0) wait1(bar(kFixFull), (fix_iter - 1) & 1u, abort_flag, p, false);
+      for (int s = 0; s < kStages; ++s) {
+        if (armed[s] > 0) {
+          wait1(bar(kX0Full + s), (armed[s] - 1) & 1u, abort_flag, p, false);
+          wait1(bar(kX1Full + s), (armed[s] - 1) & 1u, abort_flag, p, false);
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kT, kT, false);   // N = streamed rows
+      constexpr uint32_t kIdescG = ptx::idesc_bf16_f32(kT, D, true);     // N = d, B MN-major
+      const uint64_t d_k = ptx::smem_desc_sw128(sbase, 16, 1024);                // K-major
+      const uint64_t d_mn = ptx::smem_desc_sw128(sbase, Lay::kPanelBytes, 1024);  // MN-major
+      const uint32_t tS = tmem_base, tdP = tmem_base + 128;
+      const uint32_t tA0 = tmem_base + 256, tA1 = tmem_base + 256 + D;
+      uint32_t x_iter = 0, fix_iter = 0, p_cnt = 0;
+      bool ok = true;
+      // D_t = A B^T over the head dimension, both tiles K-major.
+      auto issue_ss = [&](uint32_t d_tmem, int a_off, int b_off) {
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s) {
+          const uint64_t step =
+              static_cast<uint64_t>(((s >> 2) * Lay::kPanelBytes + (s & 3) * 32) >> 4);
+          ptx::mma_ss(d_tmem, d_k + (a_off >> 4) + step, d_k + (b_off >> 4) + step, kIdescS,
+                      s > 0 ? 1u : 0u);
+        }
+      };
+      // acc (+)= A B: A = the packed bf16 halves at a_tmem (+0, +64 columns),
+      // B = the streamed tile at b_off read MN-major (rows = K).
+      auto issue_ts = [&](uint32_t acc, uint32_t a_tmem, int b_off, bool first) {
+#pragma unroll
+        for (int s = 0; s < kT / 16; ++s) {
+          const uint32_t a_col = static_cast<uint32_t>((s >> 2) * 64 + (s & 3) * 8);
+          ptx::mma_ts(acc, a_tmem + a_col, d_mn + (b_off >> 4) + static_cast<uint64_t>(s * 128),
+                      kIdescG, (first && s == 0) ? 0u : 1u);
+        }
+      };
+      for (int k = 0; ok; ++k) {
+        const int w = item_of(k, c, G);
+        if (w >= p.n_items) break;
+        BItem it;
+        decode_bitem<kDKDV>(p, n_docs, w, it);
+        if (!wait1(bar(kFixFull), fix_iter & 1u, abort_flag, p)) { ok = false; break; }
+        ++fix_iter;
+        ptx::tc_fence_after();
+        for (int f = it.x_lo; f <= it.x_hi; ++f) {
+          const uint32_t st = x_iter % kStages;
+          const uint32_t ph = (x_iter / kStages) & 1u;
+          if (!wait1(bar(kX0Full + st), ph, abort_flag, p)) { ok = false; break; }
+          if (!wait1(bar(kX1Full + st), ph, abort_flag, p)) { ok = false; break; }
+          ptx::tc_fence_after();
+          issue_ss(tS, Lay::kF0, Lay::x0(st));    // S (kDQ) or S^T (kDKDV)
+          issue_ss(tdP, Lay::kF1, Lay::x1(st));   // dP or dP^T
+          ptx::mma_commit(bar(kSFull));
+          if (!wait1(bar(kPReady), p_cnt & 1u, abort_flag, p)) { ok = false; break; }
+          ++p_cnt;
+          ptx::tc_fence_after();
+          const bool first = (f == it.x_lo);
+          if (kDKDV) {
+            issue_ts(tA0, tS, Lay::x1(st), first);   // dV += P^T dO
+            issue_ts(tA1, tdP, Lay::x0(st), first);  // dK += dS^T Q
+          } else {
+            issue_ts(tA0, tS, Lay::x0(st), first);   // dQ += dS K
+          }
+          ptx::mma_commit(bar(kXEmpty + st));
+          ++x_iter;
+        }
+        if (!ok) break;
+        ptx::mma_commit(bar(kFixEmpty));
+        ptx::mma_commit(bar(kAccFull));
+      }
+      // Wait until every MMA this thread issued has finished.
+      ptx::mma_commit(bar(kDrain));
+      wait1(bar(kDrain), 0u, abort_flag, p, false);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int wg = warp >> 2;        // column half of this warpgroup
+    const int wq = warp & 3;         // TMEM lane quarter
+    const int row_in_tile = wq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem_base + lane_off;
+    const uint32_t tdP = tS + 128;
+    const uint32_t tA0 = tS + 256, tA1 = tS + 256 + D;
+    const int col0 = wg * 64;
+    const float sc = p.scale_log2;
+    uint32_t s_cnt = 0, item_cnt = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int w = item_of(k, c, G);
+      if (w >= p.n_items) break;
+      BItem it;
+      decode_bitem<kDKDV>(p, n_docs, w, it);
+      const int r = it.r0 + row_in_tile;
+      const bool row_valid = r < it.r1;
+      const size_t bh_off = (static_cast<size_t>(it.b) * p.H + it.h) * p.S;
+      int lo_r = 0, hi_r = -1;           // streamed indices this row sees
+      float lse2_r = 0.f, d_r = 0.f;     // kDQ: per-row constants
+      if (row_valid) {
+        const int2 ds = doc_span(p, n_docs, r);
+        if (kDKDV) {
+          lo_r = p.causal ? r : ds.x;
+          hi_r = ds.y - 1;
+        } else {
+          lo_r = ds.x;
+          hi_r = p.causal ? r : ds.y - 1;
+          lse2_r = __ldg(p.lse + bh_off + r) * kLog2e;
+          d_r = __ldg(p.delta + bh_off + r);
+        }
+      }
+      for (int f = it.x_lo; f <= it.x_hi; ++f) {
+        int xs, xe;
+        tile_keys(p, f, xs, xe);
+        const int buf = static_cast<int>(s_cnt & 1u);
+        const uint32_t use = s_cnt >> 1;  // uses of this buffer before this one
+        if (kDKDV) {
+          // Per-column constants of the streamed query tile, shared by all
+          // rows: warps 0-3 write them once the previous user of the buffer
+          // is done, every softmax warp waits for them (all waits bounded).
+          if (threadIdx.x < kT) {
+            if (use > 0 &&
+                !wait_warp(bar(kVecFree + buf), (use - 1u) & 1u, abort_flag, p)) { ok = false; break; }
+            const int q = xs + threadIdx.x;
+            vec[(buf * 2 + 0) * kT + threadIdx.x] = q < xe ? __ldg(p.lse + bh_off + q) * kLog2e : 0.f;
+            vec[(buf * 2 + 1) * kT + threadIdx.x] = q < xe ? __ldg(p.delta + bh_off + q) : 0.f;
+            ptx::mbar_arrive(bar(kVecFull + buf));
+          }
+          if (!wait_warp(bar(kVecFull + buf), use & 1u, abort_flag, p)) { ok = false; break; }
+        }
+        if (!wait_warp(bar(kSFull), s_cnt & 1u, abort_flag, p)) { ok = false; break; }
+        ++s_cnt;
+        ptx::tc_fence_after();
+        const int c_lo = lo_r - xs;
+        const int c_hi = min(hi_r, xe - 1) - xs;
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          const int c0 = col0 + ch * 32;
+          uint32_t sv[32], dv[32];
+          ptx::tmem_ld32(tS + c0, sv);
+          ptx::tmem_ld32(tdP + c0, dv);
+          ptx::tmem_wait_ld();
+          ptx::reg_fence(sv);
+          ptx::reg_fence(dv);
+          uint32_t pk_p[16], pk_s[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x) {
+            float pr[2], dsr[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int cc = c0 + 2 * x + e;
+              const float l2 = kDKDV ? vec[(buf * 2 + 0) * kT + cc] : lse2_r;
+              const float dd = kDKDV ? vec[(buf * 2 + 1) * kT + cc] : d_r;
+              const bool vis = cc >= c_lo && cc <= c_hi;
+              const float pv = vis ? ptx::ex2(fmaf(__uint_as_float(sv[2 * x + e]), sc, -l2)) : 0.f;
+              pr[e] = pv;
+              dsr[e] = pv * (__uint_as_float(dv[2 * x + e]) - dd);
+            }
+            pk_p[x] = ptx::pack_bf16(pr[0], pr[1]);
+            pk_s[x] = ptx::pack_bf16(dsr[0], dsr[1]);
+          }
+          if (kDKDV) {
+            ptx::tmem_st16(tS + col0 + ch * 16, pk_p);
+            ptx::tmem_st16(tdP + col0 + ch * 16, pk_s);
+          } else {
+            ptx::tmem_st16(tS + col0 + ch * 16, pk_s);
+          }
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(kPReady));
+        if (kDKDV) ptx::mbar_arrive(bar(kVecFree + buf));
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      if (!wait_warp(bar(kAccFull), item_cnt & 1u, abort_flag, p)) { ok = false; break; }
+      ++item_cnt;
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int a = 0; a < (kDKDV ? 2 : 1); ++a) {
+        const uint32_t tacc = a == 0 ? tA0 : tA1;
+        __nv_bfloat16* g = a == 0 ? p.g0 : p.g1;
+        const float fac = (kDKDV && a == 0) ? 1.f : p.scale;  // dV unscaled; dK, dQ / sqrt(d)
+        uint4* dst = reinterpret_cast<uint4*>(g + ((static_cast<size_t>(it.b) * p.S + r) * p.H + it.h) * D);
+#pragma unroll
+        for (int ch = 0; ch < D / 64; ++ch) {
+          const int c0 = wg * (D / 2) + ch * 32;
+          uint32_t ov[32];
+          ptx::tmem_ld32(tacc + c0, ov);
+          ptx::tmem_wait_ld();
+          ptx::reg_fence(ov);
+          if (row_valid) {
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              uint4 v4;
+              v4.x = ptx::pack_bf16(__uint_as_float(ov[8 * x + 0]) * fac, __uint_as_float(ov[8 * x + 1]) * fac);
+              v4.y = ptx::pack_bf16(__uint_as_float(ov[8 * x + 2]) * fac, __uint_as_float(ov[8 * x + 3]) * fac);
+              v4.z = ptx::pack_bf16(__uint_as_float(ov[8 * x + 4]) * fac, __uint_as_float(ov[8 * x + 5]) * fac);
+              v4.w = ptx::pack_bf16(__uint_as_float(ov[8 * x + 6]) * fac, __uint_as_float(ov[8 * x + 7]) * fac);
+              dst[c0 / 8 + x] = v4;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// D[b, h, s] = sum_c dO[b, s, h, c] * O[b, s, h, c] (fp32), one warp per row.
+__global__ void __launch_bounds__(256)
+    bwd_delta_kernel(const __nv_bfloat162* __restrict__ out, const __nv_bfloat162* __restrict__ dout,
+                     float* __restrict__ delta, int B, int S, int H, int D) {
+  const long long rows = static_cast<long long>(B) * S * H;
+  const int lane = threadIdx.x & 31;
+  const int pairs = D / 2;
+  for (long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+       row < rows; row += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
+    float acc = 0.f;
+    for (int i = lane; i < pairs; i += 32) {
+      const float2 o = __bfloat1622float2(out[row * pairs + i]);
+      const float2 g = __bfloat1622float2(dout[row * pairs + i]);
+      acc = fmaf(o.x, g.x, fmaf(o.y, g.y, acc));
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) {
+      const int h = static_cast<int>(row % H);
+      const long long bs = row / H;
+      const int s = static_cast<int>(bs % S);
+      const int b = static_cast<int>(bs / S);
+      delta[(static_cast<long long>(b) * H + h) * S + s] = acc;
+    }
+  }
+}
+
+template <int D, bool kDKDV>
+cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
+  using Lay = BLayout<D>;
+  static_assert(Lay::kAlloc <= 232448, "shared memory budget");
+  auto kern = ring_attn_bwd_kernel<D, kDKDV>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kAlloc);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  // kDQ: fixed (Q, dO), streamed (K, V); kDKDV: fixed (K, V), streamed (Q, dO)
+  const void* f0 = kDKDV ? a.k : a.q;
+  const void* f1 = kDKDV ? a.v : a.dout;
+  const void* x0 = kDKDV ? a.q : a.k;
+  const void* x1 = kDKDV ? a.dout : a.v;
+  CUtensorMap m0, m1, m2, m3;
+  if (!make_map(&m0, f0, a.B, a.S, a.H, D) || !make_map(&m1, f1, a.B, a.S, a.H, D) ||
+      !make_map(&m2, x0, a.B, a.S, a.H, D) || !make_map(&m3, x1, a.B, a.S, a.H, D))
+    return cudaErrorInvalidValue;
+  BParams p{};
+  p.B = a.B;
+  p.S = a.S;
+  p.H = a.H;
+  p.n_shards = a.n_shards;
+  p.L = a.S / a.n_shards;
+  p.causal = a.causal;
+  p.doc_offsets = a.doc_offsets;
+  p.doc_info = a.doc_info;
+  p.tiles_per_shard = (p.L + kT - 1) / kT;
+  p.n_tiles = a.n_shards * p.tiles_per_shard;
+  const long long items = static_cast<long long>(a.B) * a.H * p.n_tiles;
+  if (items > INT_MAX) return cudaErrorInvalidValue;
+  p.n_items = static_cast<int>(items);
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+  p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
+  p.lse = a.lse;
+  p.delta = a.delta;
+  p.g0 = static_cast<__nv_bfloat16*>(kDKDV ? a.dv : a.dq);
+  p.g1 = static_cast<__nv_bfloat16*>(kDKDV ? a.dk : nullptr);
+  p.err = device_error_word();
+  if (!p.err) return cudaErrorInvalidValue;
+  p.timeout_ns = kTimeoutNs;
+  const int grid = static_cast<int>(std::min<long long>(items, sm_count()));
+  if (grid <= 0) return cudaSuccess;
+  kern<<<grid, kThreads, Lay::kAlloc, stream>>>(m0, m1, m2, m3, p);
+  count_launch(0);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
+  {
+    const long long rows = static_cast<long long>(a.B) * a.S * a.H;
+    const long long want = (rows * 32 + 255) / 256;
+    const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(want, 8LL * sm_count())));
+    bwd_delta_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat162*>(a.out),
+                                               static_cast<const __nv_bfloat162*>(a.dout),
+                                               a.delta, a.B, a.S, a.H, a.d);
+    count_launch(2);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e;
+  if (a.d == 128) {
+    e = launch_bwd_t<128, true>(a, stream);
+    if (e == cudaSuccess) e = launch_bwd_t<128, false>(a, stream);
+  } else if (a.d == 64) {
+    e = launch_bwd_t<64, true>(a, stream);
+    if (e == cudaSuccess) e = launch_bwd_t<64, false>(a, stream);
+  } else {
+    e = cudaErrorInvalidValue;
+  }
+  return e;
+}
+
+}  // namespace cpring

@@ -51,14 +51,15 @@
 #include <atomic>
 #include <mutex>
 
+#include "attn_common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace cpring {
 namespace {
 
-constexpr int kBM = 128;        // query rows per tile = TMEM lanes
-constexpr int kBN = 128;        // key rows per K/V tile
+constexpr int kBM = kTileRows;  // query rows per tile = TMEM lanes
+constexpr int kBN = kTileRows;  // key rows per K/V tile
 constexpr int kQTiles = 2;      // query tiles per work item
 constexpr int kStages = 2;      // K/V ring depth
 constexpr int kThreads = 384;   // three warpgroups
@@ -169,29 +170,6 @@ struct Item {
   int klo, khi;                      // key range this launch may use
 };
 
-// Document [start, end) containing token r.
-__device__ __forceinline__ int2 doc_span(const KParams& p, int n_docs, int r) {
-  if (p.doc_offsets == nullptr) return make_int2(0, p.S);
-  int lo = 0, hi = n_docs;
-  while (hi - lo > 1) {
-    int mid = (lo + hi) >> 1;
-    if (__ldg(p.doc_offsets + mid) <= r) lo = mid; else hi = mid;
-  }
-  return make_int2(__ldg(p.doc_offsets + lo), __ldg(p.doc_offsets + lo + 1));
-}
-
-__device__ __forceinline__ int flat_tile(const KParams& p, int key) {
-  int j = key / p.L;
-  return j * p.tiles_per_shard + (key - j * p.L) / kBN;
-}
-
-__device__ __forceinline__ void tile_keys(const KParams& p, int f, int& ks, int& ke) {
-  int j = f / p.tiles_per_shard;
-  int kt = f - j * p.tiles_per_shard;
-  ks = j * p.L + kt * kBN;
-  ke = min(ks + kBN, (j + 1) * p.L);
-}
-
 // Work item w: (b, h, query shard, pair of 128-row tiles).  Items are dealt
 // head group by head group (p.head_group (b, h) heads at a time), and inside
 // a group heaviest first, so that the CTAs running at any moment stream the
@@ -244,57 +222,6 @@ __device__ __forceinline__ void decode_item(const KParams& p, int n_docs, int w,
         it.F_lo = min(it.F_lo, it.f_lo[t]);
         it.F_hi = max(it.F_hi, it.f_hi[t]);
       }
-    }
-  }
-}
-
-__device__ __forceinline__ int item_of(int k, int c, int G) {
-  return k * G + ((k & 1) ? (G - 1 - c) : c);
-}
-
-// ---------------------------------------------------------------- waits
-// Single-thread bounded wait.  Returns false on abort or timeout.
-__device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                      const KParams& p, bool honour_abort = true) {
-  uint64_t t0 = 0;
-  for (uint32_t it = 1;; ++it) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if (honour_abort && *abort_flag) return false;
-    if ((it & 255u) == 0) {
-      const uint64_t now = ptx::globaltimer();
-      if (t0 == 0) {
-        t0 = now;
-      } else if (now - t0 > p.timeout_ns) {
-        *abort_flag = 1u;
-        atomicOr(p.err, kErrTimeout);
-        return false;
-      }
-    }
-  }
-}
-
-// Warp-uniform bounded wait (every lane calls it; all lanes get one answer).
-__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity,
-                                          volatile uint32_t* abort_flag, const KParams& p) {
-  uint64_t t0 = 0;
-  const int lane = threadIdx.x & 31;
-  for (uint32_t it = 1;; ++it) {
-    const bool ok = ptx::mbar_try_wait(bar, parity);
-    if (__any_sync(0xffffffffu, ok)) return true;
-    if (__any_sync(0xffffffffu, *abort_flag != 0u)) return false;
-    if ((it & 255u) == 0) {
-      int tout = 0;
-      if (lane == 0) {
-        const uint64_t now = ptx::globaltimer();
-        if (t0 == 0) {
-          t0 = now;
-        } else if (now - t0 > p.timeout_ns) {
-          *abort_flag = 1u;
-          atomicOr(p.err, kErrTimeout);
-          tout = 1;
-        }
-      }
-      if (__shfl_sync(0xffffffffu, tout, 0)) return false;
     }
   }
 }
@@ -951,44 +878,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- host side
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  });
-  return fn;
-}
-
-// [B, S, H, D] viewed as a 4-D tensor (D, H, S, B) of E-byte elements;
-// box = one 128-byte panel x 1 x 128 rows x 1.
-bool make_map(CUtensorMap* m, const void* base, int B, int S, int H, int D, int E = 2) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t e = static_cast<cuuint64_t>(E);
-  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
-                        static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * e, static_cast<cuuint64_t>(H) * D * e,
-                           static_cast<cuuint64_t>(S) * H * D * e};
-  cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / E), 1, static_cast<cuuint32_t>(kBM), 1};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, E == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
-                  const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 // V^T [B, H, D, S] of bytes viewed as (S, D, H, B); box = 128 keys x D rows.
 // Needs S % 16 == 0 (row stride a multiple of 16 bytes).
 bool make_map_vt8(CUtensorMap* m, const void* base, int B, int S, int H, int D) {

@@ -37,6 +37,24 @@ struct AttnArgs {
   const float* v_descale;
 };
 
+// The backward: gradients of sum(out * dout) for the forward's out and lse.
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* out;
+  const float* lse;
+  const void* dout;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* delta;                // device scratch [B, H, S]
+  int B, S, H, d, n_shards;
+  int causal;
+  const int32_t* doc_offsets;  // device or null
+  const int32_t* doc_info;     // written by the doc scan, or null
+};
+
 // Sticky device error word (bits of kErr*), owned by merge.cu.
 constexpr int kErrDocOffsets = 1;
 constexpr int kErrTimeout = 2;
@@ -49,6 +67,9 @@ cudaError_t launch_attn_f32(const AttnArgs& a, cudaStream_t stream);
 // FP8 form: q, k E4M3 [B, S, H, 128], v E4M3 [B, H, 128, S]; the fused
 // forward only (q_shard = k_shard = -1).
 cudaError_t launch_attn_fp8(const AttnArgs& a, cudaStream_t stream);
+// Backward: the row sums D, then the dK/dV kernel and the dQ kernel (bf16,
+// d in {64, 128}).
+cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_doc_scan(const int32_t* doc_offsets, int S, int32_t* doc_info,
                             cudaStream_t stream);
 cudaError_t launch_merge(float* o_acc, float* m_acc, float* l_acc, const float* o_part,

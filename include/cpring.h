@@ -284,6 +284,35 @@ void cp_test_set_wait_fault(int drop_first_k_tile, long long wait_limit_ns);
 void cp_launch_counts(int64_t* counts4);
 
 /*
+ * Ring-attention backward: the gradients of L = sum(out * dout) with respect
+ * to q, k and v, for the forward of cp_ring_attn_fwd (same masks, sharding
+ * and tiling).  "上下文並行（Context Parallelism, CP）" (compassingai.com),
+ * section 反向傳播: the backward walks the ring's K/V blocks again; the
+ * gradients of K_j, V_j travel with them ("大语言模型并行策略（五）：上下文并行").
+ * Per (b, h), with P recomputed from the saved lse:
+ *   D = rowsum(dout * out);  dP = dout v^T;  dS = P * (dP - D);
+ *   dv = P^T dout;  dk = dS^T q / sqrt(d);  dq = dS k / sqrt(d).
+ *  q, k, v, out, dout   device, bf16 [B,S,H,d], read only (out, lse from the
+ *                       forward on the same inputs).
+ *  lse        device, fp32 [B,H,S], read only.
+ *  dq, dk, dv device, bf16 [B,S,H,d], written.
+ *  workspace  device, >= cp_ring_attn_bwd_workspace_bytes(...) bytes,
+ *             256-byte aligned, caller-owned scratch (D and the doc-scan
+ *             word); nothing is allocated.
+ *  Shapes, masks, d, alignment and errors as cp_ring_attn_fwd; a workspace
+ *  too small returns CP_ERR_BUFFER.
+ * Four launches on `stream` (with doc_offsets, five): D, the dK/dV kernel
+ * (one CTA per 128-key tile), the dQ kernel (one CTA per 128-query tile).
+ * Both run on tcgen05 with fp32 accumulation and bf16 P / dS operands.
+ */
+int64_t cp_ring_attn_bwd_workspace_bytes(int B, int S, int H, int d, int n_shards);
+cp_status cp_ring_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                           const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                           int B, int S, int H, int d, int n_shards, int causal,
+                           const int32_t* doc_offsets, void* workspace, int64_t workspace_bytes,
+                           cudaStream_t stream);
+
+/*
  * FP8 (E4M3) quantisation of one bf16 tensor, per (b, h).
  * "上下文並行（Context Parallelism, CP）" (compassingai.com), section
  * 通訊量分析: the bytes moved depend on whether K/V travel in FP8.  Format:

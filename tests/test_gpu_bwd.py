@@ -1,0 +1,162 @@
+"""GPU parity of the backward (cp_ring_attn_bwd) against the fp64 oracle.
+
+The kernels take the forward's own out and lse (the path's data flow) and
+return bf16 dq, dk, dv; the oracle differentiates the exact forward of the
+same bf16 inputs.  Tolerance, per gradient g, relative to max|g_oracle|:
+max-abs 2^-6 and mean-abs 2^-10.  Derivation: the path rounds P and dS to
+bf16 for the tensor-core products (relative 2^-9), reads the forward's bf16
+out for D = rowsum(dO * O), accumulates in fp32 and rounds the gradients to
+bf16 (2^-9).  A numpy model of exactly those rounding points on seeded
+N(0, s^2) inputs (s = 0.7 .. 2, causal and not, d = 64 and 128) reached at
+most 0.0044 and 0.00037 of max|g|.
+
+Full-size workloads are checked on seeded query rows of dQ (a row of dQ needs
+only its own row of P), on the sums that hold at any size (the dV rows sum to
+the dO rows and the dK rows to zero), and on Q = 0, where dV has a closed
+form (suffix or document means of dO).
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import context_ring_attention_fwd_gb300 as pkg
+from context_ring_attention_fwd_gb300 import inputs
+from oracle import ref
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+REL_MAX, REL_MEAN = 2.0 ** -6, 2.0 ** -10
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    if not os.path.exists(pkg.LIB_PATH):
+        from context_ring_attention_fwd_gb300 import _build
+        _build.build()
+    pkg.lib()
+    torch.cuda.set_device(0)
+    yield
+    assert pkg.cp_get_last_status() == 0
+
+
+def _np(t):
+    return t.detach().float().cpu().numpy()
+
+
+def _grads(q, k, v, dout, N, causal, docs):
+    out, lse = pkg.ring_attn_fwd(q, k, v, N, causal, docs)
+    g = pkg.ring_attn_bwd(q, k, v, out, lse, dout, N, causal, docs)
+    assert pkg.cp_get_last_status() == 0
+    return g
+
+
+def _check(got, want, what):
+    for name, a, b in zip(("dq", "dk", "dv"), got, want):
+        a = _np(a)
+        assert np.all(np.isfinite(a)), (what, name)
+        gm = np.abs(b).max()
+        e = np.abs(a - b)
+        assert e.max() <= REL_MAX * gm, (what, name, e.max(), gm)
+        assert e.mean() <= REL_MEAN * gm, (what, name, e.mean(), gm)
+
+
+BWD_CASES = [
+    # B, S, H, d, N, causal, docs, input scale
+    (1, 512, 2, 128, 4, True, None, 1.0),
+    (2, 640, 2, 64, 2, True, None, 1.0),              # 320-row shards: ragged tiles
+    (1, 384, 3, 128, 3, False, None, 1.0),
+    (1, 1024, 2, 128, 4, True, [0, 300, 301, 777, 1024], 1.0),
+    (1, 512, 2, 64, 1, False, [0, 100, 512], 0.7071),
+    (1, 1024, 1, 128, 2, True, None, 2.0),
+]
+
+
+@pytest.mark.parametrize("B,S,H,d,N,causal,docs,scale", BWD_CASES)
+def test_bwd_against_oracle(B, S, H, d, N, causal, docs, scale):
+    q, k, v = (t.to(DEV) for t in inputs.make_qkv(B, S, H, d, 51, torch.bfloat16, scale))
+    dout = inputs.make_qkv(B, S, H, d, 52, torch.bfloat16)[0].to(DEV)
+    got = _grads(q, k, v, dout, N, causal, docs)
+    want = ref.attention_bwd(_np(q), _np(k), _np(v), _np(dout), causal, docs)
+    _check(got, want, (B, S, H, d, N, causal, docs, scale))
+
+
+def test_bwd_deterministic_and_guard_bands():
+    B, S, H, d, N = 1, 1024, 2, 128, 4
+    q, k, v = (t.to(DEV) for t in inputs.make_qkv(B, S, H, d, 53, torch.bfloat16))
+    dout = inputs.make_qkv(B, S, H, d, 54, torch.bfloat16)[0].to(DEV)
+    out, lse = pkg.ring_attn_fwd(q, k, v, N, True)
+    a = pkg.ring_attn_bwd(q, k, v, out, lse, dout, N, True)
+    # outputs inside larger buffers whose margins must stay untouched
+    n = B * S * H * d
+    bufs = [torch.full((n + 4096,), 7.0, dtype=torch.bfloat16, device=DEV) for _ in range(3)]
+    views = [b_[2048:2048 + n].view(B, S, H, d) for b_ in bufs]
+    pkg.cp_ring_attn_bwd(q, k, v, out, lse, dout, *views, N, True)
+    for x, y in zip(a, views):
+        assert torch.equal(x, y)
+    for b_ in bufs:
+        assert torch.all(b_[:2048] == 7.0) and torch.all(b_[2048 + n:] == 7.0)
+
+
+def test_bwd_constant_v_and_zero_q():
+    B, S, H, d, N = 1, 1024, 2, 128, 4
+    q, k, v = (t.to(DEV) for t in inputs.make_qkv(B, S, H, d, 55, torch.bfloat16))
+    dout = inputs.make_qkv(B, S, H, d, 56, torch.bfloat16)[0].to(DEV)
+    # constant V: dS vanishes, so dQ and dK are zero up to rounding
+    vc = v[:, :1].expand_as(v).contiguous()
+    dq, dk, dv = _grads(q, k, vc, dout, N, True, None)
+    _, gk, gv = ref.attention_bwd(_np(q), _np(k), _np(v), _np(dout), True)   # scale reference
+    assert _np(dq).__abs__().max() <= REL_MAX * np.abs(gk).max()
+    assert _np(dk).__abs__().max() <= REL_MAX * np.abs(gk).max()
+    # Q = 0: dV is the suffix mean of dO
+    dq0, dk0, dv0 = _grads(torch.zeros_like(q), k, v, dout, N, True, None)
+    want = ref.zero_query_dv_closed_form(_np(dout), True)
+    e = np.abs(_np(dv0) - want)
+    assert e.max() <= REL_MAX * np.abs(want).max() and e.mean() <= REL_MEAN * np.abs(want).max()
+
+
+def _full_size_checks(w, n_rows, heads):
+    q, k, v = inputs.make_qkv(w.B, w.S, w.H, w.d, w.seed, torch.bfloat16, w.scale, device=DEV)
+    docs = (inputs.make_doc_offsets(w.S, w.seed + 1, w.doc_min, w.doc_max)
+            if w.packed_docs else None)
+    dout = inputs.make_qkv(w.B, w.S, w.H, w.d, w.seed + 50, torch.bfloat16, device=DEV)[0]
+    dq, dk, dv = _grads(q, k, v, dout, w.n_shards, w.causal, docs)
+    # sums that hold at any size: sum_k dV = sum_q dO and sum_k dK = 0, per (b, h, c)
+    sdv, sdo = dv.float().sum(1), dout.float().sum(1)
+    scale_dv = dv.float().abs().amax().item() * np.sqrt(w.S)
+    assert (sdv - sdo).abs().max().item() <= REL_MAX * scale_dv, w.name
+    scale_dk = dk.float().abs().amax().item() * np.sqrt(w.S)
+    assert dk.float().sum(1).abs().max().item() <= REL_MAX * scale_dk, w.name
+    # sampled rows of dQ against the oracle's row form
+    qn, kn, vn, dn, dqn = _np(q), _np(k), _np(v), _np(dout), _np(dq)
+    for b in range(w.B):
+        for h in heads:
+            rows = inputs.sample_rows(w.S, n_rows, seed=w.seed * 100 + b * w.H + h)
+            want = ref.attention_bwd_rows(qn, kn, vn, dn, b, h, rows, w.causal, docs)
+            gm = np.abs(want).max()
+            e = np.abs(dqn[b, rows, h] - want)
+            assert e.max() <= REL_MAX * gm and e.mean() <= REL_MEAN * gm, (w.name, b, h, e.max(), gm)
+    # Q = 0: dV in closed form
+    del dq, dk, dv
+    _, _, dv0 = _grads(torch.zeros_like(q), k, v, dout, w.n_shards, w.causal, docs)
+    hl = list(heads)
+    want = ref.zero_query_dv_closed_form(dn[:, :, hl], w.causal, docs)
+    e = np.abs(_np(dv0[:, :, hl]) - want)
+    gm = np.abs(want).max()
+    assert e.max() <= REL_MAX * gm and e.mean() <= REL_MEAN * gm, (w.name, e.max(), gm)
+
+
+def test_bwd_workload_causal_8k():
+    _full_size_checks(inputs.BY_NAME["bf16_causal_8k"], 128, range(0, 32, 4))
+
+
+def test_bwd_workload_packed_docs_64k():
+    _full_size_checks(inputs.BY_NAME["bf16_causal_packed_64k"], 128, range(0, 16, 4))
+
+
+def test_bwd_workload_causal_128k():
+    _full_size_checks(inputs.BY_NAME["bf16_causal_128k"], 64, range(0, 32, 8))
