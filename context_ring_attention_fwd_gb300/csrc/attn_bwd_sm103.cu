@@ -50,7 +50,6 @@ namespace cpring {
 namespace {
 
 constexpr int kT = kTileRows;       // rows of every tile
-constexpr int kStages = 2;          // streamed ring depth
 constexpr int kThreads = 320;
 constexpr int kSoftmaxThreads = 256;
 constexpr int kProducerWarp = 8;
@@ -59,36 +58,49 @@ constexpr int kTmemCols = 512;
 constexpr unsigned long long kTimeoutNs = 4000000000ull;  // per wait
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D>
+// Streamed tiles run in two rings of single-tile slots: X0 (K for kDQ, Q for
+// kDKDV) and X1 (V or dO).  kDQ holds K until dQ += dS K is done but V only
+// until dP, and issues the next step's products early, so its K ring is one
+// slot deeper.
+template <int D, bool kDKDV>
 struct BLayout {
   static constexpr int kTileBytes = kT * D * 2;
   static constexpr int kPanelBytes = kT * 128;   // 128 rows x 64 bf16 columns
   static constexpr int kPanels = D / 64;
+  static constexpr int kX0Slots = kDKDV ? 2 : 3;
+  static constexpr int kX1Slots = 2;
   static constexpr int kF0 = 0;                  // fixed tiles
   static constexpr int kF1 = kTileBytes;
-  static constexpr int kX = 2 * kTileBytes;      // streamed: [stage][X0, X1]
-  static constexpr int kVec = kX + kStages * 2 * kTileBytes;  // [2][lse2, delta][128] fp32
-  static constexpr int kBar = kVec + 2 * 2 * kT * 4;
+  static constexpr int kX0 = 2 * kTileBytes;
+  static constexpr int kX1 = kX0 + kX0Slots * kTileBytes;
+  static constexpr int kVec = kX1 + kX1Slots * kTileBytes;    // kDKDV: [2][-lse2, -D][128] fp32
+  static constexpr int kBar = kVec + (kDKDV ? 2 * 2 * kT * 4 : 0);
   static constexpr int kBytes = kBar + 256;
   static constexpr int kAlloc = kBytes + 1024;
-  __host__ __device__ static constexpr int x0(int st) { return kX + st * 2 * kTileBytes; }
-  __host__ __device__ static constexpr int x1(int st) { return kX + st * 2 * kTileBytes + kTileBytes; }
+  __host__ __device__ static constexpr int x0(int slot) { return kX0 + slot * kTileBytes; }
+  __host__ __device__ static constexpr int x1(int slot) { return kX1 + slot * kTileBytes; }
 };
 
 enum BBar : int {
   kFixFull = 0,
   kFixEmpty = 1,
-  kX0Full = 2,   // + stage
-  kX1Full = 4,   // + stage
-  kXEmpty = 6,   // + stage: both streamed tiles consumed
-  kSFull = 8,    // S and dP of the current step are in TMEM
-  kPReady = 9,   // P / dS written by all 256 softmax threads
-  kAccFull = 10, // the item's accumulators are final
-  kVecFull = 11, // + buffer: per-column lse / delta of a query tile written (kDKDV)
-  kVecFree = 13, // + buffer: every softmax thread is done reading it
-  kDrain = 15,
-  kNumBars = 16
+  kX0Full = 2,     // + slot (3)
+  kX1Full = 5,     // + slot (2)
+  kX0Empty = 7,    // + slot (3)
+  kX1Empty = 10,   // + slot (2)
+  kSFull = 12,     // S and dP of the current step are in TMEM
+  kPReady = 13,    // + step parity (kDQ; kDKDV uses +0): P / dS written by all softmax threads
+  kSConsumed = 15, // kDQ: every softmax thread has read S and dP of the step
+  kAccFull = 16,   // the item's accumulators are final
+  kVecFull = 17,   // + buffer: per-column lse / delta of a query tile written (kDKDV)
+  kVecFree = 19,   // + buffer: every softmax thread is done reading it
+  kDrain = 21,
+  kNumBars = 22
 };
+// kDQ keeps packed dS in its own double buffer of TMEM columns (acc0 ends at
+// 256 + D <= 384), so S and dP of the next step can be issued while the
+// softmax still works on the current one.
+constexpr uint32_t kDsBuf = 384;
 constexpr int kTmemSlot = kNumBars * 8;
 constexpr int kAbortSlot = kNumBars * 8 + 4;
 
@@ -97,6 +109,7 @@ struct BParams {
   const int32_t* doc_offsets;
   const int32_t* doc_info;
   int tiles_per_shard, n_tiles, n_items;
+  int head_group;       // (b, h) heads whose items are dealt out together
   float scale_log2;     // log2(e) / sqrt(d)
   float scale;          // 1 / sqrt(d)
   const float* lse;     // [B, H, S], natural log
@@ -113,14 +126,20 @@ struct BItem {
   int x_lo, x_hi;    // flattened streamed tile range
 };
 
-// Item w: fixed tile slot w / (B H) of head w % (B H), heaviest slot first
-// (under causality the last query tiles see the most keys and the first key
-// tiles are seen by the most queries).
+// Item w: items are dealt head group by head group (head_group (b, h) heads
+// at a time, so the CTAs in flight stream the tiles of few heads and re-read
+// them from L2), and inside a group heaviest slot first (under causality the
+// last query tiles see the most keys and the first key tiles are seen by the
+// most queries).
 template <bool kDKDV>
 __device__ __forceinline__ void decode_bitem(const BParams& p, int n_docs, int w, BItem& it) {
   const int BH = p.B * p.H;
-  const int slot = w / BH;
-  const int bh = w - slot * BH;
+  const int HG = p.head_group;
+  const int gi = w / (HG * p.n_tiles);
+  const int rr = w - gi * HG * p.n_tiles;
+  const int hg = min(HG, BH - gi * HG);
+  const int slot = rr / hg;
+  const int bh = gi * HG + rr % hg;
   it.b = bh / p.H;
   it.h = bh - it.b * p.H;
   const int g = kDKDV ? slot : p.n_tiles - 1 - slot;
@@ -143,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tm_f1,
                          const __grid_constant__ CUtensorMap tm_x0,
                          const __grid_constant__ CUtensorMap tm_x1, const BParams p) {
-  using Lay = BLayout<D>;
+  using Lay = BLayout<D, kDKDV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -166,13 +185,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(kFixFull), 1);
     ptx::mbar_init(bar(kFixEmpty), 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < Lay::kX0Slots; ++s) {
       ptx::mbar_init(bar(kX0Full + s), 1);
+      ptx::mbar_init(bar(kX0Empty + s), 1);
+    }
+    for (int s = 0; s < Lay::kX1Slots; ++s) {
       ptx::mbar_init(bar(kX1Full + s), 1);
-      ptx::mbar_init(bar(kXEmpty + s), 1);
+      ptx::mbar_init(bar(kX1Empty + s), 1);
     }
     ptx::mbar_init(bar(kSFull), 1);
     ptx::mbar_init(bar(kPReady), kSoftmaxThreads);
+    ptx::mbar_init(bar(kPReady + 1), kSoftmaxThreads);
+    ptx::mbar_init(bar(kSConsumed), kSoftmaxThreads);
     ptx::mbar_init(bar(kAccFull), 1);
     for (int b2 = 0; b2 < 2; ++b2) {
       ptx::mbar_init(bar(kVecFull + b2), kT);
@@ -202,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tma_prefetch_desc(&tm_x0);
       ptx::tma_prefetch_desc(&tm_x1);
       uint32_t x_iter = 0, fix_iter = 0;
-      uint32_t armed[kStages] = {0u, 0u};  // loads started into each stage
+      uint32_t armed0[3] = {0u, 0u, 0u}, armed1[2] = {0u, 0u};  // loads started per slot
       bool ok = true;
       for (int k = 0; ok; ++k) {
         const int w = item_of(k, c, G);
@@ -219,31 +243,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++fix_iter;
         for (int f = it.x_lo; f <= it.x_hi; ++f) {
-          const uint32_t st = x_iter % kStages;
-          const uint32_t ph = (x_iter / kStages) & 1u;
+          const uint32_t s0 = x_iter % Lay::kX0Slots, ph0 = (x_iter / Lay::kX0Slots) & 1u;
+          const uint32_t s1 = x_iter % Lay::kX1Slots, ph1 = (x_iter / Lay::kX1Slots) & 1u;
           int xs, xe;
           tile_keys(p, f, xs, xe);
-          if (!wait1(bar(kXEmpty + st), ph ^ 1u, abort_flag, p)) { ok = false; break; }
-          ptx::mbar_arrive_expect_tx(bar(kX0Full + st), Lay::kTileBytes);
-          ptx::mbar_arrive_expect_tx(bar(kX1Full + st), Lay::kTileBytes);
-          for (int pn = 0; pn < Lay::kPanels; ++pn) {
-            ptx::tma_load_4d(sbase + Lay::x0(st) + pn * Lay::kPanelBytes, &tm_x0,
-                             bar(kX0Full + st), pn * 64, it.h, xs, it.b);
-            ptx::tma_load_4d(sbase + Lay::x1(st) + pn * Lay::kPanelBytes, &tm_x1,
-                             bar(kX1Full + st), pn * 64, it.h, xs, it.b);
-          }
-          ++armed[st];
+          if (!wait1(bar(kX0Empty + s0), ph0 ^ 1u, abort_flag, p)) { ok = false; break; }
+          ptx::mbar_arrive_expect_tx(bar(kX0Full + s0), Lay::kTileBytes);
+          for (int pn = 0; pn < Lay::kPanels; ++pn)
+            ptx::tma_load_4d(sbase + Lay::x0(s0) + pn * Lay::kPanelBytes, &tm_x0,
+                             bar(kX0Full + s0), pn * 64, it.h, xs, it.b);
+          ++armed0[s0];
+          if (!wait1(bar(kX1Empty + s1), ph1 ^ 1u, abort_flag, p)) { ok = false; break; }
+          ptx::mbar_arrive_expect_tx(bar(kX1Full + s1), Lay::kTileBytes);
+          for (int pn = 0; pn < Lay::kPanels; ++pn)
+            ptx::tma_load_4d(sbase + Lay::x1(s1) + pn * Lay::kPanelBytes, &tm_x1,
+                             bar(kX1Full + s1), pn * 64, it.h, xs, it.b);
+          ++armed1[s1];
           ++x_iter;
         }
       }
       // Let every copy this thread started land before the CTA can exit.
       if (fix_iter > 0) wait1(bar(kFixFull), (fix_iter - 1) & 1u, abort_flag, p, false);
-      for (int s = 0; s < kStages; ++s) {
-        if (armed[s] > 0) {
-          wait1(bar(kX0Full + s), (armed[s] - 1) & 1u, abort_flag, p, false);
-          wait1(bar(kX1Full + s), (armed[s] - 1) & 1u, abort_flag, p, false);
-        }
-      }
+      for (int s = 0; s < Lay::kX0Slots; ++s)
+        if (armed0[s] > 0) wait1(bar(kX0Full + s), (armed0[s] - 1) & 1u, abort_flag, p, false);
+      for (int s = 0; s < Lay::kX1Slots; ++s)
+        if (armed1[s] > 0) wait1(bar(kX1Full + s), (armed1[s] - 1) & 1u, abort_flag, p, false);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -266,16 +290,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                       s > 0 ? 1u : 0u);
         }
       };
-      // acc (+)= A B: A = the packed bf16 halves at a_tmem (+0, +64 columns),
+      // acc (+)= A B: A = packed bf16 columns at a_tmem, in two halves
+      // `half` columns apart (64: the halves of S / dP; 32: contiguous),
       // B = the streamed tile at b_off read MN-major (rows = K).
-      auto issue_ts = [&](uint32_t acc, uint32_t a_tmem, int b_off, bool first) {
+      auto issue_ts = [&](uint32_t acc, uint32_t a_tmem, int b_off, bool first, int half) {
 #pragma unroll
         for (int s = 0; s < kT / 16; ++s) {
-          const uint32_t a_col = static_cast<uint32_t>((s >> 2) * 64 + (s & 3) * 8);
+          const uint32_t a_col = static_cast<uint32_t>((s >> 2) * half + (s & 3) * 8);
           ptx::mma_ts(acc, a_tmem + a_col, d_mn + (b_off >> 4) + static_cast<uint64_t>(s * 128),
                       kIdescG, (first && s == 0) ? 0u : 1u);
         }
       };
+      uint32_t n = 0;  // kDQ: steps issued so far (all items)
       for (int k = 0; ok; ++k) {
         const int w = item_of(k, c, G);
         if (w >= p.n_items) break;
@@ -284,26 +310,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait1(bar(kFixFull), fix_iter & 1u, abort_flag, p)) { ok = false; break; }
         ++fix_iter;
         ptx::tc_fence_after();
+        if constexpr (!kDKDV) {
+          // S, dP of step n + 1 go out once the softmax has read those of
+          // step n; dQ += dS K of step n once its dS is in buffer n % 2.
+          bool have = false;  // S, dP of the current step already issued
+          // S, dP of streamed step x: K from X0 slot x % 3, V from X1 slot
+          // x % 2; V's slot is free once dP is done.
+          auto issue_step = [&](uint32_t x) -> bool {
+            const uint32_t s0 = x % Lay::kX0Slots, s1 = x % Lay::kX1Slots;
+            if (!wait1(bar(kX0Full + s0), (x / Lay::kX0Slots) & 1u, abort_flag, p)) return false;
+            if (!wait1(bar(kX1Full + s1), (x / Lay::kX1Slots) & 1u, abort_flag, p)) return false;
+            ptx::tc_fence_after();
+            issue_ss(tS, Lay::kF0, Lay::x0(s0));
+            issue_ss(tdP, Lay::kF1, Lay::x1(s1));
+            ptx::mma_commit(bar(kSFull));
+            ptx::mma_commit(bar(kX1Empty + s1));
+            return true;
+          };
+          for (int f = it.x_lo; f <= it.x_hi; ++f) {
+            if (!have) {
+              if (n > 0 && !wait1(bar(kSConsumed), (n - 1u) & 1u, abort_flag, p)) { ok = false; break; }
+              if (!issue_step(x_iter)) { ok = false; break; }
+            }
+            have = false;
+            if (f < it.x_hi) {
+              if (!wait1(bar(kSConsumed), n & 1u, abort_flag, p)) { ok = false; break; }
+              if (!issue_step(x_iter + 1)) { ok = false; break; }
+              have = true;
+            }
+            if (!wait1(bar(kPReady + (n & 1u)), (n >> 1) & 1u, abort_flag, p)) { ok = false; break; }
+            ptx::tc_fence_after();
+            const uint32_t s0 = x_iter % Lay::kX0Slots;
+            issue_ts(tA0, tmem_base + kDsBuf + (n & 1u) * 64u, Lay::x0(s0), f == it.x_lo, 32);
+            ptx::mma_commit(bar(kX0Empty + s0));
+            ++n;
+            ++x_iter;
+          }
+          if (!ok) break;
+          ptx::mma_commit(bar(kFixEmpty));
+          ptx::mma_commit(bar(kAccFull));
+          continue;
+        }
         for (int f = it.x_lo; f <= it.x_hi; ++f) {
-          const uint32_t st = x_iter % kStages;
-          const uint32_t ph = (x_iter / kStages) & 1u;
+          const uint32_t st = x_iter % Lay::kX0Slots;   // both rings have two slots here
+          const uint32_t ph = (x_iter / Lay::kX0Slots) & 1u;
           if (!wait1(bar(kX0Full + st), ph, abort_flag, p)) { ok = false; break; }
           if (!wait1(bar(kX1Full + st), ph, abort_flag, p)) { ok = false; break; }
           ptx::tc_fence_after();
-          issue_ss(tS, Lay::kF0, Lay::x0(st));    // S (kDQ) or S^T (kDKDV)
-          issue_ss(tdP, Lay::kF1, Lay::x1(st));   // dP or dP^T
+          issue_ss(tS, Lay::kF0, Lay::x0(st));    // S^T = K Q^T
+          issue_ss(tdP, Lay::kF1, Lay::x1(st));   // dP^T = V dO^T
           ptx::mma_commit(bar(kSFull));
           if (!wait1(bar(kPReady), p_cnt & 1u, abort_flag, p)) { ok = false; break; }
           ++p_cnt;
           ptx::tc_fence_after();
           const bool first = (f == it.x_lo);
-          if (kDKDV) {
-            issue_ts(tA0, tS, Lay::x1(st), first);   // dV += P^T dO
-            issue_ts(tA1, tdP, Lay::x0(st), first);  // dK += dS^T Q
-          } else {
-            issue_ts(tA0, tS, Lay::x0(st), first);   // dQ += dS K
-          }
-          ptx::mma_commit(bar(kXEmpty + st));
+          issue_ts(tA0, tS, Lay::x1(st), first, 64);   // dV += P^T dO
+          issue_ts(tA1, tdP, Lay::x0(st), first, 64);  // dK += dS^T Q
+          ptx::mma_commit(bar(kX0Empty + st));
+          ptx::mma_commit(bar(kX1Empty + st));
           ++x_iter;
         }
         if (!ok) break;
@@ -362,17 +426,74 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (use > 0 &&
                 !wait_warp(bar(kVecFree + buf), (use - 1u) & 1u, abort_flag, p)) { ok = false; break; }
             const int q = xs + threadIdx.x;
-            vec[(buf * 2 + 0) * kT + threadIdx.x] = q < xe ? __ldg(p.lse + bh_off + q) * kLog2e : 0.f;
-            vec[(buf * 2 + 1) * kT + threadIdx.x] = q < xe ? __ldg(p.delta + bh_off + q) : 0.f;
+            vec[(buf * 2 + 0) * kT + threadIdx.x] = q < xe ? -__ldg(p.lse + bh_off + q) * kLog2e : 0.f;
+            vec[(buf * 2 + 1) * kT + threadIdx.x] = q < xe ? -__ldg(p.delta + bh_off + q) : 0.f;
             ptx::mbar_arrive(bar(kVecFull + buf));
           }
           if (!wait_warp(bar(kVecFull + buf), use & 1u, abort_flag, p)) { ok = false; break; }
         }
+        const uint32_t n = s_cnt;
         if (!wait_warp(bar(kSFull), s_cnt & 1u, abort_flag, p)) { ok = false; break; }
         ++s_cnt;
         ptx::tc_fence_after();
         const int c_lo = lo_r - xs;
         const int c_hi = min(hi_r, xe - 1) - xs;
+        if constexpr (!kDKDV) {
+          // Read all of this half of S and dP, release them for the next
+          // step's products, then form dS into buffer n % 2.
+          uint32_t sv[2][32], dv[2][32];
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            ptx::tmem_ld32(tS + col0 + ch * 32, sv[ch]);
+            ptx::tmem_ld32(tdP + col0 + ch * 32, dv[ch]);
+          }
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            ptx::reg_fence(sv[ch]);
+            ptx::reg_fence(dv[ch]);
+          }
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(kSConsumed));
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            const int c0 = col0 + ch * 32;
+            uint32_t pk_s[16];
+            if (__all_sync(0xffffffffu, c_lo <= c0 && c_hi >= c0 + 31)) {
+              // every column visible to every row of the warp: paired fp32
+#pragma unroll
+              for (int x = 0; x < 16; ++x) {
+                float e0, e1, g0, g1;
+                ptx::fma_f32x2(e0, e1, __uint_as_float(sv[ch][2 * x]), __uint_as_float(sv[ch][2 * x + 1]),
+                               sc, sc, -lse2_r, -lse2_r);
+                const float p0 = ptx::ex2(e0), p1 = ptx::ex2(e1);
+                ptx::fma_f32x2(g0, g1, __uint_as_float(dv[ch][2 * x]), __uint_as_float(dv[ch][2 * x + 1]),
+                               1.f, 1.f, -d_r, -d_r);
+                ptx::fma_f32x2(g0, g1, p0, p1, g0, g1, 0.f, 0.f);
+                pk_s[x] = ptx::pack_bf16(g0, g1);
+              }
+            } else {
+#pragma unroll
+              for (int x = 0; x < 16; ++x) {
+                float dsr[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  const int cc = c0 + 2 * x + e;
+                  const bool vis = cc >= c_lo && cc <= c_hi;
+                  const float pv =
+                      vis ? ptx::ex2(fmaf(__uint_as_float(sv[ch][2 * x + e]), sc, -lse2_r)) : 0.f;
+                  dsr[e] = pv * (__uint_as_float(dv[ch][2 * x + e]) - d_r);
+                }
+                pk_s[x] = ptx::pack_bf16(dsr[0], dsr[1]);
+              }
+            }
+            ptx::tmem_st16(tmem_base + lane_off + kDsBuf + (n & 1u) * 64u + c0 / 2, pk_s);
+          }
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(kPReady + (n & 1u)));
+          continue;
+        }
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch) {
           const int c0 = col0 + ch * 32;
@@ -383,28 +504,50 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::reg_fence(sv);
           ptx::reg_fence(dv);
           uint32_t pk_p[16], pk_s[16];
+          // per-column -lse2 and -D of this chunk, four columns per load
+          const float4* nl4 = reinterpret_cast<const float4*>(vec + (buf * 2 + 0) * kT + c0);
+          const float4* nd4 = reinterpret_cast<const float4*>(vec + (buf * 2 + 1) * kT + c0);
+          if (__all_sync(0xffffffffu, c_lo <= c0 && c_hi >= c0 + 31)) {
+            // every column visible to every row of the warp: paired fp32
 #pragma unroll
-          for (int x = 0; x < 16; ++x) {
-            float pr[2], dsr[2];
+            for (int x4 = 0; x4 < 8; ++x4) {
+              const float4 nl = nl4[x4], nd = nd4[x4];
+              const float nla[4] = {nl.x, nl.y, nl.z, nl.w};
+              const float nda[4] = {nd.x, nd.y, nd.z, nd.w};
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int cc = c0 + 2 * x + e;
-              const float l2 = kDKDV ? vec[(buf * 2 + 0) * kT + cc] : lse2_r;
-              const float dd = kDKDV ? vec[(buf * 2 + 1) * kT + cc] : d_r;
-              const bool vis = cc >= c_lo && cc <= c_hi;
-              const float pv = vis ? ptx::ex2(fmaf(__uint_as_float(sv[2 * x + e]), sc, -l2)) : 0.f;
-              pr[e] = pv;
-              dsr[e] = pv * (__uint_as_float(dv[2 * x + e]) - dd);
+              for (int hx = 0; hx < 2; ++hx) {
+                const int x = 2 * x4 + hx;
+                float e0, e1, g0, g1;
+                ptx::fma_f32x2(e0, e1, __uint_as_float(sv[2 * x]), __uint_as_float(sv[2 * x + 1]), sc,
+                               sc, nla[2 * hx], nla[2 * hx + 1]);
+                const float p0 = ptx::ex2(e0), p1 = ptx::ex2(e1);
+                ptx::fma_f32x2(g0, g1, __uint_as_float(dv[2 * x]), __uint_as_float(dv[2 * x + 1]), 1.f,
+                               1.f, nda[2 * hx], nda[2 * hx + 1]);
+                ptx::fma_f32x2(g0, g1, p0, p1, g0, g1, 0.f, 0.f);
+                pk_p[x] = ptx::pack_bf16(p0, p1);
+                pk_s[x] = ptx::pack_bf16(g0, g1);
+              }
             }
-            pk_p[x] = ptx::pack_bf16(pr[0], pr[1]);
-            pk_s[x] = ptx::pack_bf16(dsr[0], dsr[1]);
-          }
-          if (kDKDV) {
-            ptx::tmem_st16(tS + col0 + ch * 16, pk_p);
-            ptx::tmem_st16(tdP + col0 + ch * 16, pk_s);
           } else {
-            ptx::tmem_st16(tS + col0 + ch * 16, pk_s);
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+              float pr[2], dsr[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int cc = c0 + 2 * x + e;
+                const bool vis = cc >= c_lo && cc <= c_hi;
+                const float pv =
+                    vis ? ptx::ex2(fmaf(__uint_as_float(sv[2 * x + e]), sc, vec[(buf * 2 + 0) * kT + cc]))
+                        : 0.f;
+                pr[e] = pv;
+                dsr[e] = pv * (__uint_as_float(dv[2 * x + e]) + vec[(buf * 2 + 1) * kT + cc]);
+              }
+              pk_p[x] = ptx::pack_bf16(pr[0], pr[1]);
+              pk_s[x] = ptx::pack_bf16(dsr[0], dsr[1]);
+            }
           }
+          ptx::tmem_st16(tS + col0 + ch * 16, pk_p);
+          ptx::tmem_st16(tdP + col0 + ch * 16, pk_s);
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
@@ -484,8 +627,9 @@ __global__ void __launch_bounds__(256)
 
 template <int D, bool kDKDV>
 cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
-  using Lay = BLayout<D>;
+  using Lay = BLayout<D, kDKDV>;
   static_assert(Lay::kAlloc <= 232448, "shared memory budget");
+  static_assert(Lay::kX0Slots <= 3 && Lay::kX1Slots == 2, "barrier slots");
   auto kern = ring_attn_bwd_kernel<D, kDKDV>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -526,6 +670,18 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
   if (!p.err) return cudaErrorInvalidValue;
   p.timeout_ns = kTimeoutNs;
   const int grid = static_cast<int>(std::min<long long>(items, sm_count()));
+  // Head groups as in the forward: a launch with at least 16 rounds of the
+  // grid and no document layout takes the smallest group whose items fill
+  // two rounds; otherwise one pool keeps the heaviest-first deal balanced.
+  {
+    const int BH = a.B * a.H;
+    long long hg = BH;
+    if (a.doc_offsets == nullptr && items >= 16LL * grid) {
+      hg = (2LL * grid + p.n_tiles - 1) / p.n_tiles;
+      hg = std::max<long long>(1, std::min<long long>(hg, BH));
+    }
+    p.head_group = static_cast<int>(hg);
+  }
   if (grid <= 0) return cudaSuccess;
   kern<<<grid, kThreads, Lay::kAlloc, stream>>>(m0, m1, m2, m3, p);
   count_launch(0);
