@@ -85,6 +85,9 @@ constexpr float kRescaleLog2 = 8.0f;
 //                          paired fp32 FMA / ADD (two elements per instruction).
 //  CPRING_SPLIT_LOAD       fast pass: read the second half of S from TMEM
 //                          while the first half's exponentials run.
+//  CPRING_FP8_FAST         the FP8 kernel uses the same no-max fast pass, with
+//                          the row-sum guard at 2^8 so that every P it keeps
+//                          is at most 2^8, inside E4M3's range (448).
 #ifndef CPRING_BALANCE
 #define CPRING_BALANCE 2
 #endif
@@ -100,8 +103,12 @@ constexpr float kRescaleLog2 = 8.0f;
 #ifndef CPRING_SPLIT_LOAD
 #define CPRING_SPLIT_LOAD 0
 #endif
+#ifndef CPRING_FP8_FAST
+#define CPRING_FP8_FAST 1
+#endif
 constexpr int kPReadyCount = 128;
 constexpr float kOverflowGuard = 18446744073709551616.0f;  // 2^64
+constexpr float kOverflowGuardFp8 = 256.0f;                  // 2^8: P <= 2^8 < 448
 constexpr unsigned long long kTimeoutNs = 4000000000ull;  // per wait
 
 template <int D, int E>  // E = bytes per element (2 bf16, 1 E4M3)
@@ -357,6 +364,25 @@ __device__ __forceinline__ void exp_chunks(const uint32_t (&sv)[4][32], int half
   }
 }
 
+// The FP8 form of exp_chunks: P as E4M3 quads into pk[0] (P[4c] lowest byte).
+__device__ __forceinline__ void exp_chunks_f8(const uint32_t (&sv)[4][32], int half, float sc,
+                                              float base, uint32_t (&pk)[2][32], uint64_t& acc) {
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc) {
+    const int ch = 2 * half + cc;
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+      float e0, e1, e2, e3;
+      fma2(e0, e1, __uint_as_float(sv[ch][4 * x]), __uint_as_float(sv[ch][4 * x + 1]), sc, -base);
+      fma2(e2, e3, __uint_as_float(sv[ch][4 * x + 2]), __uint_as_float(sv[ch][4 * x + 3]), sc, -base);
+      const float p0 = ptx::ex2(e0), p1 = ptx::ex2(e1), p2 = ptx::ex2(e2), p3 = ptx::ex2(e3);
+      add2(acc, p0, p1);
+      add2(acc, p2, p3);
+      pk[0][ch * 8 + x] = ptx::pack_e4m3x4(p0, p1, p2, p3);
+    }
+  }
+}
+
 // Masks columns outside [c_lo, c_hi] of chunks 2*half, 2*half+1.
 __device__ __forceinline__ void mask_chunks(uint32_t (&sv)[4][32], int half, int c_lo, int c_hi) {
 #pragma unroll
@@ -371,12 +397,20 @@ __device__ __forceinline__ void mask_chunks(uint32_t (&sv)[4][32], int half, int
 // The common case of the fused kernel: load this lane's S row (in two
 // halves, the second in flight while the first is exponentiated), mask it,
 // and form P and its row sum against the current reference.  No row max.
+template <bool kFp8 = false>
 __device__ __forceinline__ void fast_pass(uint32_t tS, int c_lo, int c_hi, float sc, float base,
                                           uint32_t (&sv)[4][32], uint32_t (&pk)[2][32],
                                           float& lsum) {
   const bool need_mask = (c_lo > 0 || c_hi < kBN - 1);
   uint64_t acc = 0;  // two fp32 zeros
   float ls = 0.f;
+  if constexpr (kFp8) {
+    load_scores(tS, c_lo, c_hi, sv);
+    exp_chunks_f8(sv, 0, sc, base, pk, acc);
+    exp_chunks_f8(sv, 1, sc, base, pk, acc);
+    lsum = sum2(acc);
+    return;
+  }
   if (CPRING_SPLIT_LOAD) {
     ptx::tmem_ld32(tS, sv[0]);
     ptx::tmem_ld32(tS + 32, sv[1]);
@@ -711,15 +745,18 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
         float lsum, mx;
         float alpha = 1.f;
         bool rescale_o = false;
-        const bool fast = CPRING_FUSED_NOMAX && !kPartial && !kFp8 &&
+        const bool fast = CPRING_FUSED_NOMAX && !kPartial && (!kFp8 || CPRING_FP8_FAST) &&
                           !__any_sync(0xffffffffu, m_used == -INFINITY);
         if (fast) {
-          fast_pass(tS, c_lo, c_hi, sc, m_used, sv, pk, lsum);
-          const bool redo = !(lsum <= kOverflowGuard);
+          fast_pass<kFp8>(tS, c_lo, c_hi, sc, m_used, sv, pk, lsum);
+          const bool redo = !(lsum <= (kFp8 ? kOverflowGuardFp8 : kOverflowGuard));
           if (__any_sync(0xffffffffu, redo)) {
-            // Rare: exponentials ran past 2^64.  Reload S (P is not yet
-            // written), move the reference to this tile's max and let every
-            // lane recompute (lanes that keep their reference get the same P).
+            // Rare: the row sum ran past its guard (2^64; 2^8 in the FP8
+            // form, where it keeps every P inside E4M3's range).  A sum above
+            // the guard means this tile's max is above the reference (128
+            // entries of at most 1 sum to 128 or less).  Reload S (P is not
+            // yet written), move the reference to this tile's max and let
+            // every lane recompute (lanes that keep theirs get the same P).
             load_scores(tS, c_lo, c_hi, sv);
             const float m_tile = row_max(sv) * sc;
             if (redo && m_tile > m_used) {
