@@ -36,7 +36,7 @@ def _nvcc() -> str:
 # setmaxnreg; the split is sized for exactly this many registers per thread at
 # launch, so a build that comes out different is refused (the split would not
 # fit and the kernel would stall).
-SPLIT_KERNELS = ("ring_attn_bf16_kernel", "ring_attn_fp8_kernel")
+SPLIT_KERNELS = ("ring_attn_bf16_kernel", "ring_attn_fp8_kernel", "ring_attn_bwd_kernel")
 SPLIT_LAUNCH_REGS = 168
 
 

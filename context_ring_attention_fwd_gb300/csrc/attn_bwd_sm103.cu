@@ -24,11 +24,12 @@
 // is that S and dP are formed by both kernels (7 tile products where the
 // gradient needs 5).
 //
-// CTA (320 threads): warps 0-3 and 4-7 split the 128 columns of each S / dP
+// CTA (384 threads): warps 0-3 and 4-7 split the 128 columns of each S / dP
 // tile (64 each) over the same 128 rows, one thread per TMEM lane; warp 8
-// is the TMA producer (the two fixed tiles once per item, the two streamed
-// tiles of every step into a 2-stage ring); one thread of warp 9 issues every
-// tcgen05.mma.
+// is the TMA producer (the two fixed tiles once per item, the streamed tiles
+// of every step into their slot rings); one thread of warp 9 issues every
+// tcgen05.mma; warps 10-11 only complete the third warpgroup, which hands
+// its registers to the softmax warpgroups through setmaxnreg.
 // TMEM (512 columns): S | dP | acc0 | acc1 (acc0 = dV or dQ, acc1 = dK).
 // Warpgroup w writes its packed bf16 P / dS into the first 32 columns of its
 // own 64-column half of S / dP, so no half is overwritten before its owner
@@ -50,7 +51,12 @@ namespace cpring {
 namespace {
 
 constexpr int kT = kTileRows;       // rows of every tile
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;        // three warpgroups (warps 10, 11 idle)
+constexpr int kLaunchRegs = 168;     // registers per thread at launch (checked by the build)
+constexpr int kSoftmaxRegs = 200;    // softmax warpgroups after setmaxnreg.inc
+constexpr int kControlRegs = 104;    // producer / MMA warpgroup after setmaxnreg.dec
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch's register pool");
 constexpr int kSoftmaxThreads = 256;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -218,7 +224,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = gridDim.x;
   const int c = blockIdx.x;
 
-  if (warp == kProducerWarp) {
+  if (warp >= kProducerWarp) {
+   // the third warpgroup gives registers away, then splits into its roles
+   ptx::setmaxnreg_dec<kControlRegs>();
+   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       ptx::tma_prefetch_desc(&tm_f0);
@@ -378,7 +387,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mma_commit(bar(kDrain));
       wait1(bar(kDrain), 0u, abort_flag, p, false);
     }
+   }
   } else {
+    ptx::setmaxnreg_inc<kSoftmaxRegs>();
     // ------------------------------------------------------------ softmax
     const int wg = warp >> 2;        // column half of this warpgroup
     const int wq = warp & 3;         // TMEM lane quarter
@@ -494,15 +505,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mbar_arrive(bar(kPReady + (n & 1u)));
           continue;
         }
+        // This half of S^T and dP^T in one round trip, then P^T, dS^T.
+        uint32_t svv[2][32], dvv[2][32];
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          ptx::tmem_ld32(tS + col0 + ch * 32, svv[ch]);
+          ptx::tmem_ld32(tdP + col0 + ch * 32, dvv[ch]);
+        }
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          ptx::reg_fence(svv[ch]);
+          ptx::reg_fence(dvv[ch]);
+        }
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch) {
           const int c0 = col0 + ch * 32;
-          uint32_t sv[32], dv[32];
-          ptx::tmem_ld32(tS + c0, sv);
-          ptx::tmem_ld32(tdP + c0, dv);
-          ptx::tmem_wait_ld();
-          ptx::reg_fence(sv);
-          ptx::reg_fence(dv);
+          const uint32_t (&sv)[32] = svv[ch];
+          const uint32_t (&dv)[32] = dvv[ch];
           uint32_t pk_p[16], pk_s[16];
           // per-column -lse2 and -D of this chunk, four columns per load
           const float4* nl4 = reinterpret_cast<const float4*>(vec + (buf * 2 + 0) * kT + c0);
