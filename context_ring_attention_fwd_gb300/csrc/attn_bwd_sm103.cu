@@ -30,10 +30,13 @@
 // of every step into their slot rings); one thread of warp 9 issues every
 // tcgen05.mma; warps 10-11 only complete the third warpgroup, which hands
 // its registers to the softmax warpgroups through setmaxnreg.
-// TMEM (512 columns): S | dP | acc0 | acc1 (acc0 = dV or dQ, acc1 = dK).
-// Warpgroup w writes its packed bf16 P / dS into the first 32 columns of its
-// own 64-column half of S / dP, so no half is overwritten before its owner
-// has read it; the TS products gather their A operand from the two halves.
+// TMEM (512 columns).  kDQ: S | dP | dQ | two buffers of packed dS.  kDKDV
+// runs each 128-query tile as two 64-query halves in two buffers
+// (S^T 64 | dP^T 64) x 2 | dV | dK, so the products of the next half overlap
+// the softmax of the current one.  A warpgroup writes its packed bf16 P / dS
+// into the first columns of the range it read itself, so nothing is
+// overwritten before its owner has read it; the TS products gather their A
+// operand from the warpgroups' pieces.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -94,14 +97,14 @@ enum BBar : int {
   kX1Full = 5,     // + slot (2)
   kX0Empty = 7,    // + slot (3)
   kX1Empty = 10,   // + slot (2)
-  kSFull = 12,     // S and dP of the current step are in TMEM
-  kPReady = 13,    // + step parity (kDQ; kDKDV uses +0): P / dS written by all softmax threads
-  kSConsumed = 15, // kDQ: every softmax thread has read S and dP of the step
-  kAccFull = 16,   // the item's accumulators are final
-  kVecFull = 17,   // + buffer: per-column lse / delta of a query tile written (kDKDV)
-  kVecFree = 19,   // + buffer: every softmax thread is done reading it
-  kDrain = 21,
-  kNumBars = 22
+  kSFull = 12,     // + TMEM buffer (kDKDV; kDQ uses +0): S and dP of a step are in TMEM
+  kPReady = 14,    // + step parity: P / dS written by all softmax threads
+  kSConsumed = 16, // kDQ: every softmax thread has read S and dP of the step
+  kAccFull = 17,   // the item's accumulators are final
+  kVecFull = 18,   // + buffer: per-column lse / delta of a query tile written (kDKDV)
+  kVecFree = 20,   // + buffer: every softmax thread is done reading it
+  kDrain = 22,
+  kNumBars = 23
 };
 // kDQ keeps packed dS in its own double buffer of TMEM columns (acc0 ends at
 // 256 + D <= 384), so S and dP of the next step can be issued while the
@@ -200,6 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bar(kX1Empty + s), 1);
     }
     ptx::mbar_init(bar(kSFull), 1);
+    ptx::mbar_init(bar(kSFull + 1), 1);
     ptx::mbar_init(bar(kPReady), kSoftmaxThreads);
     ptx::mbar_init(bar(kPReady + 1), kSoftmaxThreads);
     ptx::mbar_init(bar(kSConsumed), kSoftmaxThreads);
@@ -287,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t d_mn = ptx::smem_desc_sw128(sbase, Lay::kPanelBytes, 1024);  // MN-major
       const uint32_t tS = tmem_base, tdP = tmem_base + 128;
       const uint32_t tA0 = tmem_base + 256, tA1 = tmem_base + 256 + D;
-      uint32_t x_iter = 0, fix_iter = 0, p_cnt = 0;
+      uint32_t x_iter = 0, fix_iter = 0;
       bool ok = true;
       // D_t = A B^T over the head dimension, both tiles K-major.
       auto issue_ss = [&](uint32_t d_tmem, int a_off, int b_off) {
@@ -310,7 +314,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                       kIdescG, (first && s == 0) ? 0u : 1u);
         }
       };
-      uint32_t n = 0;  // kDQ: steps issued so far (all items)
+      uint32_t n = 0;       // kDQ: steps issued so far (all items)
+      uint32_t m_half = 0;  // kDKDV: halves issued so far (all items)
+      constexpr uint32_t kIdescS64 = ptx::idesc_bf16_f32(kT, 64, false);
+      // D = A B^T over the head dimension with B 64 rows (a half tile).
+      auto issue_ss64 = [&](uint32_t d_tmem, int a_off, int b_off) {
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s) {
+          const uint64_t step =
+              static_cast<uint64_t>(((s >> 2) * Lay::kPanelBytes + (s & 3) * 32) >> 4);
+          ptx::mma_ss(d_tmem, d_k + (a_off >> 4) + step, d_k + (b_off >> 4) + step, kIdescS64,
+                      s > 0 ? 1u : 0u);
+        }
+      };
+      // acc (+)= A B over 64 queries: A = the two warpgroups' packed pieces
+      // (32 columns apart), B = the half tile at b_off read MN-major.
+      auto issue_ts64 = [&](uint32_t acc, uint32_t a_tmem, int b_off, bool first) {
+#pragma unroll
+        for (int s = 0; s < 64 / 16; ++s) {
+          const uint32_t a_col = static_cast<uint32_t>((s >> 1) * 32 + (s & 1) * 8);
+          ptx::mma_ts(acc, a_tmem + a_col, d_mn + (b_off >> 4) + static_cast<uint64_t>(s * 128),
+                      kIdescG, (first && s == 0) ? 0u : 1u);
+        }
+      };
       for (int k = 0; ok; ++k) {
         const int w = item_of(k, c, G);
         if (w >= p.n_items) break;
@@ -360,25 +386,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mma_commit(bar(kAccFull));
           continue;
         }
-        for (int f = it.x_lo; f <= it.x_hi; ++f) {
-          const uint32_t st = x_iter % Lay::kX0Slots;   // both rings have two slots here
-          const uint32_t ph = (x_iter / Lay::kX0Slots) & 1u;
-          if (!wait1(bar(kX0Full + st), ph, abort_flag, p)) { ok = false; break; }
-          if (!wait1(bar(kX1Full + st), ph, abort_flag, p)) { ok = false; break; }
+        // kDKDV: half hh of the item is query rows 64 (hh % 2) .. of its
+        // streamed tile x_iter + hh / 2; m counts halves over all items and
+        // half m uses TMEM buffer m % 2.  S^T, dP^T of half m + 1 are issued
+        // before dV, dK of half m, so they run during the softmax of half m.
+        const int nh = 2 * (it.x_hi - it.x_lo + 1);
+        auto issue_half = [&](uint32_t mm, int hh2) -> bool {
+          const uint32_t xi = x_iter + static_cast<uint32_t>(hh2 >> 1);
+          const uint32_t st = xi % Lay::kX0Slots, ph = (xi / Lay::kX0Slots) & 1u;
+          if (!wait1(bar(kX0Full + st), ph, abort_flag, p)) return false;
+          if (!wait1(bar(kX1Full + st), ph, abort_flag, p)) return false;
           ptx::tc_fence_after();
-          issue_ss(tS, Lay::kF0, Lay::x0(st));    // S^T = K Q^T
-          issue_ss(tdP, Lay::kF1, Lay::x1(st));   // dP^T = V dO^T
-          ptx::mma_commit(bar(kSFull));
-          if (!wait1(bar(kPReady), p_cnt & 1u, abort_flag, p)) { ok = false; break; }
-          ++p_cnt;
+          const uint32_t b = mm & 1u;
+          const int rows = (hh2 & 1) * 64 * 128;   // byte offset of query row 64 in a panel
+          issue_ss64(tmem_base + 128u * b, Lay::kF0, Lay::x0(st) + rows);         // S^T = K Q_h^T
+          issue_ss64(tmem_base + 128u * b + 64u, Lay::kF1, Lay::x1(st) + rows);   // dP^T = V dO_h^T
+          ptx::mma_commit(bar(kSFull + b));
+          return true;
+        };
+        if (!issue_half(m_half, 0)) { ok = false; break; }
+        for (int hh = 0; hh < nh; ++hh) {
+          const uint32_t b = m_half & 1u;
+          if (hh + 1 < nh && !issue_half(m_half + 1, hh + 1)) { ok = false; break; }
+          if (!wait1(bar(kPReady + b), (m_half >> 1) & 1u, abort_flag, p)) { ok = false; break; }
           ptx::tc_fence_after();
-          const bool first = (f == it.x_lo);
-          issue_ts(tA0, tS, Lay::x1(st), first, 64);   // dV += P^T dO
-          issue_ts(tA1, tdP, Lay::x0(st), first, 64);  // dK += dS^T Q
-          ptx::mma_commit(bar(kX0Empty + st));
-          ptx::mma_commit(bar(kX1Empty + st));
-          ++x_iter;
+          const uint32_t st = (x_iter + static_cast<uint32_t>(hh >> 1)) % Lay::kX0Slots;
+          const int rows = (hh & 1) * 64 * 128;
+          issue_ts64(tA0, tmem_base + 128u * b, Lay::x1(st) + rows, hh == 0);        // dV += P^T dO_h
+          issue_ts64(tA1, tmem_base + 128u * b + 64u, Lay::x0(st) + rows, hh == 0);  // dK += dS^T Q_h
+          if (hh & 1) {
+            ptx::mma_commit(bar(kX0Empty + st));
+            ptx::mma_commit(bar(kX1Empty + st));
+          }
+          ++m_half;
         }
+        if (!ok) break;
+        x_iter += static_cast<uint32_t>(nh >> 1);
         if (!ok) break;
         ptx::mma_commit(bar(kFixEmpty));
         ptx::mma_commit(bar(kAccFull));
@@ -400,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tA0 = tS + 256, tA1 = tS + 256 + D;
     const int col0 = wg * 64;
     const float sc = p.scale_log2;
-    uint32_t s_cnt = 0, item_cnt = 0;
+    uint32_t s_cnt = 0, item_cnt = 0, h_cnt = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int w = item_of(k, c, G);
@@ -443,13 +486,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!wait_warp(bar(kVecFull + buf), use & 1u, abort_flag, p)) { ok = false; break; }
         }
-        const uint32_t n = s_cnt;
-        if (!wait_warp(bar(kSFull), s_cnt & 1u, abort_flag, p)) { ok = false; break; }
-        ++s_cnt;
-        ptx::tc_fence_after();
         const int c_lo = lo_r - xs;
         const int c_hi = min(hi_r, xe - 1) - xs;
         if constexpr (!kDKDV) {
+          const uint32_t n = s_cnt;
+          if (!wait_warp(bar(kSFull), s_cnt & 1u, abort_flag, p)) { ok = false; break; }
+          ++s_cnt;
+          ptx::tc_fence_after();
           // Read all of this half of S and dP, release them for the next
           // step's products, then form dS into buffer n % 2.
           uint32_t sv[2][32], dv[2][32];
@@ -505,24 +548,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mbar_arrive(bar(kPReady + (n & 1u)));
           continue;
         }
-        // This half of S^T and dP^T in one round trip, then P^T, dS^T.
-        uint32_t svv[2][32], dvv[2][32];
-#pragma unroll
-        for (int ch = 0; ch < 2; ++ch) {
-          ptx::tmem_ld32(tS + col0 + ch * 32, svv[ch]);
-          ptx::tmem_ld32(tdP + col0 + ch * 32, dvv[ch]);
-        }
-        ptx::tmem_wait_ld();
-#pragma unroll
-        for (int ch = 0; ch < 2; ++ch) {
-          ptx::reg_fence(svv[ch]);
-          ptx::reg_fence(dvv[ch]);
-        }
-#pragma unroll
-        for (int ch = 0; ch < 2; ++ch) {
-          const int c0 = col0 + ch * 32;
-          const uint32_t (&sv)[32] = svv[ch];
-          const uint32_t (&dv)[32] = dvv[ch];
+        ++s_cnt;  // query tiles seen: selects the per-column buffer
+        // The two 64-query halves of this tile; half m uses TMEM buffer m % 2.
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t b = h_cnt & 1u;
+          if (!wait_warp(bar(kSFull + b), (h_cnt >> 1) & 1u, abort_flag, p)) { ok = false; break; }
+          ptx::tc_fence_after();
+          // this warpgroup's 32 columns of S^T and dP^T in buffer b
+          const uint32_t tb = tmem_base + lane_off + 128u * b + 32u * static_cast<uint32_t>(wg);
+          uint32_t sv[32], dv[32];
+          ptx::tmem_ld32(tb, sv);
+          ptx::tmem_ld32(tb + 64, dv);
+          ptx::tmem_wait_ld();
+          ptx::reg_fence(sv);
+          ptx::reg_fence(dv);
+          const int c0 = 64 * h + 32 * wg;   // first tile column of this piece
           uint32_t pk_p[16], pk_s[16];
           // per-column -lse2 and -D of this chunk, four columns per load
           const float4* nl4 = reinterpret_cast<const float4*>(vec + (buf * 2 + 0) * kT + c0);
@@ -566,13 +606,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               pk_s[x] = ptx::pack_bf16(dsr[0], dsr[1]);
             }
           }
-          ptx::tmem_st16(tS + col0 + ch * 16, pk_p);
-          ptx::tmem_st16(tdP + col0 + ch * 16, pk_s);
+          ptx::tmem_st16(tb, pk_p);
+          ptx::tmem_st16(tb + 64, pk_s);
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(kPReady + b));
+          ++h_cnt;
         }
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(kPReady));
-        if (kDKDV) ptx::mbar_arrive(bar(kVecFree + buf));
+        if (!ok) break;
+        ptx::mbar_arrive(bar(kVecFree + buf));
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
