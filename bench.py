@@ -621,6 +621,52 @@ def run_bwd(args, w, local):
     }
 
 
+def run_skip_check(args, w, local):
+    """The schedule's acceptance checks on the workload's shape: the time of
+    the causal forward over the time of the same shape without the causal
+    mask (the computed-tile ratio is the ideal), and the causal time at
+    N = 1, 2, 4, 8 shards (equal work, so equal time).  One JSON line."""
+    import context_ring_attention_fwd_gb300 as pkg
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    q, k, v = inputs.make_qkv(w.B, w.S, w.H, w.d, w.seed, w.torch_dtype, w.scale, device=str(dev))
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(n_shards, causal):
+        for _ in range(args.warmup):
+            pkg.cp_ring_attn_fwd(q, k, v, out, lse, n_shards, causal, None, stream)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            pkg.cp_ring_attn_fwd(q, k, v, out, lse, n_shards, causal, None, stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / args.steps
+
+    t_causal = timed(w.n_shards, True)
+    t_full = timed(w.n_shards, False)
+    by_n = {n: timed(n, True) for n in (1, 2, 4, 8) if w.S % n == 0}
+    if pkg.cp_get_last_status(stream) != 0:
+        raise RuntimeError("device error in the schedule check")
+    L = w.S // w.n_shards
+    T = -(-L // 128)
+    n_tiles = w.n_shards * T
+    causal_tiles = sum(min(n_tiles, (qt // T) * T + qt % T + 1) for qt in range(n_tiles))
+    ideal = causal_tiles / (n_tiles * n_tiles)
+    spread = (max(by_n.values()) - min(by_n.values())) / min(by_n.values())
+    return {
+        "metric": "schedule checks of the fused forward", "impl": "skip_check",
+        "ms_causal": t_causal, "ms_full": t_full, "causal_over_full": t_causal / t_full,
+        "computed_tile_ratio": ideal, "ms_causal_by_n_shards": by_n,
+        "n_shards_spread": spread, "steps": args.steps, "warmup": args.warmup,
+        "n_gpus": 1, "dtype": w.dtype, "data": "synthetic", "config": _config(w, None, 1),
+    }
+
+
 def measured_peaks_hbm():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -647,6 +693,8 @@ def main(argv=None):
     ap.add_argument("--fp8", action="store_true",
                     help="time the FP8 (E4M3) form instead")
     ap.add_argument("--bwd", action="store_true", help="time the backward instead")
+    ap.add_argument("--skip-check", action="store_true",
+                    help="causal / full time ratio and shard-count invariance instead")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the attention kernel from an ncu capture")
     args = ap.parse_args(argv)
@@ -654,10 +702,11 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_env()
     w = inputs.BY_NAME[args.workload]
-    if args.ring_emulation or args.ulysses or args.fp8 or args.bwd:
+    if args.ring_emulation or args.ulysses or args.fp8 or args.bwd or args.skip_check:
         line = (run_ring_emulation(args, w, local) if args.ring_emulation
                 else run_ulysses(args, w, local) if args.ulysses
-                else run_fp8(args, w, local) if args.fp8 else run_bwd(args, w, local))
+                else run_fp8(args, w, local) if args.fp8
+                else run_bwd(args, w, local) if args.bwd else run_skip_check(args, w, local))
         if rank == 0:
             print(json.dumps(line), flush=True)
         return

@@ -22,7 +22,8 @@ from ._binding import (  # noqa: F401
     cp_lse_finalize, cp_lse_merge, cp_ring_attn_bwd, cp_ring_attn_bwd_workspace_bytes,
     cp_ring_attn_fwd, cp_ring_attn_fwd_emulated,
     cp_ring_attn_fwd_f32, cp_ring_attn_fwd_fp8,
-    cp_ring_emulated_workspace_bytes, cp_ring_schedule, cp_ring_step, cp_ulysses_attn_fwd,
+    cp_ring_emulated_workspace_bytes, cp_ring_schedule, cp_ring_schedule_device, cp_ring_step,
+    cp_ulysses_attn_fwd,
     cp_ulysses_workspace_bytes,
     cp_ring_traffic, cp_status_string, doc_offsets_tensor, launch_counts, lib,
     test_set_wait_fault)

@@ -50,6 +50,7 @@ _SIGS = {
                                   _vp, _vp, ctypes.POINTER(_i64)],
     "cp_fp8_quantize": [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp],
     "cp_ring_attn_bwd_workspace_bytes": [_i, _i, _i, _i, _i],
+    "cp_ring_schedule_device": [_i, _i, _i, _vp, _vp, _vp],
     "cp_ring_attn_bwd": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp,
                          _vp, _i64, _vp],
     "cp_ring_attn_fwd_fp8": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp,
@@ -361,6 +362,21 @@ def cp_ring_schedule(S: int, n_shards: int, tile_q: int, tile_k: int, causal: bo
                                                   docs, ctypes.cast(buf, ctypes.c_void_p), cnt,
                                                   ctypes.byref(n)))
     return [(buf[2 * x], buf[2 * x + 1]) for x in range(cnt)]
+
+
+def cp_ring_schedule_device(S: int, n_shards: int, causal: bool = True,
+                            doc_offsets: Optional[torch.Tensor] = None, device="cuda",
+                            stream=None) -> torch.Tensor:
+    """The fused kernel's key-tile range per 128-row query tile, computed on the
+    device: int32 [n_tiles, 2] (first, last flat key tile)."""
+    L = S // n_shards
+    n_tiles = n_shards * ((L + 127) // 128)
+    out = torch.full((n_tiles, 2), -7, dtype=torch.int32, device=device)
+    if doc_offsets is not None:
+        _need(doc_offsets, "doc_offsets", torch.int32)
+    _check("cp_ring_schedule_device", lib().cp_ring_schedule_device(
+        S, n_shards, int(bool(causal)), _ptr(doc_offsets), _ptr(out), _stream(stream)))
+    return out
 
 
 def cp_ring_traffic(B: int, S: int, H: int, d: int, dtype_bytes: int, n_shards: int,

@@ -308,6 +308,34 @@ cp_status cp_ring_schedule(int S, int n_shards, int tile_q, int tile_k, int caus
   return CP_OK;
 }
 
+cp_status cp_ring_schedule_device(int S, int n_shards, int causal, const int32_t* doc_offsets,
+                                  int32_t* ranges, cudaStream_t stream) {
+  if (!ranges) return CP_ERR_NULL;
+  if (S < 1 || n_shards < 1 || n_shards > S || S % n_shards != 0) return CP_ERR_SHAPE;
+  if (causal != 0 && causal != 1) return CP_ERR_SHAPE;
+  if (!aligned(ranges, 4) || !aligned(doc_offsets, 4)) return CP_ERR_ALIGN;
+  cp_status st = check_device();
+  if (st != CP_OK) return st;
+  AttnArgs a{};
+  a.S = S;
+  a.n_shards = n_shards;
+  a.causal = causal;
+  a.doc_offsets = doc_offsets;
+  int32_t* info = nullptr;
+  if (doc_offsets) {
+    if (cudaMallocAsync(reinterpret_cast<void**>(&info), 16, stream) != cudaSuccess)
+      return CP_ERR_CUDA;
+    if (cpring::launch_doc_scan(doc_offsets, S, info, stream) != cudaSuccess) {
+      cudaFreeAsync(info, stream);
+      return CP_ERR_CUDA;
+    }
+    a.doc_info = info;
+  }
+  const cudaError_t e = cpring::launch_schedule_probe(a, ranges, stream);
+  if (info) cudaFreeAsync(info, stream);
+  return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+}
+
 cp_status cp_ring_traffic(int64_t B, int64_t S, int64_t H, int64_t d, int dtype_bytes,
                           int n_shards, int causal, int64_t* per_rank_bytes) {
   if (!per_rank_bytes) return CP_ERR_NULL;

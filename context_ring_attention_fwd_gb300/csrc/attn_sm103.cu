@@ -1029,6 +1029,50 @@ cudaError_t launch_attn_bf16(const AttnArgs& a, cudaStream_t stream) {
   return cudaErrorInvalidValue;
 }
 
+// The tile ranges the fused kernel walks, from its own decode_item: for
+// every 128-row query tile (flat order) the first and last flat key tile.
+__global__ void schedule_probe_kernel(const KParams p, int32_t* __restrict__ ranges) {
+  const int w = blockIdx.x * blockDim.x + threadIdx.x;
+  if (w >= p.n_items) return;
+  int n_docs = 1;
+  if (p.doc_offsets != nullptr) {
+    n_docs = __ldg(p.doc_info);
+    if (n_docs <= 0) return;
+  }
+  Item it;
+  decode_item(p, n_docs, w, it);
+#pragma unroll
+  for (int t = 0; t < kQTiles; ++t) {
+    if (it.rows[t] == 0) continue;
+    const int qt = it.i * p.tiles_per_shard + (it.q0[t] - it.i * p.L) / kBM;
+    ranges[2 * qt] = it.f_lo[t];
+    ranges[2 * qt + 1] = it.f_hi[t];
+  }
+}
+
+cudaError_t launch_schedule_probe(const AttnArgs& a, int32_t* ranges, cudaStream_t stream) {
+  KParams p{};
+  p.B = 1;
+  p.S = a.S;
+  p.H = 1;
+  p.n_shards = a.n_shards;
+  p.L = a.S / a.n_shards;
+  p.q_shard = -1;
+  p.k_shard = -1;
+  p.causal = a.causal;
+  p.doc_offsets = a.doc_offsets;
+  p.doc_info = a.doc_info;
+  p.n_qshards = a.n_shards;
+  p.pairs_per_shard = (p.L + kBM * kQTiles - 1) / (kBM * kQTiles);
+  p.tiles_per_shard = (p.L + kBN - 1) / kBN;
+  p.n_items = p.n_qshards * p.pairs_per_shard;
+  p.head_group = 1;
+  const int grid = (p.n_items + 127) / 128;
+  schedule_probe_kernel<<<grid, 128, 0, stream>>>(p, ranges);
+  count_launch(2);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_attn_fp8(const AttnArgs& a, cudaStream_t stream) {
   if (a.d != 128 || a.k_shard >= 0 || a.q_shard >= 0 || !a.q_descale || !a.k_descale ||
       !a.v_descale)

@@ -67,6 +67,9 @@ cudaError_t launch_attn_f32(const AttnArgs& a, cudaStream_t stream);
 // FP8 form: q, k E4M3 [B, S, H, 128], v E4M3 [B, H, 128, S]; the fused
 // forward only (q_shard = k_shard = -1).
 cudaError_t launch_attn_fp8(const AttnArgs& a, cudaStream_t stream);
+// The fused kernel's per-query-tile key-tile ranges (first, last flat tile),
+// computed on the device by the kernel's own work decoding (B = H = 1).
+cudaError_t launch_schedule_probe(const AttnArgs& a, int32_t* ranges, cudaStream_t stream);
 // Backward: the row sums D, then the dK/dV kernel and the dQ kernel (bf16,
 // d in {64, 128}).
 cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream);

@@ -195,6 +195,22 @@ cp_status cp_ring_schedule(int S, int n_shards, int tile_q, int tile_k, int caus
                            int64_t* n_pairs);
 
 /*
+ * Diagnostic: the tile schedule the fused bf16 / FP8 kernels actually walk,
+ * computed on the device by the kernels' own work decoding.  For every
+ * 128-row query tile in flat order (tile a of shard i is i * ceil(L/128) + a,
+ * L = S / n_shards) it writes the first and the last flat 128-row key tile of
+ * its contiguous key-tile range, which must equal the range of the pairs
+ * cp_ring_schedule(S, n_shards, 128, 128, causal, ...) lists for that tile.
+ * No counterpart on the pages beyond section 因果掩碼的特殊處理 (which pairs
+ * are needed); it exists so tests can check the device schedule.
+ *  doc_offsets  NULL or device int32 (as cp_ring_attn_fwd).
+ *  ranges       device int32 [n_shards * ceil(L/128) * 2], written.
+ * Takes a 16-byte stream-ordered scratch allocation when doc_offsets is set.
+ */
+cp_status cp_ring_schedule_device(int S, int n_shards, int causal, const int32_t* doc_offsets,
+                                  int32_t* ranges, cudaStream_t stream);
+
+/*
  * Host-only, integer: bytes each virtual rank would send plus receive if the
  * K/V blocks travelled a real ring ("大语言模型并行策略（五）：上下文并行",
  * 通信模式: 2 x (G/N) x (N-1), G = K and V bytes of the whole sequence,

@@ -302,6 +302,26 @@ def test_ulysses_all_to_all_form(causal, docs):
     assert moved == 8 * shard * (N - 1)
 
 
+@pytest.mark.parametrize("S,N,causal,ndocs", [(1024, 4, True, 0), (1040, 2, True, 0),
+                                              (768, 3, False, 0), (2048, 4, True, 5),
+                                              (2048, 1, False, 3), (4096, 8, True, 12)])
+def test_device_schedule_matches_host_schedule(S, N, causal, ndocs):
+    """The key-tile range the fused kernel walks for each 128-row query tile
+    (its own decoding, run on the device) is exactly the contiguous range of
+    the host schedule, which the oracle pins bit for bit."""
+    docs = None if ndocs == 0 else inputs.random_doc_offsets(S, ndocs, seed=S + ndocs)
+    dev = pkg.cp_ring_schedule_device(S, N, causal, pkg.doc_offsets_tensor(docs, DEV)).cpu()
+    pairs = pkg.cp_ring_schedule(S, N, 128, 128, causal, docs)
+    by_q = {}
+    for qt, kt in pairs:
+        by_q.setdefault(qt, []).append(kt)
+    assert sorted(by_q) == list(range(dev.shape[0]))
+    for qt, kts in by_q.items():
+        lo, hi = min(kts), max(kts)
+        assert len(kts) == hi - lo + 1                     # contiguous
+        assert dev[qt].tolist() == [lo, hi], (qt, dev[qt].tolist(), lo, hi)
+
+
 def test_native_kernels_launch():
     before = pkg.launch_counts()
     q, k, v = (t.to(DEV) for t in inputs.make_qkv(1, 256, 1, 128, seed=1, dtype=torch.bfloat16))
