@@ -78,6 +78,7 @@ extern "C" {
 cp_status cp_ring_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
                            int B, int S, int H, int d, int n_shards, int causal,
                            const int32_t* doc_offsets, cudaStream_t stream) {
+  cpring::TraceRange trace_("cp_ring_attn_fwd");
   if (!q || !k || !v || !out || !lse) return CP_ERR_NULL;
   cp_status st = check_shape(B, S, H, d, n_shards);
   if (st != CP_OK) return st;
@@ -101,6 +102,7 @@ cp_status cp_ring_attn_fwd_fp8(const void* q8, const void* k8, const void* v8t,
                                const float* v_descale, void* out, float* lse, int B, int S, int H,
                                int d, int n_shards, int causal, const int32_t* doc_offsets,
                                cudaStream_t stream) {
+  cpring::TraceRange trace_("cp_ring_attn_fwd_fp8");
   if (!q8 || !k8 || !v8t || !q_descale || !k_descale || !v_descale || !out || !lse)
     return CP_ERR_NULL;
   cp_status st = check_shape(B, S, H, d, n_shards);
@@ -134,6 +136,7 @@ cp_status cp_ring_attn_bwd(const void* q, const void* k, const void* v, const vo
                            int B, int S, int H, int d, int n_shards, int causal,
                            const int32_t* doc_offsets, void* workspace, int64_t workspace_bytes,
                            cudaStream_t stream) {
+  cpring::TraceRange trace_("cp_ring_attn_bwd");
   if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || !workspace)
     return CP_ERR_NULL;
   cp_status st = check_shape(B, S, H, d, n_shards);
@@ -166,6 +169,7 @@ cp_status cp_ring_attn_bwd(const void* q, const void* k, const void* v, const vo
 cp_status cp_ring_attn_fwd_f32(const float* q, const float* k, const float* v, float* out,
                                float* lse, int B, int S, int H, int d, int n_shards, int causal,
                                const int32_t* doc_offsets, cudaStream_t stream) {
+  cpring::TraceRange trace_("cp_ring_attn_fwd_f32");
   if (!q || !k || !v || !out || !lse) return CP_ERR_NULL;
   cp_status st = check_shape(B, S, H, d, n_shards);
   if (st != CP_OK) return st;
@@ -217,6 +221,7 @@ cp_status cp_ring_step(const void* q, const void* k, const void* v, float* o_par
                        float* m_part, float* l_part, int B, int S, int H, int d, int n_shards,
                        int i, int j, int causal, const int32_t* doc_offsets,
                        cudaStream_t stream) {
+  cpring::TraceRange trace_("cp_ring_step");
   return ring_step_common(q, k, v, o_part, m_part, l_part, B, S, H, d, n_shards, i, j, causal,
                           doc_offsets, stream, true);
 }
@@ -225,6 +230,7 @@ cp_status cp_ring_step_f32(const float* q, const float* k, const float* v, float
                            float* m_part, float* l_part, int B, int S, int H, int d,
                            int n_shards, int i, int j, int causal,
                            const int32_t* doc_offsets, cudaStream_t stream) {
+  cpring::TraceRange trace_("cp_ring_step_f32");
   return ring_step_common(q, k, v, o_part, m_part, l_part, B, S, H, d, n_shards, i, j, causal,
                           doc_offsets, stream, false);
 }
@@ -232,6 +238,7 @@ cp_status cp_ring_step_f32(const float* q, const float* k, const float* v, float
 cp_status cp_lse_merge(float* o_acc, float* m_acc, float* l_acc, const float* o_part,
                        const float* m_part, const float* l_part, int B, int rows, int H, int d,
                        cudaStream_t stream) {
+  cpring::TraceRange trace_("cp_lse_merge");
   if (!o_acc || !m_acc || !l_acc || !o_part || !m_part || !l_part) return CP_ERR_NULL;
   if (B < 1 || rows < 1 || H < 1 || d < 1) return CP_ERR_SHAPE;
   if (d > 128) return CP_ERR_UNSUPPORTED;
@@ -251,6 +258,7 @@ cp_status cp_lse_merge(float* o_acc, float* m_acc, float* l_acc, const float* o_
 cp_status cp_lse_finalize(const float* o_acc, const float* m_acc, const float* l_acc, void* out,
                           float* lse, int B, int rows, int H, int d, int out_is_bf16,
                           cudaStream_t stream) {
+  cpring::TraceRange trace_("cp_lse_finalize");
   if (!o_acc || !m_acc || !l_acc || !out || !lse) return CP_ERR_NULL;
   if (B < 1 || rows < 1 || H < 1 || d < 1) return CP_ERR_SHAPE;
   if (d > 128) return CP_ERR_UNSUPPORTED;
@@ -310,6 +318,7 @@ cp_status cp_ring_schedule(int S, int n_shards, int tile_q, int tile_k, int caus
 
 cp_status cp_ring_schedule_device(int S, int n_shards, int causal, const int32_t* doc_offsets,
                                   int32_t* ranges, cudaStream_t stream) {
+  cpring::TraceRange trace_("cp_ring_schedule_device");
   if (!ranges) return CP_ERR_NULL;
   if (S < 1 || n_shards < 1 || n_shards > S || S % n_shards != 0) return CP_ERR_SHAPE;
   if (causal != 0 && causal != 1) return CP_ERR_SHAPE;

@@ -161,6 +161,7 @@ __global__ void fp8_descale_kernel(float* v, int n) {
 
 extern "C" cp_status cp_fp8_quantize(const void* x, void* x8, float* descale, int B, int S, int H,
                                      int d, int transpose, cudaStream_t stream) {
+  cpring::TraceRange trace_("cp_fp8_quantize");
   using namespace cpring;
   if (!x || !x8 || !descale) return CP_ERR_NULL;
   if (B < 1 || S < 1 || H < 1 || B > 65535 || H > 65535) return CP_ERR_SHAPE;

@@ -3,6 +3,7 @@
 
 #include <cstdint>
 #include <cuda_runtime_api.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/cpring.h"
 
@@ -53,6 +54,15 @@ struct BwdArgs {
   int causal;
   const int32_t* doc_offsets;  // device or null
   const int32_t* doc_info;     // written by the doc scan, or null
+};
+
+// An NVTX range named after the C-ABI call it covers (tracing for profilers;
+// a no-op unless a profiler is attached, and never a device allocation).
+struct TraceRange {
+  explicit TraceRange(const char* name) { nvtxRangePushA(name); }
+  ~TraceRange() { nvtxRangePop(); }
+  TraceRange(const TraceRange&) = delete;
+  TraceRange& operator=(const TraceRange&) = delete;
 };
 
 // Sticky device error word (bits of kErr*), owned by merge.cu.

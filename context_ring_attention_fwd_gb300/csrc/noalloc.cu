@@ -109,6 +109,7 @@ extern "C" cp_status cp_ring_attn_fwd_noalloc(const void* q, const void* k, cons
                                               void* out, float* lse, int B, int S, int H, int d,
                                               int n_shards, int causal,
                                               const int32_t* doc_offsets, cudaStream_t stream) {
+  cpring::TraceRange trace_("cp_ring_attn_fwd_noalloc");
   using namespace cpring;
   if (!q || !k || !v || !out || !lse) return CP_ERR_NULL;
   if (B < 1 || S < 1 || H < 1 || d < 1 || n_shards < 1 || n_shards > S || S % n_shards != 0)

@@ -69,6 +69,7 @@ extern "C" cp_status cp_ring_attn_fwd_emulated(const void* q, const void* k, con
                                                int64_t workspace_bytes, cudaStream_t stream,
                                                cudaStream_t copy_stream,
                                                int64_t* recv_bytes_per_rank) {
+  cpring::TraceRange trace_("cp_ring_attn_fwd_emulated");
   if (!q || !k || !v || !out || !lse || !workspace) return CP_ERR_NULL;
   if (B < 1 || S < 1 || H < 1 || n_shards < 1 || n_shards > S || S % n_shards != 0)
     return CP_ERR_SHAPE;

@@ -98,6 +98,7 @@ extern "C" cp_status cp_ulysses_attn_fwd(const void* q, const void* k, const voi
                                          int causal, const int32_t* doc_offsets, void* workspace,
                                          int64_t workspace_bytes, cudaStream_t stream,
                                          int64_t* a2a_bytes) {
+  cpring::TraceRange trace_("cp_ulysses_attn_fwd");
   using namespace cpring;
   if (!q || !k || !v || !out || !lse || !workspace) return CP_ERR_NULL;
   if (B < 1 || S < 1 || H < 1 || n_shards < 1 || n_shards > S || S % n_shards != 0)
