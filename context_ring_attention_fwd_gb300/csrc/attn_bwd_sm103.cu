@@ -64,7 +64,6 @@ constexpr int kSoftmaxThreads = 256;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kTmemCols = 512;
-constexpr unsigned long long kTimeoutNs = 4000000000ull;  // per wait
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Streamed tiles run in two rings of single-tile slots: X0 (K for kDQ, Q for
@@ -127,6 +126,7 @@ struct BParams {
   __nv_bfloat16* g1;    // dK (kDKDV)
   int* err;
   unsigned long long timeout_ns;
+  int fault_drop;       // test hook: CTA 0 never loads its first streamed X0 tile
 };
 
 struct BItem {
@@ -240,6 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tma_prefetch_desc(&tm_x1);
       uint32_t x_iter = 0, fix_iter = 0;
       uint32_t armed0[3] = {0u, 0u, 0u}, armed1[2] = {0u, 0u};  // loads started per slot
+      bool dropped = false;
       bool ok = true;
       for (int k = 0; ok; ++k) {
         const int w = item_of(k, c, G);
@@ -261,11 +262,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           int xs, xe;
           tile_keys(p, f, xs, xe);
           if (!wait1(bar(kX0Empty + s0), ph0 ^ 1u, abort_flag, p)) { ok = false; break; }
-          ptx::mbar_arrive_expect_tx(bar(kX0Full + s0), Lay::kTileBytes);
-          for (int pn = 0; pn < Lay::kPanels; ++pn)
-            ptx::tma_load_4d(sbase + Lay::x0(s0) + pn * Lay::kPanelBytes, &tm_x0,
-                             bar(kX0Full + s0), pn * 64, it.h, xs, it.b);
-          ++armed0[s0];
+          if (p.fault_drop && c == 0 && !dropped) {
+            // Test hook: this tile is never loaded, so the MMA thread's
+            // bounded wait for it runs out and the CTA takes its abort path.
+            dropped = true;
+          } else {
+            ptx::mbar_arrive_expect_tx(bar(kX0Full + s0), Lay::kTileBytes);
+            for (int pn = 0; pn < Lay::kPanels; ++pn)
+              ptx::tma_load_4d(sbase + Lay::x0(s0) + pn * Lay::kPanelBytes, &tm_x0,
+                               bar(kX0Full + s0), pn * 64, it.h, xs, it.b);
+            ++armed0[s0];
+          }
           if (!wait1(bar(kX1Empty + s1), ph1 ^ 1u, abort_flag, p)) { ok = false; break; }
           ptx::mbar_arrive_expect_tx(bar(kX1Full + s1), Lay::kTileBytes);
           for (int pn = 0; pn < Lay::kPanels; ++pn)
@@ -730,7 +737,8 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
   p.g1 = static_cast<__nv_bfloat16*>(kDKDV ? a.dk : nullptr);
   p.err = device_error_word();
   if (!p.err) return cudaErrorInvalidValue;
-  p.timeout_ns = kTimeoutNs;
+  p.timeout_ns = test_wait_limit_ns();
+  p.fault_drop = test_fault_drop();
   const int grid = static_cast<int>(std::min<long long>(items, sm_count()));
   // Head groups as in the forward: a launch with at least 16 rounds of the
   // grid and no document layout takes the smallest group whose items fill

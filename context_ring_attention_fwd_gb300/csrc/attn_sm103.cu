@@ -1080,6 +1080,9 @@ cudaError_t launch_attn_fp8(const AttnArgs& a, cudaStream_t stream) {
   return launch_t<128, false, true>(a, stream);
 }
 
+int test_fault_drop() { return g_fault_drop_k.load(); }
+unsigned long long test_wait_limit_ns() { return g_wait_limit_ns.load(); }
+
 }  // namespace cpring
 
 extern "C" void cp_test_set_wait_fault(int drop_first_k_tile, long long wait_limit_ns) {

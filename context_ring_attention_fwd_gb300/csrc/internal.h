@@ -98,6 +98,11 @@ cudaError_t launch_finalize_strided(const float* o_acc, const float* m_acc, cons
                                     int out_is_bf16, long long out_bstride, long long lse_bstride,
                                     long long lse_hstride, cudaStream_t stream);
 
+// Test hook state set by cp_test_set_wait_fault: whether CTA 0 of the next
+// tensor-core launches skips one tile load, and the wait limit in ns.
+int test_fault_drop();
+unsigned long long test_wait_limit_ns();
+
 // Host launch counters (index: 0 tcgen05 attention, 1 fp32 attention,
 // 2 merge/finalize, 3 doc scan).
 void count_launch(int which);

@@ -119,6 +119,29 @@ def test_bwd_constant_v_and_zero_q():
     assert e.max() <= REL_MAX * np.abs(want).max() and e.mean() <= REL_MEAN * np.abs(want).max()
 
 
+def test_bwd_bounded_wait_runs_out_and_context_recovers():
+    """A streamed tile that CTA 0 never loads (a flag nothing sets): the MMA
+    thread's wait gives up after 0.3 s in both backward kernels, each CTA
+    drains and frees its TMEM, the host reads CP_ERR_TIMEOUT, and the next
+    call on the same context matches the oracle."""
+    B, S, H, d, N = 1, 1024, 2, 128, 2
+    q, k, v = (t.to(DEV) for t in inputs.make_qkv(B, S, H, d, 57, torch.bfloat16))
+    dout = inputs.make_qkv(B, S, H, d, 58, torch.bfloat16)[0].to(DEV)
+    out, lse = pkg.ring_attn_fwd(q, k, v, N, True)
+    assert pkg.cp_get_last_status() == 0
+    try:
+        pkg.test_set_wait_fault(True, 300_000_000)
+        pkg.ring_attn_bwd(q, k, v, out, lse, dout, N, True)
+        assert pkg.cp_get_last_status() == pkg.STATUS_CODES["CP_ERR_TIMEOUT"]
+    finally:
+        pkg.test_set_wait_fault(False, 0)
+    assert pkg.cp_get_last_status() == 0
+    got = pkg.ring_attn_bwd(q, k, v, out, lse, dout, N, True)
+    assert pkg.cp_get_last_status() == 0
+    want = ref.attention_bwd(_np(q), _np(k), _np(v), _np(dout), True, None)
+    _check(got, want, "after timeout")
+
+
 def _full_size_checks(w, n_rows, heads):
     q, k, v = inputs.make_qkv(w.B, w.S, w.H, w.d, w.seed, torch.bfloat16, w.scale, device=DEV)
     docs = (inputs.make_doc_offsets(w.S, w.seed + 1, w.doc_min, w.doc_max)
