@@ -31,6 +31,7 @@ _vp, _i, _i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
 _SIGS = {
     "cp_ring_attn_fwd": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp],
     "cp_ring_attn_fwd_noalloc": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp],
+    "cp_ring_attn_fwd_rank": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp],
     "cp_ring_attn_fwd_f32": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp],
     "cp_ring_step": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _vp, _vp],
     "cp_ring_step_f32": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _vp, _vp],
@@ -207,6 +208,21 @@ def cp_ring_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, n_shards: int, causal:
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
         _ptr(dv), B, S, H, d, int(n_shards), int(bool(causal)), _ptr(doc_offsets),
         _ptr(workspace), int(workspace.numel()), _stream(stream)))
+
+
+def cp_ring_attn_fwd_rank(q, k, v, out, lse, n_shards: int, rank: int, causal: bool = True,
+                          doc_offsets: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Rank `rank`'s part of the bf16 fused forward (its query shard's rows of
+    out and lse); the tensors are the whole-sequence ones."""
+    B, S, H, d = q.shape
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _need(t, n, torch.bfloat16, (B, S, H, d))
+    _need(lse, "lse", torch.float32, (B, H, S))
+    if doc_offsets is not None:
+        _need(doc_offsets, "doc_offsets", torch.int32)
+    _check("cp_ring_attn_fwd_rank", lib().cp_ring_attn_fwd_rank(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, H, d, int(n_shards), int(rank),
+        int(bool(causal)), _ptr(doc_offsets), _stream(stream)))
 
 
 def cp_ring_attn_fwd_noalloc(q, k, v, out, lse, n_shards: int, causal: bool = True,

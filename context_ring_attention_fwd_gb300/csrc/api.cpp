@@ -97,6 +97,29 @@ cp_status cp_ring_attn_fwd(const void* q, const void* k, const void* v, void* ou
   return run_attn(a, true, stream);
 }
 
+cp_status cp_ring_attn_fwd_rank(const void* q, const void* k, const void* v, void* out, float* lse,
+                                int B, int S, int H, int d, int n_shards, int rank, int causal,
+                                const int32_t* doc_offsets, cudaStream_t stream) {
+  cpring::TraceRange trace_("cp_ring_attn_fwd_rank");
+  if (!q || !k || !v || !out || !lse) return CP_ERR_NULL;
+  cp_status st = check_shape(B, S, H, d, n_shards);
+  if (st != CP_OK) return st;
+  if (rank < 0 || rank >= n_shards) return CP_ERR_SHAPE;
+  if (d != 64 && d != 128) return CP_ERR_UNSUPPORTED;
+  if (causal != 0 && causal != 1) return CP_ERR_SHAPE;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4) || !aligned(doc_offsets, 4))
+    return CP_ERR_ALIGN;
+  AttnArgs a{};
+  a.q = q; a.k = k; a.v = v;
+  a.B = B; a.S = S; a.H = H; a.d = d; a.n_shards = n_shards;
+  a.q_shard = rank; a.k_shard = -1;
+  a.causal = causal;
+  a.doc_offsets = doc_offsets;
+  a.out = out; a.lse = lse;
+  return run_attn(a, 1, stream);
+}
+
 cp_status cp_ring_attn_fwd_fp8(const void* q8, const void* k8, const void* v8t,
                                const float* q_descale, const float* k_descale,
                                const float* v_descale, void* out, float* lse, int B, int S, int H,

@@ -90,6 +90,22 @@ cp_status cp_ring_attn_fwd(const void* q, const void* k, const void* v, void* ou
                            const int32_t* doc_offsets, cudaStream_t stream);
 
 /*
+ * One virtual rank's part of cp_ring_attn_fwd: rank i's whole ring ("上下文並行
+ * （Context Parallelism, CP）", section 線上 Softmax: GPU i runs the loop over
+ * the K/V shards for its own Q_i).  Writes out rows and lse entries of query
+ * shard `rank` only ([rank*S/N, (rank+1)*S/N) of every batch row and head);
+ * reads Q of that shard and K/V of the shards it needs (under causality,
+ * shards 0..rank).  Pointers, layouts, masks and errors as cp_ring_attn_fwd;
+ * rank outside [0, n_shards) returns CP_ERR_SHAPE.  The N calls for
+ * rank = 0..N-1 give bitwise the result of one cp_ring_attn_fwd call, so a
+ * caller can move shard i's inputs in and its output out while other ranks
+ * compute.
+ */
+cp_status cp_ring_attn_fwd_rank(const void* q, const void* k, const void* v, void* out, float* lse,
+                                int B, int S, int H, int d, int n_shards, int rank, int causal,
+                                const int32_t* doc_offsets, cudaStream_t stream);
+
+/*
  * cp_ring_attn_fwd for callers that cannot let a library allocate device
  * memory.  The pages have no counterpart: this is a deployment variant of the
  * fused forward above, with the same arguments, layouts and result.

@@ -322,6 +322,32 @@ def test_device_schedule_matches_host_schedule(S, N, causal, ndocs):
         assert dev[qt].tolist() == [lo, hi], (qt, dev[qt].tolist(), lo, hi)
 
 
+@pytest.mark.parametrize("B,S,H,d,N,causal,docs", [(1, 1024, 2, 128, 4, True, None),
+                                                    (2, 768, 2, 64, 3, False, None),
+                                                    (1, 1536, 2, 128, 4, True, [0, 300, 301, 777, 1536])])
+def test_rank_calls_and_host_path_equal_the_fused_call(B, S, H, d, N, causal, docs):
+    """cp_ring_attn_fwd_rank for every rank, and the pipelined host-buffer
+    path built on it, give bitwise the result of one cp_ring_attn_fwd call;
+    one rank writes only its own rows."""
+    q, k, v = (t.to(DEV) for t in inputs.make_qkv(B, S, H, d, 61, torch.bfloat16))
+    dd = pkg.doc_offsets_tensor(docs, DEV)
+    want_o, want_l = pkg.ring_attn_fwd(q, k, v, N, causal, docs)
+    out = torch.full_like(q, 3.0)
+    lse = torch.full((B, H, S), 3.0, dtype=torch.float32, device=DEV)
+    L = S // N
+    pkg.cp_ring_attn_fwd_rank(q, k, v, out, lse, N, 1, causal, dd)
+    assert torch.equal(out[:, L:2 * L], want_o[:, L:2 * L])
+    assert torch.equal(lse[:, :, L:2 * L], want_l[:, :, L:2 * L])
+    assert torch.all(out[:, :L] == 3.0) and torch.all(out[:, 2 * L:] == 3.0)
+    assert torch.all(lse[:, :, :L] == 3.0) and torch.all(lse[:, :, 2 * L:] == 3.0)
+    for r in range(N):
+        pkg.cp_ring_attn_fwd_rank(q, k, v, out, lse, N, r, causal, dd)
+    assert torch.equal(out, want_o) and torch.equal(lse, want_l)
+    ho, hl = pkg.ring_attn_fwd_host(*(t.cpu().pin_memory() for t in (q, k, v)), N, causal, docs)
+    assert torch.equal(ho, want_o.cpu()) and torch.equal(hl, want_l.cpu())
+    assert pkg.cp_get_last_status() == 0
+
+
 def test_native_kernels_launch():
     before = pkg.launch_counts()
     q, k, v = (t.to(DEV) for t in inputs.make_qkv(1, 256, 1, 128, seed=1, dtype=torch.bfloat16))

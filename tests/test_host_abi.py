@@ -113,6 +113,15 @@ def test_rejects_before_any_launch(lib):
     assert z(FAKE, FAKE, FAKE, FAKE, ODD, 1, 8, 2, 64, 1, None) == -4
 
 
+def test_rank_entry_point_rejects_before_any_launch(lib):
+    f = lib.cp_ring_attn_fwd_rank
+    assert f(None, FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 128, 4, 0, 1, None, None) == -1
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 128, 4, 4, 1, None, None) == -2
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 128, 4, -1, 1, None, None) == -2
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 96, 4, 0, 1, None, None) == -3
+    assert f(ODD, FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 128, 4, 0, 1, None, None) == -4
+
+
 def test_fp8_entry_points_reject_before_any_launch(lib):
     f = lib.cp_ring_attn_fwd_fp8
     ok = (FAKE,) * 8
