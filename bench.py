@@ -436,7 +436,7 @@ def run_ring_emulation(args, w, local):
 
 def run_ulysses(args, w, local):
     """Time the all-to-all (Ulysses) form against the fused ring kernel on the
-    same inputs.  The time of the form's N head-group attention launches alone
+    same inputs.  The time of the form's head-group attention launch alone
     is taken on head-split copies of the inputs; the rest of the step is the
     permutations (HBM-bound, reported against the measured copy peak) and
     the LSE copies.  One JSON line."""
@@ -470,17 +470,17 @@ def run_ulysses(args, w, local):
     ms_u = timed(lambda: moved.append(pkg.cp_ulysses_attn_fwd(q, k, v, out, lse, w.n_shards,
                                                               w.causal, dd, ws, stream)))
     ms_f = timed(lambda: pkg.cp_ring_attn_fwd(q, k, v, out, lse, w.n_shards, w.causal, dd, stream))
-    # The attention part alone: the same N launches over head groups that the
-    # Ulysses form makes, on head-split copies made here (outside the timing).
+    # The attention part alone: the launch the Ulysses form makes over its
+    # head groups (batch N * B, H / N heads), on head-split copies made here
+    # (outside the timing).
     N, Hg = w.n_shards, w.H // w.n_shards
-    split = [t.view(w.B, w.S, N, Hg, w.d).permute(2, 0, 1, 3, 4).contiguous() for t in (q, k, v)]
-    o_g = torch.empty_like(split[0][0])
-    l_g = torch.empty((w.B, Hg, w.S), dtype=torch.float32, device=dev)
+    split = [t.view(w.B, w.S, N, Hg, w.d).permute(2, 0, 1, 3, 4).contiguous()
+             .view(N * w.B, w.S, Hg, w.d) for t in (q, k, v)]
+    o_g = torch.empty_like(split[0])
+    l_g = torch.empty((N * w.B, Hg, w.S), dtype=torch.float32, device=dev)
 
     def heads_only():
-        for g in range(N):
-            pkg.cp_ring_attn_fwd(split[0][g], split[1][g], split[2][g], o_g, l_g, 1, w.causal, dd,
-                                 stream)
+        pkg.cp_ring_attn_fwd(split[0], split[1], split[2], o_g, l_g, 1, w.causal, dd, stream)
     ms_a = timed(heads_only)
     if pkg.cp_get_last_status(stream) != 0:
         raise RuntimeError("device error in the Ulysses form")

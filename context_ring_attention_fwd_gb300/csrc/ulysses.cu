@@ -126,7 +126,6 @@ extern "C" cp_status cp_ulysses_attn_fwd(const void* q, const void* k, const voi
   float* lh = reinterpret_cast<float*>(ws + 4 * t_bytes);
   const long long rows = static_cast<long long>(B) * S;
   const int chunk = Hg * d * 2;  // bytes of one head group of one token
-  const int64_t head_block = static_cast<int64_t>(B) * S * Hg * d * 2;  // one rank's tensor
 
   int32_t* info = nullptr;
   cudaError_t e = cudaSuccess;
@@ -142,19 +141,22 @@ extern "C" cp_status cp_ulysses_attn_fwd(const void* q, const void* k, const voi
       return CP_ERR_CUDA;
     chk(launch_doc_scan(doc_offsets, S, info, stream));
   }
-  // step 2: rank g attends over the whole sequence for its H/N heads
-  for (int g = 0; g < N && e == cudaSuccess; ++g) {
+  // step 2: rank g attends over the whole sequence for its H/N heads.  The
+  // N head-group tensors [B, S, H/N, d] lie back to back, which is one
+  // problem of batch N * B with H/N heads: a single launch covers every rank
+  // (lse comes out as [N, B, H/N, S]).
+  if (e == cudaSuccess) {
     AttnArgs a{};
-    a.q = qh + g * head_block;
-    a.k = kh + g * head_block;
-    a.v = vh + g * head_block;
-    a.B = B; a.S = S; a.H = Hg; a.d = d; a.n_shards = 1;
+    a.q = qh;
+    a.k = kh;
+    a.v = vh;
+    a.B = N * B; a.S = S; a.H = Hg; a.d = d; a.n_shards = 1;
     a.q_shard = -1; a.k_shard = -1;
     a.causal = causal;
     a.doc_offsets = doc_offsets;
     a.doc_info = info;
-    a.out = oh + g * head_block;
-    a.lse = lh + static_cast<int64_t>(g) * B * Hg * S;
+    a.out = oh;
+    a.lse = lh;
     chk(launch_attn_bf16(a, stream));
   }
   // step 3: head-split -> sequence-split (all-to-all of the output)
