@@ -36,13 +36,17 @@ cp_status run_attn(AttnArgs a, int kind, cudaStream_t stream) {
   if (st != CP_OK) return st;
   int32_t* info = nullptr;
   if (a.doc_offsets) {
-    if (cudaMallocAsync(reinterpret_cast<void**>(&info), 16, stream) != cudaSuccess)
+    // the doc-scan word, then (tensor-core paths) the cost-ranked slot order
+    const size_t perm_bytes =
+        kind == 0 ? 0 : 4 * static_cast<size_t>(cpring::slot_count(a.S, a.n_shards, a.q_shard));
+    if (cudaMallocAsync(reinterpret_cast<void**>(&info), 16 + perm_bytes, stream) != cudaSuccess)
       return CP_ERR_CUDA;
     if (cpring::launch_doc_scan(a.doc_offsets, a.S, info, stream) != cudaSuccess) {
       cudaFreeAsync(info, stream);
       return CP_ERR_CUDA;
     }
     a.doc_info = info;
+    if (perm_bytes) a.slot_perm = info + 4;
   }
   const cudaError_t e = kind == 2   ? cpring::launch_attn_fp8(a, stream)
                         : kind == 1 ? cpring::launch_attn_bf16(a, stream)

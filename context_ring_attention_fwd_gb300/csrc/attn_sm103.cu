@@ -163,6 +163,7 @@ struct KParams {
   int fault_drop_k;  // test hook: CTA 0 never loads its first K tile
   int kv_row0;       // key index of row 0 of the K/V tensors (0 unless a block)
   int head_group;    // (b, h) heads whose items are dealt out together
+  const int32_t* slot_perm;  // or null: slots heaviest first by measured cost
   const float* q_descale;  // FP8 form: [B * H] each
   const float* k_descale;
   const float* v_descale;
@@ -192,7 +193,7 @@ __device__ __forceinline__ void decode_item(const KParams& p, int n_docs, int w,
   const int gi = w / (HG * slots);                  // head group
   const int r = w - gi * HG * slots;
   const int hg = min(HG, BH - gi * HG);             // heads in this group
-  const int g = slots - 1 - r / hg;
+  const int g = p.slot_perm ? __ldg(p.slot_perm + r / hg) : slots - 1 - r / hg;
   const int bh = gi * HG + r % hg;
   it.b = bh / p.H;
   it.h = bh - it.b * p.H;
@@ -936,6 +937,47 @@ bool make_map_vt8(CUtensorMap* m, const void* base, int B, int S, int H, int D) 
 std::atomic<int> g_fault_drop_k{0};
 std::atomic<unsigned long long> g_wait_limit_ns{kTimeoutNs};
 
+// With documents the work of a slot (query shard, pair of query tiles) is
+// its number of visible key tiles, which depends on the layout, not on the
+// position: rank the slots by that cost, heaviest first (ties: later slot
+// first, the order used without documents), so the snake deal balances the
+// CTAs.  Every (b, h) shares the layout, so one block ranks the slots of
+// (b, h) = (0, 0); O(slots^2) compares, used up to kMaxRankedSlots.
+constexpr int kMaxRankedSlots = 8192;
+
+__global__ void __launch_bounds__(1024) slot_order_kernel(KParams p, int32_t* __restrict__ perm) {
+  __shared__ int cost[kMaxRankedSlots];
+  const int slots = p.n_qshards * p.pairs_per_shard;
+  int n_docs = 1;
+  if (p.doc_offsets != nullptr) {
+    n_docs = __ldg(p.doc_info);
+    if (n_docs <= 0) return;
+  }
+  p.B = 1;
+  p.H = 1;
+  p.head_group = 1;
+  p.slot_perm = nullptr;
+  for (int s = threadIdx.x; s < slots; s += blockDim.x) {
+    Item it;
+    decode_item(p, n_docs, slots - 1 - s, it);   // item w = slots - 1 - s is slot s
+    int c = 0;
+#pragma unroll
+    for (int t = 0; t < kQTiles; ++t)
+      if (it.f_lo[t] <= it.f_hi[t]) c += it.f_hi[t] - it.f_lo[t] + 1;
+    cost[s] = c;
+  }
+  __syncthreads();
+  for (int s = threadIdx.x; s < slots; s += blockDim.x) {
+    const int cs = cost[s];
+    int rank = 0;
+    for (int u = 0; u < slots; ++u) {
+      const int cu = cost[u];
+      rank += (cu > cs) || (cu == cs && u > s);
+    }
+    perm[rank] = s;
+  }
+}
+
 template <int D, bool kPartial, bool kFp8 = false>
 cudaError_t launch_t(const AttnArgs& a, cudaStream_t stream) {
   using Lay = Layout<D, kFp8 ? 1 : 2>;
@@ -1013,6 +1055,13 @@ cudaError_t launch_t(const AttnArgs& a, cudaStream_t stream) {
       hg = std::max<long long>(1, std::min<long long>(hg, BH));
     }
     p.head_group = static_cast<int>(hg);
+  }
+  p.slot_perm = nullptr;
+  if (a.doc_offsets != nullptr && a.slot_perm != nullptr &&
+      p.n_qshards * p.pairs_per_shard <= kMaxRankedSlots) {
+    slot_order_kernel<<<1, 1024, 0, stream>>>(p, a.slot_perm);
+    count_launch(2);
+    p.slot_perm = a.slot_perm;
   }
   if (grid <= 0) return cudaSuccess;
   kern<<<grid, kThreads, Lay::kAlloc, stream>>>(mq, mk, mv, p);

@@ -36,7 +36,17 @@ struct AttnArgs {
   const float* q_descale;
   const float* k_descale;
   const float* v_descale;
+  // With doc_offsets: device scratch of slot_count() int32 for the
+  // cost-ranked work order, or null to deal by position.
+  int32_t* slot_perm;
 };
+
+// Work slots (query shard, pair of 128-row query tiles) of one (b, h) of a
+// tensor-core forward launch: n_qshards * ceil((S / n_shards) / 256).
+inline int slot_count(int S, int n_shards, int q_shard) {
+  const int L = S / n_shards;
+  return (q_shard < 0 ? n_shards : 1) * ((L + 255) / 256);
+}
 
 // The backward: gradients of sum(out * dout) for the forward's out and lse.
 struct BwdArgs {

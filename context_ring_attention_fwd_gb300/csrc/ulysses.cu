@@ -137,7 +137,9 @@ extern "C" cp_status cp_ulysses_attn_fwd(const void* q, const void* k, const voi
   chk(permute(k, kh, rows, N, chunk, true, stream));
   chk(permute(v, vh, rows, N, chunk, true, stream));
   if (doc_offsets) {
-    if (cudaMallocAsync(reinterpret_cast<void**>(&info), 16, stream) != cudaSuccess)
+    // the doc-scan word, then the cost-ranked slot order of the attention launch
+    const size_t perm_bytes = 4 * static_cast<size_t>(slot_count(S, 1, -1));
+    if (cudaMallocAsync(reinterpret_cast<void**>(&info), 16 + perm_bytes, stream) != cudaSuccess)
       return CP_ERR_CUDA;
     chk(launch_doc_scan(doc_offsets, S, info, stream));
   }
@@ -155,6 +157,7 @@ extern "C" cp_status cp_ulysses_attn_fwd(const void* q, const void* k, const voi
     a.causal = causal;
     a.doc_offsets = doc_offsets;
     a.doc_info = info;
+    a.slot_perm = info ? info + 4 : nullptr;
     a.out = oh;
     a.lse = lh;
     chk(launch_attn_bf16(a, stream));
