@@ -271,10 +271,35 @@ __device__ __forceinline__ float row_max(const uint32_t (&sv)[4][32]) {
   return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
 }
 
+// Two exponent arguments s * sc - base at once (paired fp32 FMA).
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float sc,
+                                     float nb) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\tmov.b64 rc, {%5, %5};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(sc), "f"(nb));
+}
+// acc (two fp32 lanes) += (p0, p1) with one paired add.
+__device__ __forceinline__ void add2(uint64_t& acc, float p0, float p1) {
+  asm("{\n\t.reg .b64 rp;\n\tmov.b64 rp, {%1, %2};\n\tadd.rn.f32x2 %0, %0, rp;\n\t}"
+      : "+l"(acc)
+      : "f"(p0), "f"(p1));
+}
+__device__ __forceinline__ float sum2(uint64_t acc) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(acc));
+  return lo + hi;
+}
+
 // P = 2^(s * sc - base), its row sum, and the raw row max of the scores.  P is
 // packed as bf16 pairs (P[2c] low, P[2c+1] high) into pk[0..1][32], or for
 // the FP8 form as E4M3 quads (P[4c] lowest byte) into pk[0][32].
-template <bool kFp8 = false>
+// kPaired (the step kernel, where every tile takes this path): paired fp32
+// FMA / ADD.  The fused kernel reaches it only on the first tile of a row or
+// a rare redo and keeps scalar arithmetic there, which measured faster for
+// its hot loop.
+template <bool kFp8 = false, bool kPaired = false>
 __device__ __forceinline__ void exponentials(const uint32_t (&sv)[4][32], float sc, float base,
                                              uint32_t (&pk)[2][32], float& lsum, float& mx) {
   float ls[4] = {0.f, 0.f, 0.f, 0.f};
@@ -296,6 +321,24 @@ __device__ __forceinline__ void exponentials(const uint32_t (&sv)[4][32], float 
         ls[ch] += (p0 + p1) + (p2 + p3);
         pk[0][ch * 8 + x] = ptx::pack_e4m3x4(p0, p1, p2, p3);
       }
+  } else if (kPaired) {
+    // paired fp32 FMA / ADD, two scores per instruction
+    uint64_t acc = 0;
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+      for (int x = 0; x < 16; ++x) {
+        const float s0 = __uint_as_float(sv[ch][2 * x]);
+        const float s1 = __uint_as_float(sv[ch][2 * x + 1]);
+        m[ch] = max3(m[ch], s0, s1);
+        float e0, e1;
+        fma2(e0, e1, s0, s1, sc, -base);
+        const float p0 = ptx::ex2(e0);
+        const float p1 = ptx::ex2(e1);
+        add2(acc, p0, p1);
+        pk[ch >> 1][(ch & 1) * 16 + x] = ptx::pack_bf16(p0, p1);
+      }
+    ls[0] = sum2(acc);
   } else {
 #pragma unroll
     for (int ch = 0; ch < 4; ++ch)
@@ -312,27 +355,6 @@ __device__ __forceinline__ void exponentials(const uint32_t (&sv)[4][32], float 
   }
   lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
   mx = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
-}
-
-// Two exponent arguments s * sc - base at once (paired fp32 FMA).
-__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float sc,
-                                     float nb) {
-  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\tmov.b64 rc, {%5, %5};\n\t"
-      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(sc), "f"(nb));
-}
-// acc (two fp32 lanes) += (p0, p1) with one paired add.
-__device__ __forceinline__ void add2(uint64_t& acc, float p0, float p1) {
-  asm("{\n\t.reg .b64 rp;\n\tmov.b64 rp, {%1, %2};\n\tadd.rn.f32x2 %0, %0, rp;\n\t}"
-      : "+l"(acc)
-      : "f"(p0), "f"(p1));
-}
-__device__ __forceinline__ float sum2(uint64_t acc) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(acc));
-  return lo + hi;
 }
 
 // P for two 32-column chunks of S against `base`, into pk row `half`.
@@ -766,7 +788,7 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
               l_run *= alpha;
               m_used = m_tile;
             }
-            exponentials<kFp8>(sv, sc, m_used, pk, lsum, mx);
+            exponentials<kFp8, kPartial>(sv, sc, m_used, pk, lsum, mx);
           }
         } else {
         load_scores(tS, c_lo, c_hi, sv);
@@ -781,13 +803,13 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
             l_run *= alpha;
             m_used = m_tile;
           }
-          exponentials<kFp8>(sv, sc, (m_used == -INFINITY) ? 0.f : m_used, pk, lsum, mx);
+          exponentials<kFp8, kPartial>(sv, sc, (m_used == -INFINITY) ? 0.f : m_used, pk, lsum, mx);
         } else {
           // Exponentials against the current reference; the row max is
           // taken in the same pass and only forces a redo (rare) when it
           // moved more than 2^8 above the reference.
           {
-            exponentials<kFp8>(sv, sc, m_used, pk, lsum, mx);
+            exponentials<kFp8, kPartial>(sv, sc, m_used, pk, lsum, mx);
             const float m_tile = mx * sc;
             m_true = fmaxf(m_true, m_tile);
             const bool redo = m_tile > m_used + kRescaleLog2;
@@ -799,7 +821,7 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
                 m_used = m_tile;
               }
               load_scores(tS, c_lo, c_hi, sv);  // S is still in TMEM: P not yet written
-              exponentials<kFp8>(sv, sc, m_used, pk, lsum, mx);
+              exponentials<kFp8, kPartial>(sv, sc, m_used, pk, lsum, mx);
             }
           }
         }
