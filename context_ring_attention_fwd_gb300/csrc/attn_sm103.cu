@@ -18,7 +18,8 @@
 //   warp  8    TMA producer: Q tiles once per work item, then K/V tiles of
 //              each visited shard into a 2-stage shared-memory ring
 //              (the ring's send/receive becomes this double-buffered walk)
-//   warp  9    a single thread issues every tcgen05.mma
+//   warp  9    issues every tcgen05.mma (the whole warp runs the loop; one
+//              lane, picked by elect.sync, issues each instruction)
 //   warps 10-11 idle (they complete the third warpgroup, which gives its
 //              registers to the softmax warpgroups through setmaxnreg)
 // TMEM (512 columns): S_0 | S_1 | O_0 | O_1.  S_t = Q_t K^T lands in TMEM
@@ -585,7 +586,10 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
     }
    } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop with warp-uniform values; each MMA and
+    // commit is issued by one lane that elect.sync picks (the warp-collective
+    // forms in ptx.cuh), and every wait is the warp-uniform one.
+    {
       constexpr uint32_t kIdescQK =
           kFp8 ? ptx::idesc_e4m3_f32(kBM, kBN) : ptx::idesc_bf16_f32(kBM, kBN, false);
       constexpr uint32_t kIdescPV =
@@ -596,7 +600,7 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
       bool ok = true;
       // Shared-memory descriptors of every operand tile, built once.  A k-step
       // moves the start address (bits 0-13, in 16-byte units) by a constant,
-      // so each MMA needs one add: this thread issues 32 MMAs per K/V tile
+      // so each MMA needs one add: this warp issues 32 MMAs per K/V tile
       // while sharing its scheduler with two softmax warps.
       // (Shared addresses stay below 2^18 bytes, so the 14-bit start field
       // never carries into the offsets above it.)
@@ -609,19 +613,19 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
           const uint64_t dv = d_qk + ((Lay::kVOff + st * Lay::kTileBytes) >> 4);
 #pragma unroll
           for (int s = 0; s < kBN / kKStep; ++s)
-            ptx::mma_ts_f8(tmem_base + 256 + t * D, tmem_base + t * 128 + s * 8,
+            ptx::mma_ts_f8_w(tmem_base + 256 + t * D, tmem_base + t * 128 + s * 8,
                            dv + static_cast<uint64_t>((s * 32) >> 4), kIdescPV,
                            (first && s == 0) ? 0u : 1u);
         } else {
           const uint64_t dv = d_v + ((Lay::kVOff + st * Lay::kTileBytes) >> 4);
 #pragma unroll
           for (int s = 0; s < kBN / 16; ++s) {
-            ptx::mma_ts(tmem_base + 256 + t * D, tmem_base + t * 128 + s * 8,
+            ptx::mma_ts_w(tmem_base + 256 + t * D, tmem_base + t * 128 + s * 8,
                         dv + static_cast<uint64_t>((s * 16 * 128) >> 4), kIdescPV,
                         (first && s == 0) ? 0u : 1u);
           }
         }
-        ptx::mma_commit(bar(kOBar + t));
+        ptx::mma_commit_w(bar(kOBar + t));
       };
       // S_t = Q_t K^T (both K-major, 128-byte swizzled panels; a K step is
       // 32 bytes, four steps per panel).
@@ -632,11 +636,11 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
         for (int s = 0; s < D / kKStep; ++s) {
           const uint64_t step = static_cast<uint64_t>(((s >> 2) * Lay::kPanelBytes + (s & 3) * 32) >> 4);
           if constexpr (kFp8)
-            ptx::mma_ss_f8(tmem_base + t * 128, dq + step, dk + step, kIdescQK, s > 0 ? 1u : 0u);
+            ptx::mma_ss_f8_w(tmem_base + t * 128, dq + step, dk + step, kIdescQK, s > 0 ? 1u : 0u);
           else
-            ptx::mma_ss(tmem_base + t * 128, dq + step, dk + step, kIdescQK, s > 0 ? 1u : 0u);
+            ptx::mma_ss_w(tmem_base + t * 128, dq + step, dk + step, kIdescQK, s > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(bar(kSFull + t));
+        ptx::mma_commit_w(bar(kSFull + t));
       };
       for (int k = 0; ok; ++k) {
         const int w = item_of(k, c, G);
@@ -644,7 +648,7 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
         Item it;
         decode_item(p, n_docs, w, it);
         if (it.F_lo > it.F_hi) continue;
-        if (!wait1(bar(kQFull), q_iter & 1u, abort_flag, p)) { ok = false; break; }
+        if (!wait_warp(bar(kQFull), q_iter & 1u, abort_flag, p)) { ok = false; break; }
         ++q_iter;
         ptx::tc_fence_after();
         bool pend0 = false, pend1 = false;    // an S issued whose PV is still owed
@@ -654,10 +658,10 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
         // Owed PV of tile t on the previous K/V stage: wait for V and P, issue.
         auto flush = [&](int t, uint32_t& pc, bool& first) -> bool {
           if (!prev_v_ready) {
-            if (!wait1(bar(kVFull + prev_st), prev_ph, abort_flag, p)) return false;
+            if (!wait_warp(bar(kVFull + prev_st), prev_ph, abort_flag, p)) return false;
             prev_v_ready = true;
           }
-          if (!wait1(bar(kPReady + t), pc & 1u, abort_flag, p)) return false;
+          if (!wait_warp(bar(kPReady + t), pc & 1u, abort_flag, p)) return false;
           ++pc;
           ptx::tc_fence_after();
           issue_pv(t, prev_st, first);
@@ -671,7 +675,7 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
             if (!flush(0, p_cnt0, first0)) { ok = false; break; }
             pend0 = false;
           }
-          if (!wait1(bar(kKFull + st), ph, abort_flag, p)) { ok = false; break; }
+          if (!wait_warp(bar(kKFull + st), ph, abort_flag, p)) { ok = false; break; }
           ptx::tc_fence_after();
           if (f >= it.f_lo[0] && f <= it.f_hi[0]) {
             issue_s(0, st);
@@ -685,8 +689,8 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
             issue_s(1, st);
             pend1 = true;
           }
-          ptx::mma_commit(bar(kKEmpty + st));                      // K(f) read by every S
-          if (have_prev) ptx::mma_commit(bar(kVEmpty + prev_st));  // V(f-1) read by every PV
+          ptx::mma_commit_w(bar(kKEmpty + st));                      // K(f) read by every S
+          if (have_prev) ptx::mma_commit_w(bar(kVEmpty + prev_st));  // V(f-1) read by every PV
           prev_st = st;
           prev_ph = ph;
           have_prev = true;
@@ -694,18 +698,18 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
           ++kv_iter;
         }
         if (!ok) break;
-        ptx::mma_commit(bar(kQEmpty));  // every S of this item has been issued
+        ptx::mma_commit_w(bar(kQEmpty));  // every S of this item has been issued
         if (pend0) {
           if (!flush(0, p_cnt0, first0)) { ok = false; break; }
         }
         if (pend1) {
           if (!flush(1, p_cnt1, first1)) { ok = false; break; }
         }
-        if (have_prev) ptx::mma_commit(bar(kVEmpty + prev_st));
+        if (have_prev) ptx::mma_commit_w(bar(kVEmpty + prev_st));
       }
       // Wait until every MMA this thread issued has finished.
-      ptx::mma_commit(bar(kDrain));
-      wait1(bar(kDrain), 0u, abort_flag, p, false);
+      ptx::mma_commit_w(bar(kDrain));
+      wait_warp(bar(kDrain), 0u, abort_flag, p, false);
     }
    }
   } else {
