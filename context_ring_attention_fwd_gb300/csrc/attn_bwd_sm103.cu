@@ -27,9 +27,10 @@
 // CTA (384 threads): warps 0-3 and 4-7 split the 128 columns of each S / dP
 // tile (64 each) over the same 128 rows, one thread per TMEM lane; warp 8
 // is the TMA producer (the two fixed tiles once per item, the streamed tiles
-// of every step into their slot rings); one thread of warp 9 issues every
-// tcgen05.mma; warps 10-11 only complete the third warpgroup, which hands
-// its registers to the softmax warpgroups through setmaxnreg.
+// of every step into their slot rings); warp 9 issues every tcgen05.mma
+// (one lane, picked by elect.sync, per instruction); warps 10-11 only
+// complete the third warpgroup, which hands its registers to the softmax
+// warpgroups through setmaxnreg.
 // TMEM (512 columns).  kDQ: S | dP | dQ | two buffers of packed dS.  kDKDV
 // runs each 128-query tile as two 64-query halves in two buffers
 // (S^T 64 | dP^T 64) x 2 | dV | dK, so the products of the next half overlap
@@ -291,7 +292,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop with warp-uniform values; one lane picked
+    // by elect.sync issues each MMA and commit (the warp-collective forms in
+    // ptx.cuh), and every wait is the warp-uniform one.
+    {
       constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kT, kT, false);   // N = streamed rows
       constexpr uint32_t kIdescG = ptx::idesc_bf16_f32(kT, D, true);     // N = d, B MN-major
       const uint64_t d_k = ptx::smem_desc_sw128(sbase, 16, 1024);                // K-major
@@ -306,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < D / 16; ++s) {
           const uint64_t step =
               static_cast<uint64_t>(((s >> 2) * Lay::kPanelBytes + (s & 3) * 32) >> 4);
-          ptx::mma_ss(d_tmem, d_k + (a_off >> 4) + step, d_k + (b_off >> 4) + step, kIdescS,
+          ptx::mma_ss_w(d_tmem, d_k + (a_off >> 4) + step, d_k + (b_off >> 4) + step, kIdescS,
                       s > 0 ? 1u : 0u);
         }
       };
@@ -317,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int s = 0; s < kT / 16; ++s) {
           const uint32_t a_col = static_cast<uint32_t>((s >> 2) * half + (s & 3) * 8);
-          ptx::mma_ts(acc, a_tmem + a_col, d_mn + (b_off >> 4) + static_cast<uint64_t>(s * 128),
+          ptx::mma_ts_w(acc, a_tmem + a_col, d_mn + (b_off >> 4) + static_cast<uint64_t>(s * 128),
                       kIdescG, (first && s == 0) ? 0u : 1u);
         }
       };
@@ -330,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < D / 16; ++s) {
           const uint64_t step =
               static_cast<uint64_t>(((s >> 2) * Lay::kPanelBytes + (s & 3) * 32) >> 4);
-          ptx::mma_ss(d_tmem, d_k + (a_off >> 4) + step, d_k + (b_off >> 4) + step, kIdescS64,
+          ptx::mma_ss_w(d_tmem, d_k + (a_off >> 4) + step, d_k + (b_off >> 4) + step, kIdescS64,
                       s > 0 ? 1u : 0u);
         }
       };
@@ -340,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int s = 0; s < 64 / 16; ++s) {
           const uint32_t a_col = static_cast<uint32_t>((s >> 1) * 32 + (s & 1) * 8);
-          ptx::mma_ts(acc, a_tmem + a_col, d_mn + (b_off >> 4) + static_cast<uint64_t>(s * 128),
+          ptx::mma_ts_w(acc, a_tmem + a_col, d_mn + (b_off >> 4) + static_cast<uint64_t>(s * 128),
                       kIdescG, (first && s == 0) ? 0u : 1u);
         }
       };
@@ -349,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (w >= p.n_items) break;
         BItem it;
         decode_bitem<kDKDV>(p, n_docs, w, it);
-        if (!wait1(bar(kFixFull), fix_iter & 1u, abort_flag, p)) { ok = false; break; }
+        if (!wait_warp(bar(kFixFull), fix_iter & 1u, abort_flag, p)) { ok = false; break; }
         ++fix_iter;
         ptx::tc_fence_after();
         if constexpr (!kDKDV) {
@@ -360,37 +364,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           // x % 2; V's slot is free once dP is done.
           auto issue_step = [&](uint32_t x) -> bool {
             const uint32_t s0 = x % Lay::kX0Slots, s1 = x % Lay::kX1Slots;
-            if (!wait1(bar(kX0Full + s0), (x / Lay::kX0Slots) & 1u, abort_flag, p)) return false;
-            if (!wait1(bar(kX1Full + s1), (x / Lay::kX1Slots) & 1u, abort_flag, p)) return false;
+            if (!wait_warp(bar(kX0Full + s0), (x / Lay::kX0Slots) & 1u, abort_flag, p)) return false;
+            if (!wait_warp(bar(kX1Full + s1), (x / Lay::kX1Slots) & 1u, abort_flag, p)) return false;
             ptx::tc_fence_after();
             issue_ss(tS, Lay::kF0, Lay::x0(s0));
             issue_ss(tdP, Lay::kF1, Lay::x1(s1));
-            ptx::mma_commit(bar(kSFull));
-            ptx::mma_commit(bar(kX1Empty + s1));
+            ptx::mma_commit_w(bar(kSFull));
+            ptx::mma_commit_w(bar(kX1Empty + s1));
             return true;
           };
           for (int f = it.x_lo; f <= it.x_hi; ++f) {
             if (!have) {
-              if (n > 0 && !wait1(bar(kSConsumed), (n - 1u) & 1u, abort_flag, p)) { ok = false; break; }
+              if (n > 0 && !wait_warp(bar(kSConsumed), (n - 1u) & 1u, abort_flag, p)) { ok = false; break; }
               if (!issue_step(x_iter)) { ok = false; break; }
             }
             have = false;
             if (f < it.x_hi) {
-              if (!wait1(bar(kSConsumed), n & 1u, abort_flag, p)) { ok = false; break; }
+              if (!wait_warp(bar(kSConsumed), n & 1u, abort_flag, p)) { ok = false; break; }
               if (!issue_step(x_iter + 1)) { ok = false; break; }
               have = true;
             }
-            if (!wait1(bar(kPReady + (n & 1u)), (n >> 1) & 1u, abort_flag, p)) { ok = false; break; }
+            if (!wait_warp(bar(kPReady + (n & 1u)), (n >> 1) & 1u, abort_flag, p)) { ok = false; break; }
             ptx::tc_fence_after();
             const uint32_t s0 = x_iter % Lay::kX0Slots;
             issue_ts(tA0, tmem_base + kDsBuf + (n & 1u) * 64u, Lay::x0(s0), f == it.x_lo, 32);
-            ptx::mma_commit(bar(kX0Empty + s0));
+            ptx::mma_commit_w(bar(kX0Empty + s0));
             ++n;
             ++x_iter;
           }
           if (!ok) break;
-          ptx::mma_commit(bar(kFixEmpty));
-          ptx::mma_commit(bar(kAccFull));
+          ptx::mma_commit_w(bar(kFixEmpty));
+          ptx::mma_commit_w(bar(kAccFull));
           continue;
         }
         // kDKDV: half hh of the item is query rows 64 (hh % 2) .. of its
@@ -401,41 +405,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto issue_half = [&](uint32_t mm, int hh2) -> bool {
           const uint32_t xi = x_iter + static_cast<uint32_t>(hh2 >> 1);
           const uint32_t st = xi % Lay::kX0Slots, ph = (xi / Lay::kX0Slots) & 1u;
-          if (!wait1(bar(kX0Full + st), ph, abort_flag, p)) return false;
-          if (!wait1(bar(kX1Full + st), ph, abort_flag, p)) return false;
+          if (!wait_warp(bar(kX0Full + st), ph, abort_flag, p)) return false;
+          if (!wait_warp(bar(kX1Full + st), ph, abort_flag, p)) return false;
           ptx::tc_fence_after();
           const uint32_t b = mm & 1u;
           const int rows = (hh2 & 1) * 64 * 128;   // byte offset of query row 64 in a panel
           issue_ss64(tmem_base + 128u * b, Lay::kF0, Lay::x0(st) + rows);         // S^T = K Q_h^T
           issue_ss64(tmem_base + 128u * b + 64u, Lay::kF1, Lay::x1(st) + rows);   // dP^T = V dO_h^T
-          ptx::mma_commit(bar(kSFull + b));
+          ptx::mma_commit_w(bar(kSFull + b));
           return true;
         };
         if (!issue_half(m_half, 0)) { ok = false; break; }
         for (int hh = 0; hh < nh; ++hh) {
           const uint32_t b = m_half & 1u;
           if (hh + 1 < nh && !issue_half(m_half + 1, hh + 1)) { ok = false; break; }
-          if (!wait1(bar(kPReady + b), (m_half >> 1) & 1u, abort_flag, p)) { ok = false; break; }
+          if (!wait_warp(bar(kPReady + b), (m_half >> 1) & 1u, abort_flag, p)) { ok = false; break; }
           ptx::tc_fence_after();
           const uint32_t st = (x_iter + static_cast<uint32_t>(hh >> 1)) % Lay::kX0Slots;
           const int rows = (hh & 1) * 64 * 128;
           issue_ts64(tA0, tmem_base + 128u * b, Lay::x1(st) + rows, hh == 0);        // dV += P^T dO_h
           issue_ts64(tA1, tmem_base + 128u * b + 64u, Lay::x0(st) + rows, hh == 0);  // dK += dS^T Q_h
           if (hh & 1) {
-            ptx::mma_commit(bar(kX0Empty + st));
-            ptx::mma_commit(bar(kX1Empty + st));
+            ptx::mma_commit_w(bar(kX0Empty + st));
+            ptx::mma_commit_w(bar(kX1Empty + st));
           }
           ++m_half;
         }
         if (!ok) break;
         x_iter += static_cast<uint32_t>(nh >> 1);
         if (!ok) break;
-        ptx::mma_commit(bar(kFixEmpty));
-        ptx::mma_commit(bar(kAccFull));
+        ptx::mma_commit_w(bar(kFixEmpty));
+        ptx::mma_commit_w(bar(kAccFull));
       }
-      // Wait until every MMA this thread issued has finished.
-      ptx::mma_commit(bar(kDrain));
-      wait1(bar(kDrain), 0u, abort_flag, p, false);
+      // Wait until every MMA this warp issued has finished.
+      ptx::mma_commit_w(bar(kDrain));
+      wait_warp(bar(kDrain), 0u, abort_flag, p, false);
     }
    }
   } else {
