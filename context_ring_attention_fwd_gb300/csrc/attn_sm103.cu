@@ -136,7 +136,7 @@ enum Bar : int {
   kVEmpty = 8,    // + stage: V tile consumed by both PV MMAs
   kSFull = 10,    // + tile
   kPReady = 12,   // + tile
-  kOBar = 14,     // + tile
+  kOBar = 14,     // + tile: every PV of tile t in the item done (once per item)
   kDrain = 16,
   kNumBars = 17
 };
@@ -625,7 +625,6 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
                         (first && s == 0) ? 0u : 1u);
           }
         }
-        ptx::mma_commit_w(bar(kOBar + t));
       };
       // S_t = Q_t K^T (both K-major, 128-byte swizzled panels; a K step is
       // 32 bytes, four steps per panel).
@@ -656,7 +655,9 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
         uint32_t prev_st = 0, prev_ph = 0;
         bool have_prev = false, prev_v_ready = false;
         // Owed PV of tile t on the previous K/V stage: wait for V and P, issue.
-        auto flush = [&](int t, uint32_t& pc, bool& first) -> bool {
+        // After the item's last PV of tile t, O_t is final: commit kOBar + t
+        // (the epilogue waits on it; nothing else does).
+        auto flush = [&](int t, uint32_t& pc, bool& first, bool last) -> bool {
           if (!prev_v_ready) {
             if (!wait_warp(bar(kVFull + prev_st), prev_ph, abort_flag, p)) return false;
             prev_v_ready = true;
@@ -665,6 +666,7 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
           ++pc;
           ptx::tc_fence_after();
           issue_pv(t, prev_st, first);
+          if (last) ptx::mma_commit_w(bar(kOBar + t));
           first = false;
           return true;
         };
@@ -672,7 +674,7 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
           const uint32_t st = kv_iter % kStages;
           const uint32_t ph = (kv_iter / kStages) & 1u;
           if (pend0) {
-            if (!flush(0, p_cnt0, first0)) { ok = false; break; }
+            if (!flush(0, p_cnt0, first0, f - 1 == it.f_hi[0])) { ok = false; break; }
             pend0 = false;
           }
           if (!wait_warp(bar(kKFull + st), ph, abort_flag, p)) { ok = false; break; }
@@ -682,7 +684,7 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
             pend0 = true;
           }
           if (pend1) {
-            if (!flush(1, p_cnt1, first1)) { ok = false; break; }
+            if (!flush(1, p_cnt1, first1, f - 1 == it.f_hi[1])) { ok = false; break; }
             pend1 = false;
           }
           if (f >= it.f_lo[1] && f <= it.f_hi[1]) {
@@ -700,14 +702,14 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
         if (!ok) break;
         ptx::mma_commit_w(bar(kQEmpty));  // every S of this item has been issued
         if (pend0) {
-          if (!flush(0, p_cnt0, first0)) { ok = false; break; }
+          if (!flush(0, p_cnt0, first0, true)) { ok = false; break; }
         }
         if (pend1) {
-          if (!flush(1, p_cnt1, first1)) { ok = false; break; }
+          if (!flush(1, p_cnt1, first1, true)) { ok = false; break; }
         }
         if (have_prev) ptx::mma_commit_w(bar(kVEmpty + prev_st));
       }
-      // Wait until every MMA this thread issued has finished.
+      // Wait until every MMA this warp issued has finished.
       ptx::mma_commit_w(bar(kDrain));
       wait_warp(bar(kDrain), 0u, abort_flag, p, false);
     }
@@ -722,7 +724,7 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
     const uint32_t tS = tmem_base + lane_off + static_cast<uint32_t>(t * 128);
     const uint32_t tO = tmem_base + lane_off + 256u + static_cast<uint32_t>(t * D);
     float sc = p.scale_log2;
-    uint32_t s_cnt = 0, pv_cnt = 0;
+    uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int w = item_of(k, c, G);
@@ -834,9 +836,9 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
         ptx::tmem_st32(tS, pk[0]);
         if constexpr (!kFp8) ptx::tmem_st32(tS + 32, pk[1]);
         if (__any_sync(0xffffffffu, rescale_o)) {
-          // O_t holds the sum up to the previous tile once that PV is done.
-          if (!wait_warp(bar(kOBar + t), (pv_cnt - 1u) & 1u, abort_flag, p)) { ok = false; break; }
-          ptx::tc_fence_after();
+          // O_t already holds the sum up to the previous tile: the MMA warp
+          // issued that PV before this tile's S, and the commit this warp
+          // waited on for S tracks every MMA issued before it.
 #pragma unroll
           for (int ch = 0; ch < D / 32; ++ch) {
             uint32_t ov[32];
@@ -851,11 +853,11 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(kPReady + t));
-        ++pv_cnt;
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
-      if (!wait_warp(bar(kOBar + t), (pv_cnt - 1u) & 1u, abort_flag, p)) { ok = false; break; }
+      if (!wait_warp(bar(kOBar + t), o_cnt & 1u, abort_flag, p)) { ok = false; break; }
+      ++o_cnt;
       ptx::tc_fence_after();
       if (!kPartial) {
         const float inv_l = (kFp8 ? __ldg(p.v_descale + bh) : 1.f) / l_run;
