@@ -79,16 +79,17 @@ constexpr float kRescaleLog2 = 8.0f;
 //  CPRING_GROUP_MIN_ROUNDS ... when the launch has at least this many rounds;
 //                          shorter launches deal every item from one pool.
 //  CPRING_FUSED_NOMAX      fused forward only: after the first tile, skip the
-//                          row max and redo a tile only if its row sum shows
-//                          exponentials above 2^64 (the reference point never
+//                          row max and redo a tile only if its first 64 keys'
+//                          row sum or its last 64 keys' row max shows an
+//                          exponential above 2^64 (the reference point never
 //                          affects P's relative precision, only its range).
+//                          P then goes out in two halves of 64 keys, each
+//                          signalled as soon as it is stored.
 //  CPRING_PACKED_F32X2     fast pass: scale-and-shift and row sum with the
 //                          paired fp32 FMA / ADD (two elements per instruction).
-//  CPRING_SPLIT_LOAD       fast pass: read the second half of S from TMEM
-//                          while the first half's exponentials run.
 //  CPRING_FP8_FAST         the FP8 kernel uses the same no-max fast pass, with
-//                          the row-sum guard at 2^8 so that every P it keeps
-//                          is at most 2^8, inside E4M3's range (448).
+//                          the guards at 2^8 so that every P it keeps is at
+//                          most 2^8, inside E4M3's range (448).
 #ifndef CPRING_BALANCE
 #define CPRING_BALANCE 2
 #endif
@@ -101,15 +102,13 @@ constexpr float kRescaleLog2 = 8.0f;
 #ifndef CPRING_PACKED_F32X2
 #define CPRING_PACKED_F32X2 1
 #endif
-#ifndef CPRING_SPLIT_LOAD
-#define CPRING_SPLIT_LOAD 0
-#endif
 #ifndef CPRING_FP8_FAST
 #define CPRING_FP8_FAST 1
 #endif
 constexpr int kPReadyCount = 128;
 constexpr float kOverflowGuard = 18446744073709551616.0f;  // 2^64
 constexpr float kOverflowGuardFp8 = 256.0f;                  // 2^8: P <= 2^8 < 448
+constexpr float kOverflowGuardLog2 = 64.0f;                  // 2^64 as an exponent
 constexpr unsigned long long kTimeoutNs = 4000000000ull;  // per wait
 
 template <int D, int E>  // E = bytes per element (2 bf16, 1 E4M3)
@@ -135,10 +134,11 @@ enum Bar : int {
   kKEmpty = 6,    // + stage: K tile consumed by both S MMAs
   kVEmpty = 8,    // + stage: V tile consumed by both PV MMAs
   kSFull = 10,    // + tile
-  kPReady = 12,   // + tile
-  kOBar = 14,     // + tile: every PV of tile t in the item done (once per item)
-  kDrain = 16,
-  kNumBars = 17
+  kPReady = 12,   // + tile: the first 64 keys' P of tile t stored
+  kPReadyB = 14,  // + tile: the last 64 keys' P of tile t stored (and O rescaled)
+  kOBar = 16,     // + tile: every PV of tile t in the item done (once per item)
+  kDrain = 18,
+  kNumBars = 19
 };
 constexpr int kTmemSlot = kNumBars * 8;       // u32: TMEM base address
 constexpr int kAbortSlot = kNumBars * 8 + 4;  // u32: CTA abort flag
@@ -407,55 +407,42 @@ __device__ __forceinline__ void exp_chunks_f8(const uint32_t (&sv)[4][32], int h
   }
 }
 
-// Masks columns outside [c_lo, c_hi] of chunks 2*half, 2*half+1.
-__device__ __forceinline__ void mask_chunks(uint32_t (&sv)[4][32], int half, int c_lo, int c_hi) {
+// Raw max of the scores of chunks 2*half, 2*half+1 (64 keys).
+__device__ __forceinline__ float half_max(const uint32_t (&sv)[4][32], int half) {
+  float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
-  for (int cc = 0; cc < 2; ++cc)
-#pragma unroll
-    for (int x = 0; x < 32; ++x) {
-      const int col = (2 * half + cc) * 32 + x;
-      if (col < c_lo || col > c_hi) sv[2 * half + cc][x] = __float_as_uint(-INFINITY);
-    }
+  for (int x = 0; x < 32; x += 2) {
+    m0 = max3(m0, __uint_as_float(sv[2 * half][x]), __uint_as_float(sv[2 * half][x + 1]));
+    m1 = max3(m1, __uint_as_float(sv[2 * half + 1][x]), __uint_as_float(sv[2 * half + 1][x + 1]));
+  }
+  return fmaxf(m0, m1);
 }
 
-// The common case of the fused kernel: load this lane's S row (in two
-// halves, the second in flight while the first is exponentiated), mask it,
-// and form P and its row sum against the current reference.  No row max.
-template <bool kFp8 = false>
-__device__ __forceinline__ void fast_pass(uint32_t tS, int c_lo, int c_hi, float sc, float base,
-                                          uint32_t (&sv)[4][32], uint32_t (&pk)[2][32],
-                                          float& lsum) {
-  const bool need_mask = (c_lo > 0 || c_hi < kBN - 1);
+// P of 64 keys (half 0: keys 0-63, half 1: keys 64-127) against `base` into
+// pk, and its row sum.
+template <bool kFp8>
+__device__ __forceinline__ float exp_half(const uint32_t (&sv)[4][32], int half, float sc,
+                                          float base, uint32_t (&pk)[2][32]) {
   uint64_t acc = 0;  // two fp32 zeros
   float ls = 0.f;
   if constexpr (kFp8) {
-    load_scores(tS, c_lo, c_hi, sv);
-    exp_chunks_f8(sv, 0, sc, base, pk, acc);
-    exp_chunks_f8(sv, 1, sc, base, pk, acc);
-    lsum = sum2(acc);
-    return;
-  }
-  if (CPRING_SPLIT_LOAD) {
-    ptx::tmem_ld32(tS, sv[0]);
-    ptx::tmem_ld32(tS + 32, sv[1]);
-    ptx::tmem_wait_ld();
-    ptx::reg_fence(sv[0]);
-    ptx::reg_fence(sv[1]);
-    ptx::tmem_ld32(tS + 64, sv[2]);
-    ptx::tmem_ld32(tS + 96, sv[3]);
-    if (need_mask) mask_chunks(sv, 0, c_lo, c_hi);
-    exp_chunks(sv, 0, sc, base, pk, acc, ls);
-    ptx::tmem_wait_ld();
-    ptx::reg_fence(sv[2]);
-    ptx::reg_fence(sv[3]);
-    if (need_mask) mask_chunks(sv, 1, c_lo, c_hi);
-    exp_chunks(sv, 1, sc, base, pk, acc, ls);
+    exp_chunks_f8(sv, half, sc, base, pk, acc);
+    return sum2(acc);
   } else {
-    load_scores(tS, c_lo, c_hi, sv);
-    exp_chunks(sv, 0, sc, base, pk, acc, ls);
-    exp_chunks(sv, 1, sc, base, pk, acc, ls);
+    exp_chunks(sv, half, sc, base, pk, acc, ls);
+    return CPRING_PACKED_F32X2 ? sum2(acc) : ls;
   }
-  lsum = CPRING_PACKED_F32X2 ? sum2(acc) : ls;
+}
+
+// Stores the P of one half of the keys over this lane's S row: bf16 pairs in
+// columns 32*half .. +32, or E4M3 quads in columns 16*half .. +16.
+template <bool kFp8>
+__device__ __forceinline__ void store_p_half(uint32_t tS, const uint32_t (&pk)[2][32], int half) {
+  if constexpr (kFp8) {
+    ptx::tmem_st16(tS + 16u * half, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0][16 * half]));
+  } else {
+    ptx::tmem_st32(tS + 32u * half, pk[half]);
+  }
 }
 
 // ---------------------------------------------------------------- kernel
@@ -496,6 +483,7 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
     for (int t = 0; t < kQTiles; ++t) {
       ptx::mbar_init(bar(kSFull + t), 1);
       ptx::mbar_init(bar(kPReady + t), kPReadyCount);
+      ptx::mbar_init(bar(kPReadyB + t), kPReadyCount);
       ptx::mbar_init(bar(kOBar + t), 1);
     }
     ptx::mbar_init(bar(kDrain), 1);
@@ -608,18 +596,21 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
       const uint64_t d_v = ptx::smem_desc_sw128(sbase, Lay::kPanelBytes, 1024);
       // O_t (+)= P_t V: P_t from TMEM (8 columns per K step in both forms),
       // V MN-major (bf16) or V^T K-major (FP8) from the given stage.
-      auto issue_pv = [&](int t, uint32_t st, bool first) {
+      // Half `part` of the K steps: keys 0-63 (part 0) or 64-127 (part 1),
+      // whose P the softmax signals separately.
+      auto issue_pv = [&](int t, uint32_t st, bool first, int part) {
+        constexpr int kHalfSteps = kBN / kKStep / 2;
         if constexpr (kFp8) {
           const uint64_t dv = d_qk + ((Lay::kVOff + st * Lay::kTileBytes) >> 4);
 #pragma unroll
-          for (int s = 0; s < kBN / kKStep; ++s)
+          for (int s = part * kHalfSteps; s < (part + 1) * kHalfSteps; ++s)
             ptx::mma_ts_f8_w(tmem_base + 256 + t * D, tmem_base + t * 128 + s * 8,
                            dv + static_cast<uint64_t>((s * 32) >> 4), kIdescPV,
                            (first && s == 0) ? 0u : 1u);
         } else {
           const uint64_t dv = d_v + ((Lay::kVOff + st * Lay::kTileBytes) >> 4);
 #pragma unroll
-          for (int s = 0; s < kBN / 16; ++s) {
+          for (int s = part * kHalfSteps; s < (part + 1) * kHalfSteps; ++s) {
             ptx::mma_ts_w(tmem_base + 256 + t * D, tmem_base + t * 128 + s * 8,
                         dv + static_cast<uint64_t>((s * 16 * 128) >> 4), kIdescPV,
                         (first && s == 0) ? 0u : 1u);
@@ -663,9 +654,12 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
             prev_v_ready = true;
           }
           if (!wait_warp(bar(kPReady + t), pc & 1u, abort_flag, p)) return false;
+          ptx::tc_fence_after();
+          issue_pv(t, prev_st, first, 0);
+          if (!wait_warp(bar(kPReadyB + t), pc & 1u, abort_flag, p)) return false;
           ++pc;
           ptx::tc_fence_after();
-          issue_pv(t, prev_st, first);
+          issue_pv(t, prev_st, false, 1);
           if (last) ptx::mma_commit_w(bar(kOBar + t));
           first = false;
           return true;
@@ -777,24 +771,73 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
         const bool fast = CPRING_FUSED_NOMAX && !kPartial && (!kFp8 || CPRING_FP8_FAST) &&
                           !__any_sync(0xffffffffu, m_used == -INFINITY);
         if (fast) {
-          fast_pass<kFp8>(tS, c_lo, c_hi, sc, m_used, sv, pk, lsum);
-          const bool redo = !(lsum <= (kFp8 ? kOverflowGuardFp8 : kOverflowGuard));
-          if (__any_sync(0xffffffffu, redo)) {
-            // Rare: the row sum ran past its guard (2^64; 2^8 in the FP8
-            // form, where it keeps every P inside E4M3's range).  A sum above
-            // the guard means this tile's max is above the reference (128
-            // entries of at most 1 sum to 128 or less).  Reload S (P is not
-            // yet written), move the reference to this tile's max and let
-            // every lane recompute (lanes that keep theirs get the same P).
+          if constexpr (kFp8) {
+            // One pass over the 128 keys; a row sum above 2^8 sends the tile
+            // to the redo below, which keeps every P inside E4M3's range
+            // (448).  (Its P V is only four MMAs, too short to gain from the
+            // split that the bf16 form uses.)
             load_scores(tS, c_lo, c_hi, sv);
+            {
+              uint64_t acc = 0;  // two fp32 zeros
+              exp_chunks_f8(sv, 0, sc, m_used, pk, acc);
+              exp_chunks_f8(sv, 1, sc, m_used, pk, acc);
+              lsum = sum2(acc);
+            }
+            const bool redo = !(lsum <= kOverflowGuardFp8);
+            if (__any_sync(0xffffffffu, redo)) {
+              // Rare: a sum above the guard means this tile's max is above
+              // the reference (128 entries of at most 1 sum to 128 or less).
+              // Reload S (P is not yet written), move the reference of those
+              // rows to this tile's max and let every lane recompute.
+              load_scores(tS, c_lo, c_hi, sv);
+              const float m_tile = row_max(sv) * sc;
+              if (redo && m_tile > m_used) {
+                rescale_o = true;
+                alpha = ptx::ex2(m_used - m_tile);
+                l_run *= alpha;
+                m_used = m_tile;
+              }
+              exponentials<kFp8, kPartial>(sv, sc, m_used, pk, lsum, mx);
+            }
+          } else {
+          // P in two halves of 64 keys: the first half is stored and
+          // signalled (kPReady + t) before the second half's exponentials
+          // run, so the MMA warp starts that half of P V meanwhile.  Both
+          // halves use the current reference; before anything is stored the
+          // first half's row sum and the second half's row max are checked
+          // against the guard (2^64, as a sum and as an exponent).
+          load_scores(tS, c_lo, c_hi, sv);
+          const float lsum1 = exp_half<false>(sv, 0, sc, m_used, pk);
+          const float mx2 = half_max(sv, 1);
+          const bool in_range = (lsum1 <= kOverflowGuard) & (mx2 * sc <= m_used + kOverflowGuardLog2);
+          if (__all_sync(0xffffffffu, in_range)) {
+            store_p_half<false>(tS, pk, 0);
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(kPReady + t));
+            const float lsum2 = exp_half<false>(sv, 1, sc, m_used, pk);
+            l_run += lsum1 + lsum2;
+            store_p_half<false>(tS, pk, 1);
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(kPReadyB + t));
+            continue;
+          }
+          // Rare: a row ran past the guard, so this tile's max is above the
+          // reference (64 entries of at most 1 sum to 64 or less).  Nothing
+          // is stored yet and sv still holds the scores: move the reference
+          // of those rows to this tile's max and let every lane recompute
+          // (lanes that keep theirs get the same P).
+          {
             const float m_tile = row_max(sv) * sc;
-            if (redo && m_tile > m_used) {
+            if (!in_range && m_tile > m_used) {
               rescale_o = true;
               alpha = ptx::ex2(m_used - m_tile);
               l_run *= alpha;
               m_used = m_tile;
             }
             exponentials<kFp8, kPartial>(sv, sc, m_used, pk, lsum, mx);
+          }
           }
         } else {
         load_scores(tS, c_lo, c_hi, sv);
@@ -853,6 +896,7 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(kPReady + t));
+        ptx::mbar_arrive(bar(kPReadyB + t));
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue

@@ -128,6 +128,28 @@ def test_fp8_fused_against_oracle(B, S, H, N, causal, docs, scale):
     _check_fp8(out, lse, want_o, want_l, vmax, (B, S, H, N, causal, docs))
 
 
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("blocks", [(128, 384), (192, 448)], ids=["first-half", "second-half"])
+def test_fp8_scores_jump_past_the_reference(causal, blocks):
+    """Blocks of keys whose scores rise by about 2^16 and 2^32 (as base-2
+    exponents) over the first key tile's: past the FP8 pass's 2^8 guard, so
+    the kernel must move its reference point (keeping every P inside E4M3's
+    range) instead of saturating."""
+    B, S, H, d = 1, 768, 2, 128
+    q, k, v = inputs.make_qkv(B, S, H, d, seed=72, dtype=torch.bfloat16)
+    q = (q.float() * 0.25 + 1.0).to(torch.bfloat16)
+    k = k.float() * 0.25
+    for a, bump in zip(blocks, (1.0, 2.0)):
+        k[:, a:a + 32] += bump
+    fp8 = pkg.fp8_quantize_qkv(q.to(DEV), k.to(torch.bfloat16).to(DEV), v.to(DEV))
+    out, lse = pkg.ring_attn_fwd_fp8(fp8, 2, causal)
+    assert pkg.cp_get_last_status() == 0
+    q8, k8, v8, qd, kd, vd = _oracle_operands(fp8)
+    want_o, want_l = ref.attention_fp8(q8, k8, v8, qd, kd, vd, causal)
+    vmax = np.abs(ref.fp8_dequantize(v8, vd)).max()
+    _check_fp8(out, lse, want_o, want_l, vmax, (causal, blocks))
+
+
 def test_fp8_zero_query_is_the_prefix_mean():
     B, S, H, d, N = 1, 1024, 2, 128, 4
     (q, k, v), _ = _fp8_inputs(B, S, H, d, seed=44)

@@ -119,6 +119,32 @@ def test_bf16_fused_against_oracle(B, S, H, d, N, causal, docs):
     _check_bf16(out, lse, want_o, want_l)
 
 
+def _jump_inputs(seed, bumps, blocks, B=1, S=768, H=2, d=128):
+    """Small keys (scores of order 1) except blocks of 32 keys raised by the
+    given amounts, so a row's scores jump far past its running maximum."""
+    q, k, v = inputs.make_qkv(B, S, H, d, seed=seed, dtype=torch.bfloat16)
+    q = (q.float() * 0.25 + 1.0).to(torch.bfloat16)
+    k = (k.float() * 0.25)
+    for a, bump in zip(blocks, bumps):
+        k[:, a:a + 32] += bump
+    return q, k.to(torch.bfloat16), v
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("blocks", [(128, 384), (192, 448), (176, 432)],
+                         ids=["first-half", "second-half", "straddling"])
+def test_bf16_scores_jump_past_the_reference(causal, blocks):
+    """Scores that rise by about 2^98 and then 2^196 (as base-2 exponents)
+    over the first key tile's: the kernel's no-max pass must see it (through
+    the first 64 keys' row sum or the last 64 keys' row max, depending on
+    where the block sits) and redo the tile against a new reference point."""
+    q, k, v = _jump_inputs(71, (6.0, 12.0), blocks)
+    out, lse = pkg.ring_attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), 2, causal)
+    assert pkg.cp_get_last_status() == 0
+    want_o, want_l = ref.attention(_np(q), _np(k), _np(v), causal)
+    _check_bf16(out, lse, want_o, want_l, (causal, blocks))
+
+
 @pytest.mark.parametrize("causal,docs", [(True, None), (False, None),
                                          (True, [0, 300, 301, 700, 1024])])
 def test_bf16_steps_against_oracle(causal, docs):
