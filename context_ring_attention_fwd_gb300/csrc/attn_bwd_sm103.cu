@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tile_keys(p, f, xs, xe);
           if (!wait1(bar(kX0Empty + s0), ph0 ^ 1u, abort_flag, p)) { ok = false; break; }
           if (p.fault_drop && c == 0 && !dropped) {
-            // Test hook: this tile is never loaded, so the MMA thread's
+            // Test hook: this tile is never loaded, so the MMA warp's
             // bounded wait for it runs out and the CTA takes its abort path.
             dropped = true;
           } else {

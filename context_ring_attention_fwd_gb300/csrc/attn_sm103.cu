@@ -24,9 +24,10 @@
 //              registers to the softmax warpgroups through setmaxnreg)
 // TMEM (512 columns): S_0 | S_1 | O_0 | O_1.  S_t = Q_t K^T lands in TMEM
 // (fp32); the softmax warps read it with tcgen05.ld, write P (bf16 pairs)
-// back over S_t, and the MMA thread issues O_t += P V with P taken from TMEM.
-// While one warpgroup does its exponentials the tensor cores work on the
-// other tile, so the two tiles ping-pong.
+// back over S_t, and the MMA warp issues O_t += P V with P taken from TMEM
+// (bf16: in two halves of 64 keys, the first signalled before the second is
+// computed).  While one warpgroup does its exponentials the tensor cores work
+// on the other tile, so the two tiles ping-pong.
 //
 // Running state.  m is kept in base-2 units (scores pre-multiplied by
 // log2(e)/sqrt(d)).  The reference point used for the exponentials moves
@@ -538,7 +539,7 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
           tile_keys(p, f, ks, ke);
           if (!wait1(bar(kKEmpty + st), ph ^ 1u, abort_flag, p)) { ok = false; break; }
           if (p.fault_drop_k && c == 0 && !dropped) {
-            // Test hook: this K tile is never loaded, so the MMA thread's
+            // Test hook: this K tile is never loaded, so the MMA warp's
             // bounded wait for it runs out and the CTA takes its abort path.
             dropped = true;
           } else {
