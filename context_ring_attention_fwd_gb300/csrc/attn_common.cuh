@@ -76,6 +76,8 @@ __device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, volatile ui
 }
 
 // Warp-uniform bounded wait (every lane calls it; all lanes get one answer).
+// It returns once every lane has itself seen the phase complete, so whichever
+// lane then issues an MMA or a tcgen05 access has acquired the barrier.
 // With honour_abort false it ignores the CTA's abort flag and ends only on the
 // phase or its own time limit (the final drain of a CTA that is giving up).
 template <class P>
@@ -86,7 +88,7 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity,
   const int lane = threadIdx.x & 31;
   for (uint32_t it = 1;; ++it) {
     const bool ok = ptx::mbar_try_wait(bar, parity);
-    if (__any_sync(0xffffffffu, ok)) return true;
+    if (__all_sync(0xffffffffu, ok)) return true;
     if (honour_abort && __any_sync(0xffffffffu, *abort_flag != 0u)) return false;
     if ((it & 255u) == 0) {
       int tout = 0;
