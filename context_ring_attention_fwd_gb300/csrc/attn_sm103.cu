@@ -419,31 +419,20 @@ __device__ __forceinline__ float half_max(const uint32_t (&sv)[4][32], int half)
   return fmaxf(m0, m1);
 }
 
-// P of 64 keys (half 0: keys 0-63, half 1: keys 64-127) against `base` into
-// pk, and its row sum.
-template <bool kFp8>
+// bf16 P of 64 keys (half 0: keys 0-63, half 1: keys 64-127) against `base`
+// into pk[half], and its row sum.
 __device__ __forceinline__ float exp_half(const uint32_t (&sv)[4][32], int half, float sc,
                                           float base, uint32_t (&pk)[2][32]) {
   uint64_t acc = 0;  // two fp32 zeros
   float ls = 0.f;
-  if constexpr (kFp8) {
-    exp_chunks_f8(sv, half, sc, base, pk, acc);
-    return sum2(acc);
-  } else {
-    exp_chunks(sv, half, sc, base, pk, acc, ls);
-    return CPRING_PACKED_F32X2 ? sum2(acc) : ls;
-  }
+  exp_chunks(sv, half, sc, base, pk, acc, ls);
+  return CPRING_PACKED_F32X2 ? sum2(acc) : ls;
 }
 
-// Stores the P of one half of the keys over this lane's S row: bf16 pairs in
-// columns 32*half .. +32, or E4M3 quads in columns 16*half .. +16.
-template <bool kFp8>
+// Stores one half of the keys' bf16 P (columns 32*half .. +32 of the lane's
+// S row).
 __device__ __forceinline__ void store_p_half(uint32_t tS, const uint32_t (&pk)[2][32], int half) {
-  if constexpr (kFp8) {
-    ptx::tmem_st16(tS + 16u * half, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0][16 * half]));
-  } else {
-    ptx::tmem_st32(tS + 32u * half, pk[half]);
-  }
+  ptx::tmem_st32(tS + 32u * half, pk[half]);
 }
 
 // ---------------------------------------------------------------- kernel
@@ -808,17 +797,17 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
           // first half's row sum and the second half's row max are checked
           // against the guard (2^64, as a sum and as an exponent).
           load_scores(tS, c_lo, c_hi, sv);
-          const float lsum1 = exp_half<false>(sv, 0, sc, m_used, pk);
+          const float lsum1 = exp_half(sv, 0, sc, m_used, pk);
           const float mx2 = half_max(sv, 1);
           const bool in_range = (lsum1 <= kOverflowGuard) & (mx2 * sc <= m_used + kOverflowGuardLog2);
           if (__all_sync(0xffffffffu, in_range)) {
-            store_p_half<false>(tS, pk, 0);
+            store_p_half(tS, pk, 0);
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(kPReady + t));
-            const float lsum2 = exp_half<false>(sv, 1, sc, m_used, pk);
+            const float lsum2 = exp_half(sv, 1, sc, m_used, pk);
             l_run += lsum1 + lsum2;
-            store_p_half<false>(tS, pk, 1);
+            store_p_half(tS, pk, 1);
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(kPReadyB + t));
