@@ -103,8 +103,9 @@ enum BBar : int {
   kAccFull = 17,   // the item's accumulators are final
   kVecFull = 18,   // + buffer: per-column lse / delta of a query tile written (kDKDV)
   kVecFree = 20,   // + buffer: every softmax thread is done reading it
-  kDrain = 22,
-  kNumBars = 23
+  kPReadyS = 22,   // + TMEM buffer (kDKDV): dS^T written (kPReady + buffer: P^T written)
+  kDrain = 24,
+  kNumBars = 25
 };
 // kDQ keeps packed dS in its own double buffer of TMEM columns (acc0 ends at
 // 256 + D <= 384), so S and dP of the next step can be issued while the
@@ -213,6 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bar(kVecFull + b2), kT);
       ptx::mbar_init(bar(kVecFree + b2), kSoftmaxThreads);
     }
+    ptx::mbar_init(bar(kPReadyS), kSoftmaxThreads);
+    ptx::mbar_init(bar(kPReadyS + 1), kSoftmaxThreads);
     ptx::mbar_init(bar(kDrain), 1);
     *abort_flag = 0u;
     ptx::fence_barrier_init();
@@ -419,12 +422,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int hh = 0; hh < nh; ++hh) {
           const uint32_t b = m_half & 1u;
           if (hh + 1 < nh && !issue_half(m_half + 1, hh + 1)) { ok = false; break; }
+          // dV += P^T dO_h as soon as P^T is in TMEM, dK += dS^T Q_h once dS^T is
           if (!wait_warp(bar(kPReady + b), (m_half >> 1) & 1u, abort_flag, p)) { ok = false; break; }
           ptx::tc_fence_after();
           const uint32_t st = (x_iter + static_cast<uint32_t>(hh >> 1)) % Lay::kX0Slots;
           const int rows = (hh & 1) * 64 * 128;
-          issue_ts64(tA0, tmem_base + 128u * b, Lay::x1(st) + rows, hh == 0);        // dV += P^T dO_h
-          issue_ts64(tA1, tmem_base + 128u * b + 64u, Lay::x0(st) + rows, hh == 0);  // dK += dS^T Q_h
+          issue_ts64(tA0, tmem_base + 128u * b, Lay::x1(st) + rows, hh == 0);
+          if (!wait_warp(bar(kPReadyS + b), (m_half >> 1) & 1u, abort_flag, p)) { ok = false; break; }
+          ptx::tc_fence_after();
+          issue_ts64(tA1, tmem_base + 128u * b + 64u, Lay::x0(st) + rows, hh == 0);
           if (hh & 1) {
             ptx::mma_commit_w(bar(kX0Empty + st));
             ptx::mma_commit_w(bar(kX1Empty + st));
@@ -575,53 +581,80 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::reg_fence(dv);
           const int c0 = 64 * h + 32 * wg;   // first tile column of this piece
           uint32_t pk_p[16], pk_s[16];
+          float pf[32];  // this chunk's P in fp32, for dS
           // per-column -lse2 and -D of this chunk, four columns per load
           const float4* nl4 = reinterpret_cast<const float4*>(vec + (buf * 2 + 0) * kT + c0);
           const float4* nd4 = reinterpret_cast<const float4*>(vec + (buf * 2 + 1) * kT + c0);
-          if (__all_sync(0xffffffffu, c_lo <= c0 && c_hi >= c0 + 31)) {
+          // P^T first: it is stored and announced (kPReady) before dS^T is
+          // formed, so the MMA warp starts dV += P^T dO meanwhile.
+          const bool all_visible = __all_sync(0xffffffffu, c_lo <= c0 && c_hi >= c0 + 31);
+          if (all_visible) {
             // every column visible to every row of the warp: paired fp32
 #pragma unroll
             for (int x4 = 0; x4 < 8; ++x4) {
-              const float4 nl = nl4[x4], nd = nd4[x4];
+              const float4 nl = nl4[x4];
               const float nla[4] = {nl.x, nl.y, nl.z, nl.w};
+#pragma unroll
+              for (int hx = 0; hx < 2; ++hx) {
+                const int x = 2 * x4 + hx;
+                float e0, e1;
+                ptx::fma_f32x2(e0, e1, __uint_as_float(sv[2 * x]), __uint_as_float(sv[2 * x + 1]), sc,
+                               sc, nla[2 * hx], nla[2 * hx + 1]);
+                pf[2 * x] = ptx::ex2(e0);
+                pf[2 * x + 1] = ptx::ex2(e1);
+                pk_p[x] = ptx::pack_bf16(pf[2 * x], pf[2 * x + 1]);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int cc = c0 + 2 * x + e;
+                const bool vis = cc >= c_lo && cc <= c_hi;
+                pf[2 * x + e] =
+                    vis ? ptx::ex2(fmaf(__uint_as_float(sv[2 * x + e]), sc, vec[(buf * 2 + 0) * kT + cc]))
+                        : 0.f;
+              }
+              pk_p[x] = ptx::pack_bf16(pf[2 * x], pf[2 * x + 1]);
+            }
+          }
+          ptx::tmem_st16(tb, pk_p);
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(kPReady + b));
+          // dS^T = P^T (dP^T - D)
+          if (all_visible) {
+#pragma unroll
+            for (int x4 = 0; x4 < 8; ++x4) {
+              const float4 nd = nd4[x4];
               const float nda[4] = {nd.x, nd.y, nd.z, nd.w};
 #pragma unroll
               for (int hx = 0; hx < 2; ++hx) {
                 const int x = 2 * x4 + hx;
-                float e0, e1, g0, g1;
-                ptx::fma_f32x2(e0, e1, __uint_as_float(sv[2 * x]), __uint_as_float(sv[2 * x + 1]), sc,
-                               sc, nla[2 * hx], nla[2 * hx + 1]);
-                const float p0 = ptx::ex2(e0), p1 = ptx::ex2(e1);
+                float g0, g1;
                 ptx::fma_f32x2(g0, g1, __uint_as_float(dv[2 * x]), __uint_as_float(dv[2 * x + 1]), 1.f,
                                1.f, nda[2 * hx], nda[2 * hx + 1]);
-                ptx::fma_f32x2(g0, g1, p0, p1, g0, g1, 0.f, 0.f);
-                pk_p[x] = ptx::pack_bf16(p0, p1);
+                ptx::fma_f32x2(g0, g1, pf[2 * x], pf[2 * x + 1], g0, g1, 0.f, 0.f);
                 pk_s[x] = ptx::pack_bf16(g0, g1);
               }
             }
           } else {
 #pragma unroll
             for (int x = 0; x < 16; ++x) {
-              float pr[2], dsr[2];
+              float dsr[2];
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
                 const int cc = c0 + 2 * x + e;
-                const bool vis = cc >= c_lo && cc <= c_hi;
-                const float pv =
-                    vis ? ptx::ex2(fmaf(__uint_as_float(sv[2 * x + e]), sc, vec[(buf * 2 + 0) * kT + cc]))
-                        : 0.f;
-                pr[e] = pv;
-                dsr[e] = pv * (__uint_as_float(dv[2 * x + e]) + vec[(buf * 2 + 1) * kT + cc]);
+                dsr[e] = pf[2 * x + e] * (__uint_as_float(dv[2 * x + e]) + vec[(buf * 2 + 1) * kT + cc]);
               }
-              pk_p[x] = ptx::pack_bf16(pr[0], pr[1]);
               pk_s[x] = ptx::pack_bf16(dsr[0], dsr[1]);
             }
           }
-          ptx::tmem_st16(tb, pk_p);
           ptx::tmem_st16(tb + 64, pk_s);
           ptx::tmem_wait_st();
           ptx::tc_fence_before();
-          ptx::mbar_arrive(bar(kPReady + b));
+          ptx::mbar_arrive(bar(kPReadyS + b));
           ++h_cnt;
         }
         if (!ok) break;
