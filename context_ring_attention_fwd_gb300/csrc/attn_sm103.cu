@@ -843,6 +843,35 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
             m_used = m_tile;
           }
           exponentials<kFp8, kPartial>(sv, sc, (m_used == -INFINITY) ? 0.f : m_used, pk, lsum, mx);
+        } else if constexpr (kPartial) {
+          // Step kernel: the exact row max first (its epilogue exports it),
+          // then P in two halves of 64 keys, each signalled once stored, as
+          // in the fused pass.  When a row's reference has to move, O is
+          // rescaled before any of this tile's P V, so P goes out whole.
+          mx = row_max(sv);
+          const float m_tile = mx * sc;
+          m_true = fmaxf(m_true, m_tile);
+          if (m_tile > m_used + kRescaleLog2) {
+            rescale_o = true;
+            alpha = ptx::ex2(m_used - m_tile);
+            l_run *= alpha;
+            m_used = m_tile;
+          }
+          if (!__any_sync(0xffffffffu, rescale_o)) {
+            const float lsum1 = exp_half(sv, 0, sc, m_used, pk);
+            store_p_half(tS, pk, 0);
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(kPReady + t));
+            const float lsum2 = exp_half(sv, 1, sc, m_used, pk);
+            l_run += lsum1 + lsum2;
+            store_p_half(tS, pk, 1);
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(kPReadyB + t));
+            continue;
+          }
+          exponentials<kFp8, kPartial>(sv, sc, m_used, pk, lsum, mx);
         } else {
           // Exponentials against the current reference; the row max is
           // taken in the same pass and only forces a redo (rare) when it
