@@ -790,44 +790,45 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
               exponentials<kFp8, kPartial>(sv, sc, m_used, pk, lsum, mx);
             }
           } else {
-          // P in two halves of 64 keys: the first half is stored and
-          // signalled (kPReady + t) before the second half's exponentials
-          // run, so the MMA warp starts that half of P V meanwhile.  Both
-          // halves use the current reference; before anything is stored the
-          // first half's row sum and the second half's row max are checked
-          // against the guard (2^64, as a sum and as an exponent).
-          load_scores(tS, c_lo, c_hi, sv);
-          const float lsum1 = exp_half(sv, 0, sc, m_used, pk);
-          const float mx2 = half_max(sv, 1);
-          const bool in_range = (lsum1 <= kOverflowGuard) & (mx2 * sc <= m_used + kOverflowGuardLog2);
-          if (__all_sync(0xffffffffu, in_range)) {
-            store_p_half(tS, pk, 0);
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(kPReady + t));
-            const float lsum2 = exp_half(sv, 1, sc, m_used, pk);
-            l_run += lsum1 + lsum2;
-            store_p_half(tS, pk, 1);
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(kPReadyB + t));
-            continue;
-          }
-          // Rare: a row ran past the guard, so this tile's max is above the
-          // reference (64 entries of at most 1 sum to 64 or less).  Nothing
-          // is stored yet and sv still holds the scores: move the reference
-          // of those rows to this tile's max and let every lane recompute
-          // (lanes that keep theirs get the same P).
-          {
-            const float m_tile = row_max(sv) * sc;
-            if (!in_range && m_tile > m_used) {
-              rescale_o = true;
-              alpha = ptx::ex2(m_used - m_tile);
-              l_run *= alpha;
-              m_used = m_tile;
+            // P in two halves of 64 keys: the first half is stored and
+            // signalled (kPReady + t) before the second half's exponentials
+            // run, so the MMA warp starts that half of P V meanwhile.  Both
+            // halves use the current reference; before anything is stored the
+            // first half's row sum and the second half's row max are checked
+            // against the guard (2^64, as a sum and as an exponent).
+            load_scores(tS, c_lo, c_hi, sv);
+            const float lsum1 = exp_half(sv, 0, sc, m_used, pk);
+            const float mx2 = half_max(sv, 1);
+            const bool in_range =
+                (lsum1 <= kOverflowGuard) & (mx2 * sc <= m_used + kOverflowGuardLog2);
+            if (__all_sync(0xffffffffu, in_range)) {
+              store_p_half(tS, pk, 0);
+              ptx::tmem_wait_st();
+              ptx::tc_fence_before();
+              ptx::mbar_arrive(bar(kPReady + t));
+              const float lsum2 = exp_half(sv, 1, sc, m_used, pk);
+              l_run += lsum1 + lsum2;
+              store_p_half(tS, pk, 1);
+              ptx::tmem_wait_st();
+              ptx::tc_fence_before();
+              ptx::mbar_arrive(bar(kPReadyB + t));
+              continue;
             }
-            exponentials<kFp8, kPartial>(sv, sc, m_used, pk, lsum, mx);
-          }
+            // Rare: a row ran past the guard, so this tile's max is above the
+            // reference (64 entries of at most 1 sum to 64 or less).  Nothing
+            // is stored yet and sv still holds the scores: move the reference
+            // of those rows to this tile's max and let every lane recompute
+            // (lanes that keep theirs get the same P).
+            {
+              const float m_tile = row_max(sv) * sc;
+              if (!in_range && m_tile > m_used) {
+                rescale_o = true;
+                alpha = ptx::ex2(m_used - m_tile);
+                l_run *= alpha;
+                m_used = m_tile;
+              }
+              exponentials<kFp8, kPartial>(sv, sc, m_used, pk, lsum, mx);
+            }
           }
         } else {
         load_scores(tS, c_lo, c_hi, sv);
