@@ -38,12 +38,20 @@ METRIC = "effective causal TFLOP/s of ring-attention fwd (1 GB300) and % of bf16
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "bf16_causal_128k"
 # DRAM bytes (read + write) per launch of the fused attention kernel, from one
-# ncu capture of dram__bytes_read.sum + dram__bytes_write.sum on this bench
-# command with that workload.  They hold for the kernel they were taken on:
-# re-take them whenever the kernel changes.
-NCU_TRAFFIC_BYTES = {
-    "bf16_causal_128k": 14.518e9 + 1.081e9,
+# ncu capture of dram__bytes_read.sum + dram__bytes_write.sum limited to that
+# kernel (-k regex:ring_attn_bf16 -c 1) on this bench command with the
+# workload named.  Each figure holds only for the kernel source it was taken
+# on: "sources" is the SHA-256 prefix of the forward kernel's source files
+# (KERNEL_SOURCES), and a line whose sources differ reports traffic null.
+NCU_TRAFFIC = {
+    "bf16_causal_128k": {"bytes": None, "sources": None},
 }
+KERNEL_SOURCES = ("context_ring_attention_fwd_gb300/csrc/attn_sm103.cu",
+                  "context_ring_attention_fwd_gb300/csrc/attn_common.cuh",
+                  "context_ring_attention_fwd_gb300/csrc/ptx.cuh")
+# tcgen05 dense bf16 -> fp32 rate per SM and clock: a 128x128x16 MMA
+# (524,288 FLOPs) every 64 clocks.
+TCGEN05_BF16_FLOP_PER_CLK_SM = 8192
 
 
 # ------------------------------------------------------------------ helpers
@@ -56,6 +64,78 @@ def visible_pairs(S: int, causal: bool, docs) -> int:
 
 def effective_flops(w, docs) -> int:
     return 4 * w.d * visible_pairs(w.S, w.causal, docs) * w.B * w.H
+
+
+def kernel_sources_digest() -> str:
+    """SHA-256 prefix over the forward kernel's source files."""
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(name: str):
+    """The recorded DRAM traffic of the kernel for this workload, or None when
+    it was not recorded for the kernel source as it stands."""
+    rec = NCU_TRAFFIC.get(name)
+    if not rec or rec["bytes"] is None or rec["sources"] != kernel_sources_digest():
+        return None
+    return rec["bytes"]
+
+
+def computed_tile_ratio(S: int, n_shards: int, tile: int = 128) -> float:
+    """Causal over full count of the (query tile, key tile) pairs the fused
+    kernel computes, with tiles laid from each shard's first row."""
+    L = S // n_shards
+    T = -(-L // tile)
+    first = np.array([i * L + a * tile for i in range(n_shards) for a in range(T)])
+    last = np.minimum(first + tile, (first // L + 1) * L) - 1
+    # key tile (k0, .) is computed for query tile (., q1) iff k0 <= q1
+    causal = int(np.searchsorted(first, last, side="right").sum())
+    return causal / (first.size ** 2)
+
+
+def blas_threads():
+    """Threads of the BLAS numpy calls into, or None when it cannot be asked."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads") for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:  # noqa: BLE001 - optional module, absent on some hosts
+        pass
+    import ctypes
+    try:
+        with open("/proc/self/maps") as f:
+            libs = {ln.split()[-1] for ln in f if "blas" in ln.lower() and ".so" in ln}
+    except OSError:
+        return None
+    for path in sorted(libs):
+        try:
+            h = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for sym in ("openblas_get_num_threads", "scipy_openblas_get_num_threads64_",
+                    "openblas_get_num_threads64_"):
+            fn = getattr(h, sym, None)
+            if fn is not None:
+                fn.restype = ctypes.c_int
+                return int(fn())
+    return None
+
+
+def core_record():
+    cpu = os.cpu_count() or 1
+    try:
+        aff = len(os.sched_getaffinity(0))
+    except AttributeError:
+        aff = cpu
+    bt = blas_threads()
+    # the matrix products run on the BLAS threads; the rest of numpy on one
+    return {"cores": bt if bt else aff, "cpu_count": cpu, "affinity_cores": aff,
+            "blas_threads": bt}
 
 
 def dist_env():
@@ -205,13 +285,6 @@ def oracle_sample(w, get_head, docs, budget_s: float, rows_per_head: int, seed: 
     return flops, dt, desc
 
 
-def host_cores() -> int:
-    try:
-        return len(os.sched_getaffinity(0))
-    except AttributeError:
-        return os.cpu_count() or 1
-
-
 # ------------------------------------------------------------------- arms
 def run_reference(args, w, rank, world):
     """The reference arm: the fp64 CPU oracle, on rank 0 only, each step a
@@ -252,7 +325,7 @@ def run_reference(args, w, rank, world):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",
         "config": _config(w, docs, world),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, **core_record(), "kind": "oracle",
                          "sample": "each step: " + desc,
                          # the whole workload at the sample's rate (extrapolated, not run)
                          "extrapolated_full_seconds": effective_flops(w, docs) / (value * 1e12)},
@@ -326,14 +399,28 @@ def run_ours(args, w, rank, world, local):
     avg_launch_ms = statistics.mean(per_launch_ms)
     achieved = flops / (avg_launch_ms * 1e-3) / 1e12
     peak_burst, peak_sust, peak_src = measured_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    tc_at_clock = (TCGEN05_BF16_FLOP_PER_CLK_SM * sms * clk["sm_mhz"] * 1e6 / 1e12
+                   if clk.get("sm_mhz") else None)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
                 "frac": achieved / peak_burst,
-                "traffic": args.traffic if args.traffic is not None
-                else NCU_TRAFFIC_BYTES.get(w.name),
+                "traffic": args.traffic if args.traffic is not None else ncu_traffic(w.name),
+                "traffic_sources": kernel_sources_digest(),
+                "algorithmic_bytes": 4 * w.B * w.S * w.H * w.d * w.elem_bytes
+                + 4 * w.B * w.H * w.S,
                 "peak_kind": f"{peak_src} bf16 dense burst (cuBLAS)",
-                "frac_of_sustained": achieved / peak_sust if peak_sust else None}
+                "frac_of_sustained": achieved / peak_sust if peak_sust else None,
+                # the tensor pipe's own rate at the SM clock sampled in the timed region
+                "tcgen05_peak_at_sampled_clock": tc_at_clock,
+                "frac_of_tcgen05_at_sampled_clock": achieved / tc_at_clock if tc_at_clock
+                else None}
 
-    # end to end through the public API from pinned host buffers
+    # the schedule's acceptance checks on this shape (untimed for the metric)
+    gates = None
+    if docs is None and not args.no_gates:
+        gates = schedule_gates(pkg, w, q, k, v, out, lse, stream, dev)
+
+    # end to end through the C ABI's host-buffer entry point (cp_ring_attn_fwd_host)
     e2e = None
     if args.e2e_steps > 0:
         hq = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
@@ -342,8 +429,13 @@ def run_ours(args, w, rank, world, local):
         hq.copy_(q)
         hk.copy_(k)
         hv.copy_(v)
-        bufs = (q, k, v, out, lse, torch.empty(q.shape, dtype=q.dtype, pin_memory=True),
-                torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True))
+        del q, k, v, out, lse
+        torch.cuda.empty_cache()
+        esz = hq.element_size()
+        bufs = (torch.empty(pkg.cp_ring_attn_fwd_host_workspace_bytes(
+                    w.B, w.S, w.H, w.d, w.n_shards, esz), dtype=torch.uint8, device=dev),
+                torch.empty(hq.shape, dtype=hq.dtype, pin_memory=True),
+                torch.empty((w.B, w.H, w.S), dtype=torch.float32, pin_memory=True))
         pkg.ring_attn_fwd_host(hq, hk, hv, w.n_shards, w.causal, docs, buffers=bufs)
         barrier(world, dev)
         torch.cuda.synchronize(dev)
@@ -352,21 +444,27 @@ def run_ours(args, w, rank, world, local):
             pkg.ring_attn_fwd_host(hq, hk, hv, w.n_shards, w.causal, docs, buffers=bufs)
         dt = time.perf_counter() - t0
         dt = max_over_ranks(dt, world, dev)
-        elem = q.numel() * q.element_size()
+        elem = hq.numel() * hq.element_size()
         e2e = {"value": flops * world * args.e2e_steps / dt / 1e12, "unit": UNIT,
-               "h2d_bytes_per_step": 3 * elem + (0 if docs is None else 4 * len(docs)),
-               "d2h_bytes_per_step": elem + lse.numel() * 4,
-               "ms_per_step": 1e3 * dt / args.e2e_steps, "steps": args.e2e_steps}
-        del hq, hk, hv, bufs
+               "h2d_bytes_per_step": 3 * elem,
+               "d2h_bytes_per_step": elem + w.B * w.H * w.S * 4,
+               "ms_per_step": 1e3 * dt / args.e2e_steps, "steps": args.e2e_steps,
+               "entry_point": "cp_ring_attn_fwd_host"}
+        if docs is not None:
+            e2e["doc_offsets"] = "resident on the device, as the C ABI takes them"
+        host_inputs = (hq, hk, hv)
+        del bufs
+    else:
+        host_inputs = tuple(t.cpu() for t in (q, k, v))
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         def get_head(b, h):
-            return tuple(t[b:b + 1, :, h:h + 1].float().cpu().numpy() for t in (q, k, v))
+            return tuple(t[b:b + 1, :, h:h + 1].float().numpy() for t in host_inputs)
 
         f, dt, desc = oracle_sample(w, get_head, docs, budget_s=args.cpu_budget,
                                     rows_per_head=args.cpu_rows)
-        cpu = {"value": f / dt / 1e12, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+        cpu = {"value": f / dt / 1e12, "unit": UNIT, **core_record(), "kind": "oracle",
                "sample": desc, "seconds": dt,
                # the whole workload at the sample's rate (extrapolated, not run)
                "extrapolated_full_seconds": effective_flops(w, docs) / (f / dt)}
@@ -378,10 +476,42 @@ def run_ours(args, w, rank, world, local):
         "config": _config(w, docs, world),
         "frac_of_peak": value / world / peak_burst,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
-        "clocks": clk,
+        "clocks": clk, "gates": gates,
         "effective_flops_per_step": flops * world,
     }
     return line
+
+
+def schedule_gates(pkg, w, q, k, v, out, lse, stream, dev, steps: int = 3):
+    """The schedule's acceptance checks on the workload's shape: the causal
+    forward's time over the same shape without the causal mask (ideal: the
+    computed-tile ratio; gate <= 0.53), and the causal time at N = 1, 2, 4, 8
+    shards (equal work; gate: spread <= 3 %).  One warm-up launch and `steps`
+    timed launches each, CUDA events on the launching stream."""
+    def timed(n_shards, causal):
+        pkg.cp_ring_attn_fwd(q, k, v, out, lse, n_shards, causal, None, stream)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            pkg.cp_ring_attn_fwd(q, k, v, out, lse, n_shards, causal, None, stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / steps
+
+    by_n = {n: timed(n, True) for n in (1, 2, 4, 8) if w.S % n == 0}
+    t_full = timed(w.n_shards, False)
+    t_causal = by_n.get(w.n_shards) or timed(w.n_shards, True)
+    if pkg.cp_get_last_status(stream) != 0:
+        raise RuntimeError("device error in the schedule checks")
+    ideal = computed_tile_ratio(w.S, w.n_shards)
+    spread = (max(by_n.values()) - min(by_n.values())) / min(by_n.values())
+    ratio = t_causal / t_full
+    return {"ms_causal": t_causal, "ms_full": t_full, "causal_over_full": ratio,
+            "computed_tile_ratio": ideal, "causal_over_full_ok": ratio <= 0.53,
+            "ms_causal_by_n_shards": {str(n): t for n, t in by_n.items()},
+            "n_shards_spread": spread, "n_shards_spread_ok": spread <= 0.03,
+            "steps_each": steps}
 
 
 def run_ring_emulation(args, w, local):
@@ -671,6 +801,85 @@ def run_skip_check(args, w, local):
     }
 
 
+def run_hbm_kernels(args, w, local):
+    """Time the bandwidth-bound kernels at the workload's shape, each against
+    the measured HBM copy peak: the online merge and the finalize over one
+    rank's fp32 state [B, S/N, H, d] (cp_lse_merge, cp_lse_finalize) and the
+    FP8 quantiser of one bf16 tensor (cp_fp8_quantize, plain and transposed);
+    the all-to-all permutation of the Ulysses form is reported by --ulysses.
+    Algorithmic bytes per unit: merge 12 d + 24 per (b, row, h) (O, m, l of
+    both operands read, the running state written); finalize 4 d + 8 read and
+    2 d + 4 written (bf16 out); quantiser 2 B read for the amax, then 2 B read
+    and 1 B written per element.  One JSON line."""
+    import context_ring_attention_fwd_gb300 as pkg
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    B, H, d, N = w.B, w.H, w.d, w.n_shards
+    L = w.S // N
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    o_acc = torch.randn((B, L, H, d), generator=g, device=dev)
+    o_p = torch.randn((B, L, H, d), generator=g, device=dev)
+    m_acc = torch.randn((B, H, L), generator=g, device=dev)
+    m_p = torch.randn((B, H, L), generator=g, device=dev)
+    l_acc = torch.rand((B, H, L), generator=g, device=dev) + 1.0
+    l_p = torch.rand((B, H, L), generator=g, device=dev) + 1.0
+    out = torch.empty((B, L, H, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, L), dtype=torch.float32, device=dev)
+    x = torch.randn((w.B, w.S, w.H, w.d), generator=g, device=dev).to(torch.bfloat16)
+    x8 = torch.empty((w.B, w.S, w.H, w.d), dtype=torch.uint8, device=dev)
+    x8t = torch.empty((w.B, w.H, w.d, w.S), dtype=torch.uint8, device=dev)
+    desc = torch.empty((w.B, w.H), dtype=torch.float32, device=dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        times = []
+        for _ in range(args.steps):
+            flush.zero_()   # 512 MB written: the L2 (129 MB) holds nothing of the inputs
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(e0.elapsed_time(e1))
+        return statistics.median(times)
+
+    rows = B * L * H
+    elems = w.B * w.S * w.H * w.d
+    hbm, _, hbm_src = measured_peaks_hbm()
+    kernels = []
+
+    def add(name, ms, nbytes, unit_desc):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        kernels.append({"kernel": name, "ms": ms, "bytes": int(nbytes), "GB/s": gbs,
+                        "frac_of_hbm": gbs / hbm, "units": unit_desc})
+
+    add("lse_merge_kernel (cp_lse_merge)",
+        timed(lambda: pkg.cp_lse_merge(o_acc, m_acc, l_acc, o_p, m_p, l_p, stream)),
+        rows * (12 * d + 24), f"{rows} (b,row,h) x (12 d + 24) B")
+    add("lse_finalize_kernel (cp_lse_finalize, bf16 out)",
+        timed(lambda: pkg.cp_lse_finalize(o_acc, m_acc, l_acc, out, lse, stream)),
+        rows * (6 * d + 12), f"{rows} (b,row,h) x (6 d + 12) B")
+    add("fp8 quantiser (cp_fp8_quantize, [B,S,H,d])",
+        timed(lambda: pkg.cp_fp8_quantize(x, x8, desc, False, stream)),
+        elems * 5, f"{elems} elements x 5 B")
+    add("fp8 quantiser (cp_fp8_quantize, transposed [B,H,d,S])",
+        timed(lambda: pkg.cp_fp8_quantize(x, x8t, desc, True, stream)),
+        elems * 5, f"{elems} elements x 5 B")
+    if pkg.cp_get_last_status(stream) != 0:
+        raise RuntimeError("device error in the bandwidth-bound kernels")
+    return {"metric": "achieved GB/s of the bandwidth-bound kernels (1 GB300)",
+            "impl": "hbm_kernels", "unit": "GB/s", "hbm_peak_GBps": hbm,
+            "hbm_peak_kind": f"{hbm_src} copy bandwidth", "kernels": kernels,
+            "l2_flush": "512 MB written between timed launches",
+            "steps": args.steps, "warmup": args.warmup, "n_gpus": 1, "data": "synthetic",
+            "config": _config(w, None, 1)}
+
+
 def measured_peaks_hbm():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -689,7 +898,12 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
-    ap.add_argument("--cpu-rows", type=int, default=128)
+    ap.add_argument("--cpu-rows", type=int, default=512)
+    ap.add_argument("--no-gates", action="store_true",
+                    help="leave the schedule checks out of the default line")
+    ap.add_argument("--hbm-kernels", action="store_true",
+                    help="time the bandwidth-bound kernels (merge, finalize, FP8 quantiser, "
+                         "all-to-all permutation) against the measured HBM peak instead")
     ap.add_argument("--ring-emulation", action="store_true",
                     help="time the ring with explicit per-rank buffers instead")
     ap.add_argument("--ulysses", action="store_true",
@@ -706,10 +920,12 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_env()
     w = inputs.BY_NAME[args.workload]
-    if args.ring_emulation or args.ulysses or args.fp8 or args.bwd or args.skip_check:
+    if (args.ring_emulation or args.ulysses or args.fp8 or args.bwd or args.skip_check
+            or args.hbm_kernels):
         line = (run_ring_emulation(args, w, local) if args.ring_emulation
                 else run_ulysses(args, w, local) if args.ulysses
                 else run_fp8(args, w, local) if args.fp8
+                else run_hbm_kernels(args, w, local) if args.hbm_kernels
                 else run_bwd(args, w, local) if args.bwd else run_skip_check(args, w, local))
         if rank == 0:
             print(json.dumps(line), flush=True)

@@ -19,7 +19,8 @@ import torch
 
 from ._binding import (  # noqa: F401
     CP_OK, STATUS_CODES, STATUS_NAMES, CpError, LIB_PATH, cp_fp8_quantize, cp_get_last_status,
-    cp_ring_attn_fwd_rank,
+    cp_ring_attn_fwd_rank, cp_ring_attn_fwd_host, cp_ring_attn_fwd_host_workspace_bytes,
+    cp_ring_attn_fwd_noalloc,
     cp_lse_finalize, cp_lse_merge, cp_ring_attn_bwd, cp_ring_attn_bwd_workspace_bytes,
     cp_ring_attn_fwd, cp_ring_attn_fwd_emulated,
     cp_ring_attn_fwd_f32, cp_ring_attn_fwd_fp8,
@@ -33,6 +34,7 @@ __all__ = [
     "cp_ring_attn_fwd", "cp_ring_attn_fwd_f32", "cp_ring_step", "cp_lse_merge",
     "cp_lse_finalize", "cp_ring_schedule", "cp_ring_traffic", "cp_get_last_status",
     "cp_status_string", "ring_attn_fwd", "ring_attn_fwd_host", "ring_attn_composed",
+    "cp_ring_attn_fwd_host", "cp_ring_attn_fwd_noalloc",
     "cp_fp8_quantize", "cp_ring_attn_fwd_fp8", "fp8_quantize_qkv", "ring_attn_fwd_fp8",
     "cp_ring_attn_bwd", "ring_attn_bwd",
     "CpError", "lib",
@@ -56,85 +58,31 @@ def ring_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, n_shards: i
     return out, lse
 
 
-_COPY_STREAMS = {}
-
-
-def _copy_streams(device):
-    """Two streams per device for host <-> device copies (one per direction)."""
-    key = torch.device(device).index if torch.device(device).index is not None else \
-        torch.cuda.current_device()
-    if key not in _COPY_STREAMS:
-        _COPY_STREAMS[key] = (torch.cuda.Stream(device=key), torch.cuda.Stream(device=key))
-    return _COPY_STREAMS[key]
-
-
 def ring_attn_fwd_host(q_host: torch.Tensor, k_host: torch.Tensor, v_host: torch.Tensor,
                        n_shards: int = 1, causal: bool = True, doc_offsets=None,
                        device: str = "cuda", buffers=None, stream=None):
-    """End-to-end call from host tensors: copy Q/K/V to the device, run the
-    fused forward, copy out and lse back.  `buffers` may hold reusable
-    (q, k, v, out, lse, out_host, lse_host) tensors.  Returns the host
-    (out, lse).
-
-    bf16 runs rank by rank (cp_ring_attn_fwd_rank): shard i's Q/K/V go in on a
-    copy stream, rank i starts once the shards it reads have landed (0..i
-    under causality, all shards otherwise), and its rows of out come back on
-    a second copy stream while later ranks compute.  The result is bitwise
-    that of one cp_ring_attn_fwd call."""
+    """End-to-end call from host tensors through cp_ring_attn_fwd_host (the
+    library copies Q/K/V in shard by shard, runs rank by rank and copies out
+    and lse back while later ranks compute).  `buffers` may hold a reusable
+    (workspace, out_host, lse_host); otherwise they are allocated here (the
+    host ones page-locked).  Waits for the stream and returns the host
+    (out, lse)."""
     B, S, H, d = q_host.shape
+    esz = 2 if q_host.dtype == torch.bfloat16 else 4
+    dev = torch.device(device)
     if buffers is None:
-        dq = torch.empty(q_host.shape, dtype=q_host.dtype, device=device)
-        dk = torch.empty_like(dq)
-        dv = torch.empty_like(dq)
-        dout = torch.empty_like(dq)
-        dlse = torch.empty((B, H, S), dtype=torch.float32, device=device)
+        need = cp_ring_attn_fwd_host_workspace_bytes(B, S, H, d, int(n_shards), esz)
+        if need < 0:
+            raise CpError("cp_ring_attn_fwd_host_workspace_bytes", STATUS_CODES["CP_ERR_SHAPE"])
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
         hout = torch.empty(q_host.shape, dtype=q_host.dtype, pin_memory=True)
         hlse = torch.empty((B, H, S), dtype=torch.float32, pin_memory=True)
     else:
-        dq, dk, dv, dout, dlse, hout, hlse = buffers
-    docs = doc_offsets_tensor(doc_offsets, dq.device)
-    compute = stream if stream is not None else torch.cuda.current_stream(dq.device)
-    if dq.dtype != torch.bfloat16:
-        with torch.cuda.stream(compute):
-            dq.copy_(q_host, non_blocking=True)
-            dk.copy_(k_host, non_blocking=True)
-            dv.copy_(v_host, non_blocking=True)
-            cp_ring_attn_fwd_f32(dq, dk, dv, dout, dlse, n_shards, causal, docs, compute)
-            hout.copy_(dout, non_blocking=True)
-            hlse.copy_(dlse, non_blocking=True)
-        compute.synchronize()
-        return hout, hlse
-    N = int(n_shards)
-    L = S // N
-    h2d, d2h = _copy_streams(dq.device)
-    landed = []
-    h2d.wait_stream(compute)          # the device buffers are free to overwrite
-    with torch.cuda.stream(h2d):
-        for i in range(N):
-            for b in range(B):
-                rows = slice(i * L, (i + 1) * L)
-                dq[b, rows].copy_(q_host[b, rows], non_blocking=True)
-                dk[b, rows].copy_(k_host[b, rows], non_blocking=True)
-                dv[b, rows].copy_(v_host[b, rows], non_blocking=True)
-            ev = torch.cuda.Event()
-            ev.record(h2d)
-            landed.append(ev)
-    d2h.wait_stream(compute)          # the host output buffers are free
-    for i in range(N):
-        compute.wait_event(landed[i if causal else N - 1])
-        cp_ring_attn_fwd_rank(dq, dk, dv, dout, dlse, N, i, causal, docs, compute)
-        done = torch.cuda.Event()
-        done.record(compute)
-        d2h.wait_event(done)
-        with torch.cuda.stream(d2h):
-            for b in range(B):
-                rows = slice(i * L, (i + 1) * L)
-                hout[b, rows].copy_(dout[b, rows], non_blocking=True)
-    with torch.cuda.stream(d2h):
-        hlse.copy_(dlse, non_blocking=True)
-    d2h.synchronize()
-    compute.wait_stream(d2h)
-    compute.synchronize()
+        ws, hout, hlse = buffers
+    docs = doc_offsets_tensor(doc_offsets, ws.device)
+    st = stream if stream is not None else torch.cuda.current_stream(ws.device)
+    cp_ring_attn_fwd_host(q_host, k_host, v_host, hout, hlse, n_shards, causal, docs, ws, st)
+    st.synchronize()
     return hout, hlse
 
 

@@ -47,8 +47,8 @@ _SIGS = {
     "cp_ulysses_workspace_bytes": [_i, _i, _i, _i, _i],
     "cp_ulysses_attn_fwd": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _i64, _vp,
                             ctypes.POINTER(_i64)],
-    "cp_ring_attn_fwd_emulated": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _i64,
-                                  _vp, _vp, ctypes.POINTER(_i64)],
+    "cp_ring_attn_fwd_emulated": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp,
+                                  _i64, _vp, _vp, ctypes.POINTER(_i64)],
     "cp_fp8_quantize": [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp],
     "cp_ring_attn_bwd_workspace_bytes": [_i, _i, _i, _i, _i],
     "cp_ring_schedule_device": [_i, _i, _i, _vp, _vp, _vp],
@@ -56,6 +56,11 @@ _SIGS = {
                          _vp, _i64, _vp],
     "cp_ring_attn_fwd_fp8": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp,
                              _vp],
+    "cp_ring_attn_fwd_host_workspace_bytes": [_i, _i, _i, _i, _i, _i],
+    "cp_ring_attn_fwd_host": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _i64,
+                              _vp],
+    "cp_ring_attn_fwd_host_f32": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp,
+                                  _i64, _vp],
 }
 
 
@@ -86,7 +91,8 @@ def lib() -> ctypes.CDLL:
                 elif name in ("cp_launch_counts", "cp_test_set_wait_fault"):
                     fn.restype = None
                 elif name in ("cp_ring_emulated_workspace_bytes", "cp_ulysses_workspace_bytes",
-                              "cp_ring_attn_bwd_workspace_bytes"):
+                              "cp_ring_attn_bwd_workspace_bytes",
+                              "cp_ring_attn_fwd_host_workspace_bytes"):
                     fn.restype = _i64
                 else:
                     fn.restype = _i
@@ -225,6 +231,51 @@ def cp_ring_attn_fwd_rank(q, k, v, out, lse, n_shards: int, rank: int, causal: b
         int(bool(causal)), _ptr(doc_offsets), _stream(stream)))
 
 
+def cp_ring_attn_fwd_host_workspace_bytes(B: int, S: int, H: int, d: int, n_shards: int,
+                                          elem_bytes: int = 2) -> int:
+    return int(lib().cp_ring_attn_fwd_host_workspace_bytes(B, S, H, d, n_shards, elem_bytes))
+
+
+def _need_host(t: torch.Tensor, name: str, dtype: torch.dtype, shape) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.is_cuda:
+        raise ValueError(f"{name} must live in host memory")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def cp_ring_attn_fwd_host(q_host, k_host, v_host, out_host, lse_host, n_shards: int,
+                          causal: bool = True, doc_offsets: Optional[torch.Tensor] = None,
+                          workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """The fused forward from host tensors (bf16 or fp32 [B,S,H,d], lse fp32
+    [B,H,S]; page-locked for overlap): asynchronous on `stream`, whose
+    synchronisation completes out_host and lse_host.  workspace: a uint8
+    device tensor of cp_ring_attn_fwd_host_workspace_bytes bytes."""
+    B, S, H, d = q_host.shape
+    dt = q_host.dtype
+    if dt not in (torch.bfloat16, torch.float32):
+        raise TypeError("q_host must be bf16 or fp32")
+    for t, n in ((q_host, "q_host"), (k_host, "k_host"), (v_host, "v_host"),
+                 (out_host, "out_host")):
+        _need_host(t, n, dt, (B, S, H, d))
+    _need_host(lse_host, "lse_host", torch.float32, (B, H, S))
+    if doc_offsets is not None:
+        _need(doc_offsets, "doc_offsets", torch.int32)
+    if workspace is None:
+        raise ValueError("workspace is required")
+    _need(workspace, "workspace", torch.uint8)
+    name = "cp_ring_attn_fwd_host" if dt == torch.bfloat16 else "cp_ring_attn_fwd_host_f32"
+    _check(name, getattr(lib(), name)(
+        _ptr(q_host), _ptr(k_host), _ptr(v_host), _ptr(out_host), _ptr(lse_host), B, S, H, d,
+        int(n_shards), int(bool(causal)), _ptr(doc_offsets), _ptr(workspace),
+        int(workspace.numel()), _stream(stream)))
+
+
 def cp_ring_attn_fwd_noalloc(q, k, v, out, lse, n_shards: int, causal: bool = True,
                              doc_offsets: Optional[torch.Tensor] = None, stream=None) -> None:
     """cp_ring_attn_fwd without any device allocation by the library, for
@@ -243,7 +294,7 @@ def cp_ring_attn_fwd_noalloc(q, k, v, out, lse, n_shards: int, causal: bool = Tr
 
 def cp_ring_attn_fwd_emulated(q, k, v, out, lse, n_shards: int, causal: bool = True,
                               workspace: Optional[torch.Tensor] = None, stream=None,
-                              copy_stream=None):
+                              copy_stream=None, doc_offsets: Optional[torch.Tensor] = None):
     """The ring with explicit per-rank K/V buffers and copy-engine transfers
     (overlapped on copy_stream, or in order when copy_stream is None).
     Returns the bytes each rank received.  workspace: a uint8 device tensor
@@ -253,6 +304,8 @@ def cp_ring_attn_fwd_emulated(q, k, v, out, lse, n_shards: int, causal: bool = T
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
         _need(t, n, torch.bfloat16, (B, S, H, d))
     _need(lse, "lse", torch.float32, (B, H, S))
+    if doc_offsets is not None:
+        _need(doc_offsets, "doc_offsets", torch.int32)
     need = int(lib().cp_ring_emulated_workspace_bytes(B, S, H, d, int(n_shards)))
     if need < 0:
         raise CpError("cp_ring_emulated_workspace_bytes", STATUS_CODES["CP_ERR_SHAPE"])
@@ -262,7 +315,8 @@ def cp_ring_attn_fwd_emulated(q, k, v, out, lse, n_shards: int, causal: bool = T
     cs = None if copy_stream is None else _stream(copy_stream)
     _check("cp_ring_attn_fwd_emulated", lib().cp_ring_attn_fwd_emulated(
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, H, d, int(n_shards),
-        int(bool(causal)), _ptr(workspace), int(workspace.numel()), _stream(stream), cs, recv))
+        int(bool(causal)), _ptr(doc_offsets), _ptr(workspace), int(workspace.numel()),
+        _stream(stream), cs, recv))
     return list(recv)
 
 

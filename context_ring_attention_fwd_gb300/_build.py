@@ -21,7 +21,8 @@ LIB = os.path.join(LIBDIR, "libcpring.so")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 
 SOURCES = ["attn_sm103.cu", "attn_f32.cu", "merge.cu", "noalloc.cu", "ring_emulation.cpp",
-           "ulysses.cu", "fp8.cu", "attn_bwd_sm103.cu", "api.cpp"]
+           "ulysses.cu", "fp8.cu", "attn_bwd_sm103.cu", "api.cpp", "scratch.cpp",
+           "host_path.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -13,17 +13,8 @@
 namespace {
 
 using cpring::AttnArgs;
-
-bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-cp_status check_shape(int B, int S, int H, int d, int n_shards) {
-  if (B < 1 || S < 1 || H < 1 || d < 1 || n_shards < 1 || n_shards > S) return CP_ERR_SHAPE;
-  if (S % n_shards != 0) return CP_ERR_SHAPE;
-  const long long elems = static_cast<long long>(B) * S * H * d;
-  if (elems > (1LL << 40)) return CP_ERR_SHAPE;
-  if (static_cast<long long>(B) * H > INT_MAX / 4) return CP_ERR_SHAPE;
-  return CP_OK;
-}
+using cpring::aligned;
+using cpring::check_shape;
 
 cp_status check_device() {
   if (cpring::device_cc() != 103) return CP_ERR_DEVICE;
@@ -31,27 +22,27 @@ cp_status check_device() {
 }
 
 // kind: 0 fp32 CUDA-core kernel, 1 bf16 tcgen05 kernel, 2 FP8 tcgen05 kernel.
+// With documents the launch reads the doc-scan word and (tensor-core paths)
+// the cost-ranked slot order from the library's cached per-device scratch.
 cp_status run_attn(AttnArgs a, int kind, cudaStream_t stream) {
   cp_status st = check_device();
   if (st != CP_OK) return st;
-  int32_t* info = nullptr;
-  if (a.doc_offsets) {
-    // the doc-scan word, then (tensor-core paths) the cost-ranked slot order
-    const size_t perm_bytes =
-        kind == 0 ? 0 : 4 * static_cast<size_t>(cpring::slot_count(a.S, a.n_shards, a.q_shard));
-    if (cudaMallocAsync(reinterpret_cast<void**>(&info), 16 + perm_bytes, stream) != cudaSuccess)
-      return CP_ERR_CUDA;
-    if (cpring::launch_doc_scan(a.doc_offsets, a.S, info, stream) != cudaSuccess) {
-      cudaFreeAsync(info, stream);
-      return CP_ERR_CUDA;
-    }
-    a.doc_info = info;
-    if (perm_bytes) a.slot_perm = info + 4;
+  if (!a.doc_offsets) {
+    const cudaError_t e = kind == 2   ? cpring::launch_attn_fp8(a, stream)
+                          : kind == 1 ? cpring::launch_attn_bf16(a, stream)
+                                      : cpring::launch_attn_f32(a, stream);
+    return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
   }
+  cpring::ScratchLease lease(cpring::doc_scratch_bytes(a.S, a.n_shards, a.q_shard, kind != 0),
+                             stream);
+  if (!lease.ok()) return CP_ERR_CUDA;
+  int32_t* info = static_cast<int32_t*>(lease.get());
+  if (cpring::launch_doc_scan(a.doc_offsets, a.S, info, stream) != cudaSuccess) return CP_ERR_CUDA;
+  a.doc_info = info;
+  if (kind != 0) a.slot_perm = info + 4;
   const cudaError_t e = kind == 2   ? cpring::launch_attn_fp8(a, stream)
                         : kind == 1 ? cpring::launch_attn_bf16(a, stream)
                                     : cpring::launch_attn_f32(a, stream);
-  if (info) cudaFreeAsync(info, stream);
   return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
 
@@ -357,19 +348,14 @@ cp_status cp_ring_schedule_device(int S, int n_shards, int causal, const int32_t
   a.n_shards = n_shards;
   a.causal = causal;
   a.doc_offsets = doc_offsets;
-  int32_t* info = nullptr;
-  if (doc_offsets) {
-    if (cudaMallocAsync(reinterpret_cast<void**>(&info), 16, stream) != cudaSuccess)
-      return CP_ERR_CUDA;
-    if (cpring::launch_doc_scan(doc_offsets, S, info, stream) != cudaSuccess) {
-      cudaFreeAsync(info, stream);
-      return CP_ERR_CUDA;
-    }
-    a.doc_info = info;
-  }
-  const cudaError_t e = cpring::launch_schedule_probe(a, ranges, stream);
-  if (info) cudaFreeAsync(info, stream);
-  return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+  if (!doc_offsets)
+    return cpring::launch_schedule_probe(a, ranges, stream) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+  cpring::ScratchLease lease(cpring::doc_scratch_bytes(S, n_shards, -1, false), stream);
+  if (!lease.ok()) return CP_ERR_CUDA;
+  int32_t* info = static_cast<int32_t*>(lease.get());
+  if (cpring::launch_doc_scan(doc_offsets, S, info, stream) != cudaSuccess) return CP_ERR_CUDA;
+  a.doc_info = info;
+  return cpring::launch_schedule_probe(a, ranges, stream) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
 
 cp_status cp_ring_traffic(int64_t B, int64_t S, int64_t H, int64_t d, int dtype_bytes,

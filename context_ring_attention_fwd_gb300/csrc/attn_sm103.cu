@@ -1035,7 +1035,6 @@ std::atomic<unsigned long long> g_wait_limit_ns{kTimeoutNs};
 // first, the order used without documents), so the snake deal balances the
 // CTAs.  Every (b, h) shares the layout, so one block ranks the slots of
 // (b, h) = (0, 0); O(slots^2) compares, used up to kMaxRankedSlots.
-constexpr int kMaxRankedSlots = 8192;
 
 __global__ void __launch_bounds__(1024) slot_order_kernel(KParams p, int32_t* __restrict__ perm) {
   __shared__ int cost[kMaxRankedSlots];

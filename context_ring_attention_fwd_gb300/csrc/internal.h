@@ -48,6 +48,57 @@ inline int slot_count(int S, int n_shards, int q_shard) {
   return (q_shard < 0 ? n_shards : 1) * ((L + 255) / 256);
 }
 
+// Launches with documents rank their slots by cost (slot_order_kernel) when
+// they hold at most this many; larger ones deal by position.
+constexpr int kMaxRankedSlots = 8192;
+
+// Bytes of scratch a forward launch with documents uses: the doc-scan word
+// (16 bytes), then the cost-ranked slot order (tensor-core paths only).
+inline size_t doc_scratch_bytes(int S, int n_shards, int q_shard, bool ranked) {
+  return 16 + (ranked ? 4 * static_cast<size_t>(slot_count(S, n_shards, q_shard)) : 0);
+}
+
+inline bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+// The shape checks every forward entry point shares: sizes >= 1, an equal
+// split into n_shards, at most 2^40 elements and B * H small enough for the
+// kernels' int work counters.
+inline cp_status check_shape(int B, int S, int H, int d, int n_shards) {
+  if (B < 1 || S < 1 || H < 1 || d < 1 || n_shards < 1 || n_shards > S) return CP_ERR_SHAPE;
+  if (S % n_shards != 0) return CP_ERR_SHAPE;
+  const long long elems = static_cast<long long>(B) * S * H * d;
+  if (elems > (1LL << 40)) return CP_ERR_SHAPE;
+  if (static_cast<long long>(B) * H > 0x7fffffff / 4) return CP_ERR_SHAPE;
+  return CP_OK;
+}
+
+// The library's cached per-device scratch (the doc-scan word and the
+// cost-ranked slot order of launches with documents).  One buffer per device
+// grows on demand with stream-ordered allocation (cudaMallocAsync /
+// cudaFreeAsync on the caller's stream) and is kept for the process's life.
+// A lease holds the device's lock from construction to destruction, so host
+// threads take turns; its constructor orders `stream` after the work of the
+// previous lease when that ran on another stream, and its destructor records
+// the point after which the next lease may reuse the buffer.  Every launch
+// that reads the buffer must be enqueued on `stream` while the lease lives.
+class ScratchLease {
+ public:
+  ScratchLease(size_t bytes, cudaStream_t stream);
+  ~ScratchLease();
+  ScratchLease(const ScratchLease&) = delete;
+  ScratchLease& operator=(const ScratchLease&) = delete;
+  void* get() const { return ptr_; }
+  bool ok() const { return ok_; }
+
+ private:
+  int dev_ = -1;
+  void* ptr_ = nullptr;
+  bool ok_ = false;
+  cudaStream_t stream_ = nullptr;
+};
+
 // The backward: gradients of sum(out * dout) for the forward's out and lse.
 struct BwdArgs {
   const void* q;

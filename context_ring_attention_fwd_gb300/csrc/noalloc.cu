@@ -1,10 +1,11 @@
 // cp_ring_attn_fwd_noalloc: the fused bf16 forward without any device
 // allocation by the library.
 //
-// Why it exists.  cp_ring_attn_fwd takes a 16-byte stream-ordered allocation
-// (cudaMallocAsync) for every call that passes doc_offsets.  Some callers
-// cannot let a library allocate: serving processes that hand almost all of the
-// GPU's memory to their own pool at start-up and forbid any later
+// Why it exists.  cp_ring_attn_fwd keeps a small cached scratch per device
+// for calls that pass doc_offsets, and allocates it (cudaMallocAsync) the
+// first time and whenever a call needs more than it holds.  Some callers
+// cannot let a library allocate at all: serving processes that hand almost
+// all of the GPU's memory to their own pool at start-up and forbid any later
 // cudaMalloc/cudaMallocAsync (an allocation there can fail, or fragment or
 // shrink the pool under load), and latency-critical loops that must never
 // enter the driver's allocator.  This entry point serves them: it computes
@@ -12,24 +13,28 @@
 // device array compiled into the library.
 //
 // The scratch.  g_noalloc_scratch below is a file-scope device array of
-// kScratchInts int32 (262,208 bytes).  Every GPU that loads the library holds
-// it until the process exits.  It stores the document count (header word 0)
-// and a validated copy of the document boundaries (from word kHeaderInts on),
-// which the attention kernel then reads.  The copy holds at most
-// kMaxDocs + 1 boundaries, so at most kMaxDocs = 65,535 documents per call.
+// kScratchInts int32 (295,168 bytes).  Every GPU that loads the library holds
+// it until the process exits.  It stores the document count (header word 0),
+// a validated copy of the document boundaries (from word kHeaderInts on),
+// which the attention kernel then reads, and the cost-ranked order of the
+// launch's work slots (the last kMaxRankedSlots words), the same order
+// cp_ring_attn_fwd deals by.  The copy holds at most kMaxDocs + 1
+// boundaries, so at most kMaxDocs = 65,535 documents per call.
 //
 // Host code must never hand the array's name to a kernel: on the host that
 // name is only a stand-in, not a device address.  The device address comes
 // from cudaGetSymbolAddress, called once per device with that device
 // current, the first time this entry point runs on it.  Make that first call
-// on each device before any stream capture.
+// on each device before any stream capture.  The address is cached for the
+// life of the process, so the library must not be used across
+// cudaDeviceReset.
 //
 // Sharing.  All calls on a device share the one array, and it keeps what the
-// last call wrote.  Each call rewrites the header and the boundary copy
-// before its attention kernel reads them (stream order), so nothing from an
-// earlier call is ever read and nothing needs clearing to zero.  Calls whose
-// work overlaps on the GPU (different streams, no ordering between them)
-// race on the array and must not be issued.
+// last call wrote.  Each call rewrites the header, the boundary copy and the
+// slot order before its attention kernel reads them (stream order), so
+// nothing from an earlier call is ever read and nothing needs clearing to
+// zero.  Calls whose work overlaps on the GPU (different streams, no ordering
+// between them) race on the array and must not be issued.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -42,9 +47,11 @@ namespace {
 
 constexpr int kHeaderInts = 64;      // word 0: document count, or -1
 constexpr int kMaxDocs = 65535;      // boundaries copied: at most kMaxDocs + 1
-constexpr int kScratchInts = kHeaderInts + kMaxDocs + 1;
+constexpr int kPermOff = kHeaderInts + kMaxDocs + 1;  // the slot order
+constexpr int kScratchInts = kPermOff + kMaxRankedSlots;
 
 static __device__ __align__(256) int32_t g_noalloc_scratch[kScratchInts];
+static_assert(sizeof(g_noalloc_scratch) == 295168, "the documented size of the fixed scratch");
 
 // Validate doc_offsets (0 = o_0 < o_1 < ... < o_n = S, read up to the first
 // entry equal to S and never past it) and copy it into the scratch.  Writes
@@ -100,8 +107,6 @@ int32_t* scratch_address() {
   return addr[dev];
 }
 
-bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
 }  // namespace
 }  // namespace cpring
 
@@ -112,9 +117,8 @@ extern "C" cp_status cp_ring_attn_fwd_noalloc(const void* q, const void* k, cons
   cpring::TraceRange trace_("cp_ring_attn_fwd_noalloc");
   using namespace cpring;
   if (!q || !k || !v || !out || !lse) return CP_ERR_NULL;
-  if (B < 1 || S < 1 || H < 1 || d < 1 || n_shards < 1 || n_shards > S || S % n_shards != 0)
-    return CP_ERR_SHAPE;
-  if (static_cast<long long>(B) * S * H * d > (1LL << 40)) return CP_ERR_SHAPE;
+  const cp_status st = check_shape(B, S, H, d, n_shards);
+  if (st != CP_OK) return st;
   if (d != 64 && d != 128) return CP_ERR_UNSUPPORTED;
   if (causal != 0 && causal != 1) return CP_ERR_SHAPE;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
@@ -145,6 +149,7 @@ extern "C" cp_status cp_ring_attn_fwd_noalloc(const void* q, const void* k, cons
     if (cudaGetLastError() != cudaSuccess) return CP_ERR_CUDA;
     a.doc_offsets = scratch + kHeaderInts;  // the validated copy
     a.doc_info = scratch;
+    a.slot_perm = scratch + kPermOff;        // written by the launch's slot ranking
   }
   return launch_attn_bf16(a, stream) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }

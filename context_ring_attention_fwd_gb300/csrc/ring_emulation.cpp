@@ -18,10 +18,12 @@
 // a slot is overwritten only after the step that read it has finished and
 // read only after its copy has landed.  Without a copy stream the copies run
 // in order on the compute stream (no overlap), which measures what the
-// overlap hides.
+// overlap hides.  With documents every step applies the document mask, so
+// packed sequences keep their boundaries across the ranks' blocks.
 #include <cuda_runtime_api.h>
 
 #include <cstdint>
+#include <optional>
 #include <vector>
 
 #include "internal.h"
@@ -65,20 +67,20 @@ extern "C" int64_t cp_ring_emulated_workspace_bytes(int B, int S, int H, int d, 
 
 extern "C" cp_status cp_ring_attn_fwd_emulated(const void* q, const void* k, const void* v,
                                                void* out, float* lse, int B, int S, int H, int d,
-                                               int n_shards, int causal, void* workspace,
+                                               int n_shards, int causal,
+                                               const int32_t* doc_offsets, void* workspace,
                                                int64_t workspace_bytes, cudaStream_t stream,
                                                cudaStream_t copy_stream,
                                                int64_t* recv_bytes_per_rank) {
   cpring::TraceRange trace_("cp_ring_attn_fwd_emulated");
+  using cpring::aligned;
   if (!q || !k || !v || !out || !lse || !workspace) return CP_ERR_NULL;
-  if (B < 1 || S < 1 || H < 1 || n_shards < 1 || n_shards > S || S % n_shards != 0)
-    return CP_ERR_SHAPE;
+  const cp_status shape = cpring::check_shape(B, S, H, d, n_shards);
+  if (shape != CP_OK) return shape;
   if (causal != 0 && causal != 1) return CP_ERR_SHAPE;
   if (d != 64 && d != 128) return CP_ERR_UNSUPPORTED;
-  if (static_cast<long long>(B) * S * H * d > (1LL << 40)) return CP_ERR_SHAPE;
-  auto aligned = [](const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; };
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
-      !aligned(lse, 4) || !aligned(workspace, 256))
+      !aligned(lse, 4) || !aligned(workspace, 256) || !aligned(doc_offsets, 4))
     return CP_ERR_ALIGN;
   const int N = n_shards;
   const Plan pl = make_plan(B, S, H, d, N);
@@ -125,6 +127,22 @@ extern "C" cp_status cp_ring_attn_fwd_emulated(const void* q, const void* k, con
   auto chk = [&](cudaError_t e) {
     if (err == cudaSuccess && e != cudaSuccess) err = e;
   };
+  // Documents ("Context Parallel", section 常见失败模式: packed samples keep
+  // their boundaries across shards): every step masks by document as the
+  // fused kernel does; the doc-scan word and the step launches' slot order
+  // live in the library's cached scratch for the rest of the call.
+  std::optional<cpring::ScratchLease> lease;
+  int32_t* info = nullptr;
+  if (doc_offsets) {
+    lease.emplace(cpring::doc_scratch_bytes(S, N, 0, true), stream);
+    if (!lease->ok()) {
+      cudaEventDestroy(ev_copied);
+      cudaEventDestroy(ev_computed);
+      return CP_ERR_CUDA;
+    }
+    info = static_cast<int32_t*>(lease->get());
+    chk(cpring::launch_doc_scan(doc_offsets, S, info, stream));
+  }
   // Step 0: every rank holds its own block (local placement, not ring traffic).
   for (int i = 0; i < N; ++i) {
     chk(copy_in(kv_slot(i, 0, 0), k, i, stream));
@@ -161,6 +179,9 @@ extern "C" cp_status cp_ring_attn_fwd_emulated(const void* q, const void* k, con
       a.B = B; a.S = S; a.H = H; a.d = d; a.n_shards = N;
       a.q_shard = i; a.k_shard = j;
       a.causal = causal;
+      a.doc_offsets = doc_offsets;
+      a.doc_info = info;
+      a.slot_perm = info ? info + 4 : nullptr;
       a.kv_rows = L;
       a.kv_row0 = j * L;
       if (!started[i]) {

@@ -17,6 +17,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <optional>
 
 #include "internal.h"
 
@@ -129,6 +130,13 @@ extern "C" cp_status cp_ulysses_attn_fwd(const void* q, const void* k, const voi
 
   int32_t* info = nullptr;
   cudaError_t e = cudaSuccess;
+  // with documents: the doc-scan word and the attention launch's slot order,
+  // in the library's cached scratch for the rest of this call
+  std::optional<ScratchLease> lease;
+  if (doc_offsets) {
+    lease.emplace(doc_scratch_bytes(S, 1, -1, true), stream);
+    if (!lease->ok()) return CP_ERR_CUDA;
+  }
   auto chk = [&](cudaError_t x) {
     if (e == cudaSuccess && x != cudaSuccess) e = x;
   };
@@ -137,10 +145,7 @@ extern "C" cp_status cp_ulysses_attn_fwd(const void* q, const void* k, const voi
   chk(permute(k, kh, rows, N, chunk, true, stream));
   chk(permute(v, vh, rows, N, chunk, true, stream));
   if (doc_offsets) {
-    // the doc-scan word, then the cost-ranked slot order of the attention launch
-    const size_t perm_bytes = 4 * static_cast<size_t>(slot_count(S, 1, -1));
-    if (cudaMallocAsync(reinterpret_cast<void**>(&info), 16 + perm_bytes, stream) != cudaSuccess)
-      return CP_ERR_CUDA;
+    info = static_cast<int32_t*>(lease->get());
     chk(launch_doc_scan(doc_offsets, S, info, stream));
   }
   // step 2: rank g attends over the whole sequence for its H/N heads.  The
@@ -170,7 +175,6 @@ extern "C" cp_status cp_ulysses_attn_fwd(const void* q, const void* k, const voi
                           lh + static_cast<int64_t>(g) * B * Hg * S,
                           static_cast<size_t>(Hg) * S * 4, static_cast<size_t>(Hg) * S * 4, B,
                           cudaMemcpyDeviceToDevice, stream));
-  if (info) cudaFreeAsync(info, stream);
   if (a2a_bytes) {
     // every rank keeps 1/N of its shard and exchanges the rest, both ways:
     // Q, K, V before the attention and O after it, per rank sent + received

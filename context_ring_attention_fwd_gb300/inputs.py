@@ -40,6 +40,10 @@ class Workload:
     def torch_dtype(self):
         return torch.float32 if self.dtype == "f32" else torch.bfloat16
 
+    @property
+    def elem_bytes(self) -> int:
+        return 4 if self.dtype == "f32" else 2
+
     def describe(self) -> str:
         docs = ", packed documents" if self.packed_docs else ""
         kind = "causal" if self.causal else "non-causal"

@@ -31,8 +31,17 @@
  *              only if both lie in the same document.
  *  Ownership   the caller owns every buffer and the stream.  Calls are
  *              asynchronous on `stream`; only cp_get_last_status
- *              synchronises.  When doc_offsets is given the library takes a
- *              16-byte stream-ordered scratch allocation for the call.
+ *              synchronises.  When doc_offsets is given the call reads its
+ *              doc-scan word and work order from a small scratch that the
+ *              library caches per device: it is allocated in stream order
+ *              (cudaMallocAsync on `stream`) on first use and whenever a
+ *              call needs more than it holds (4 bytes per 256 query rows of
+ *              the launch, plus 16), and kept until the process exits.  A
+ *              call on another stream than the previous user's first waits
+ *              for that user's work.  cp_ring_attn_fwd_noalloc allocates
+ *              nothing.  State cached per device (this scratch, the error
+ *              word's address, the host path's copy streams) does not
+ *              survive cudaDeviceReset: do not use the library across one.
  *  Errors      arguments are checked on the host before any launch; a
  *              violation returns a negative cp_status and launches nothing.
  *              Faults found on the device (malformed doc_offsets, a wait
@@ -110,28 +119,78 @@ cp_status cp_ring_attn_fwd_rank(const void* q, const void* k, const void* v, voi
  * memory.  The pages have no counterpart: this is a deployment variant of the
  * fused forward above, with the same arguments, layouts and result.
  *
- * cp_ring_attn_fwd allocates 16 bytes of stream-ordered scratch for every call
- * that passes doc_offsets.  Processes that give nearly all GPU memory to their
+ * cp_ring_attn_fwd allocates its small per-device scratch (stream-ordered
+ * cudaMallocAsync) the first time a call passes doc_offsets and whenever a call
+ * needs more than it holds.  Processes that give nearly all GPU memory to their
  * own pool at start-up and forbid later cudaMalloc/cudaMallocAsync, and loops
  * that must never enter the driver's allocator, call this entry point instead:
  * it allocates nothing and keeps its scratch in a fixed device array built into
- * the library (262,208 bytes per GPU that loads the library, held until the
- * process exits).
+ * the library (295,168 bytes per GPU that loads the library, held until the
+ * process exits).  It deals the work in the same cost-ranked order.
  *
  * Limit: doc_offsets may describe at most 65,535 documents.  A larger array
  * is rejected on the device: nothing is written, and cp_get_last_status
- * reports CP_ERR_SCRATCH.  Host-side checks are those of cp_ring_attn_fwd.
+ * reports CP_ERR_SCRATCH.  A malformed one is rejected the same way with
+ * CP_ERR_DOC_OFFSETS.  Host-side checks are those of cp_ring_attn_fwd.
  *
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  All calls share the array and it keeps the last
- * call's contents; every call rewrites what it reads, so nothing needs
- * clearing.  Calls whose GPU work can overlap (unordered streams) race on the
- * array and must not be issued.
+ * before any stream capture.  The address is cached for the process's life:
+ * do not use the library across cudaDeviceReset.  All calls share the array
+ * and it keeps the last call's contents; every call rewrites what it reads,
+ * so nothing needs clearing.  Calls whose GPU work can overlap (unordered
+ * streams) race on the array and must not be issued.
  */
 cp_status cp_ring_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out,
                                    float* lse, int B, int S, int H, int d, int n_shards,
                                    int causal, const int32_t* doc_offsets, cudaStream_t stream);
+
+/*
+ * cp_ring_attn_fwd end to end from HOST buffers ("上下文並行（Context
+ * Parallelism, CP）", section 線上 Softmax: a GPU computes on the block it holds
+ * while the next one is sent and received, asynchronously and side by side;
+ * section 因果掩碼的特殊處理: under causality rank i needs only shards 0..i).
+ * Shard i's Q, K, V are copied to the device on a copy stream of the
+ * library's, rank i starts once the shards it reads have landed (0..i when
+ * causal, all of them otherwise), and its rows of out and lse are copied back
+ * on a second copy stream while later ranks compute.  The result equals
+ * cp_ring_attn_fwd's bit for bit.
+ *
+ *  q_host, k_host, v_host  host, bf16 [B,S,H,d], read.
+ *  out_host   host, bf16 [B,S,H,d], written.
+ *  lse_host   host, fp32 [B,H,S], written.
+ *             Host buffers should be page-locked (cudaHostAlloc /
+ *             cudaHostRegister) for the copies to overlap the kernels;
+ *             pageable memory gives the same result with serialised copies.
+ *  doc_offsets  NULL or DEVICE int32, as for cp_ring_attn_fwd.
+ *  workspace  device, >= cp_ring_attn_fwd_host_workspace_bytes(B, S, H, d,
+ *             n_shards, 2) bytes, 256-byte aligned, owned by the caller: the
+ *             device copies of q, k, v, out and lse (its layout is private;
+ *             contents undefined after the call).
+ *  stream     the caller's stream.  The call is asynchronous: it returns
+ *             once everything is enqueued, and `stream` then waits for the
+ *             last copy back, so after synchronising `stream` the host
+ *             outputs are complete.  The host inputs must stay unchanged and
+ *             the host outputs unread until then.
+ *  Shapes, masks, d and errors as cp_ring_attn_fwd; workspace too small:
+ *  CP_ERR_BUFFER.  With doc_offsets the call uses the cached scratch that
+ *  cp_ring_attn_fwd uses.  The copy streams and their events are created on
+ *  the first call on each device and kept; a per-device lock is held while a
+ *  call enqueues, so concurrent host threads take turns.
+ */
+int64_t cp_ring_attn_fwd_host_workspace_bytes(int B, int S, int H, int d, int n_shards,
+                                              int elem_bytes /* 2 bf16, 4 fp32 */);
+cp_status cp_ring_attn_fwd_host(const void* q_host, const void* k_host, const void* v_host,
+                                void* out_host, float* lse_host, int B, int S, int H, int d,
+                                int n_shards, int causal, const int32_t* doc_offsets,
+                                void* workspace, int64_t workspace_bytes, cudaStream_t stream);
+/* The same with fp32 host buffers and the fp32 path (d in [1, 128];
+ * workspace from cp_ring_attn_fwd_host_workspace_bytes(..., 4)). */
+cp_status cp_ring_attn_fwd_host_f32(const float* q_host, const float* k_host,
+                                    const float* v_host, float* out_host, float* lse_host, int B,
+                                    int S, int H, int d, int n_shards, int causal,
+                                    const int32_t* doc_offsets, void* workspace,
+                                    int64_t workspace_bytes, cudaStream_t stream);
 
 /* Same operation in true fp32 (CUDA-core FFMA, no TF32): q, k, v, out are
  * float [B,S,H,d]; d in [1, 128]; 4-byte alignment suffices. */
@@ -221,7 +280,7 @@ cp_status cp_ring_schedule(int S, int n_shards, int tile_q, int tile_k, int caus
  * are needed); it exists so tests can check the device schedule.
  *  doc_offsets  NULL or device int32 (as cp_ring_attn_fwd).
  *  ranges       device int32 [n_shards * ceil(L/128) * 2], written.
- * Takes a 16-byte stream-ordered scratch allocation when doc_offsets is set.
+ * With doc_offsets it uses the library's cached per-device scratch.
  */
 cp_status cp_ring_schedule_device(int S, int n_shards, int causal, const int32_t* doc_offsets,
                                   int32_t* ranges, cudaStream_t stream);
@@ -259,7 +318,8 @@ const char* cp_status_string(cp_status status);
  * of rank (i - t) mod N, runs cp_ring_step on it and merges the partial, while
  * the copy engine moves each held block into the next rank's other slot for
  * step t + 1.  Same arguments and result as cp_ring_attn_fwd (bf16, d 64 or
- * 128, no doc_offsets), plus:
+ * 128; doc_offsets NULL or device int32, every step masking by document, the
+ * doc-scan word in the library's cached scratch), plus:
  *  workspace        device, >= cp_ring_emulated_workspace_bytes(...) bytes,
  *                   256-byte aligned; owned by the caller; contents undefined
  *                   after the call.
@@ -273,7 +333,8 @@ const char* cp_status_string(cp_status status);
 int64_t cp_ring_emulated_workspace_bytes(int B, int S, int H, int d, int n_shards);
 cp_status cp_ring_attn_fwd_emulated(const void* q, const void* k, const void* v, void* out,
                                     float* lse, int B, int S, int H, int d, int n_shards,
-                                    int causal, void* workspace, int64_t workspace_bytes,
+                                    int causal, const int32_t* doc_offsets, void* workspace,
+                                    int64_t workspace_bytes,
                                     cudaStream_t stream, cudaStream_t copy_stream,
                                     int64_t* recv_bytes_per_rank);
 

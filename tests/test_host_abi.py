@@ -52,11 +52,14 @@ def test_ring_emulation_workspace_and_checks(lib):
     assert n >= 4 * 2 * 2 * blk * 2 + 5 * blk * 4
     assert pkg.cp_ring_emulated_workspace_bytes(2, 1000, 2, 128, 3) == -1
     f = lib.cp_ring_attn_fwd_emulated
-    assert f(None, FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 128, 4, 1, FAKE, 1 << 30, None, None,
+    assert f(None, FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 128, 4, 1, None, FAKE, 1 << 30, None, None,
              None) == -1
-    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 96, 4, 1, FAKE, 1 << 30, None, None,
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 96, 4, 1, None, FAKE, 1 << 30, None, None,
              None) == -3
-    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 128, 4, 1, FAKE, 16, None, None, None) == -6
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 128, 4, 1, None, FAKE, 16, None, None,
+             None) == -6
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 128, 4, 1, ctypes.c_void_p(0x10002), FAKE,
+             1 << 30, None, None, None) == -4
 
 
 def test_ulysses_checks(lib):

@@ -4,11 +4,14 @@ forbids later cudaMalloc/cudaMallocAsync, or loops that must stay out of the
 driver's allocator).  It keeps its scratch in a fixed array built into the
 library instead.
 
-The GPU test calls it through the C ABI and checks it against
-cp_ring_attn_fwd on two calls in a row with different document layouts (the
-second call must not see anything left by the first), then checks that more
-documents than the fixed array holds are rejected.  This file is collected
-last so that a run stopping at its first failure has run everything else.
+The GPU tests call it through the C ABI and require it to equal
+cp_ring_attn_fwd bit for bit (the same kernel computes the same work items;
+only where the scratch lives differs), on calls in a row with different
+document layouts and shard counts (a later call must not see anything left
+by an earlier one), and once against the oracle.  Malformed and oversized
+document arrays are rejected on the device and leave the outputs untouched.
+This file is collected last so that a run stopping at its first failure has
+run everything else.
 """
 import ctypes
 import os
@@ -19,6 +22,7 @@ import torch
 
 import context_ring_attention_fwd_gb300 as pkg
 from context_ring_attention_fwd_gb300 import inputs
+from oracle import ref
 
 BF16_MAX, BF16_MEAN = 2e-2, 2e-3
 FAKE = ctypes.c_void_p(0x10000)
@@ -38,6 +42,10 @@ def test_noalloc_rejects_bad_arguments_on_host():
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 96, 4, 1, None, None) == -3
     assert f(ctypes.c_void_p(0x10002), FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 128, 4, 1, None,
              None) == -4
+    # the shape checks are cp_ring_attn_fwd's: B * H beyond the kernels' work counters
+    g = _lib().cp_ring_attn_fwd
+    for fn in (f, g):
+        assert fn(FAKE, FAKE, FAKE, FAKE, FAKE, 65536, 1, 16384, 64, 1, 1, None, None) == -2
 
 
 def _call_noalloc(lib, q, k, v, out, lse, N, causal, docs_t):
@@ -49,37 +57,63 @@ def _call_noalloc(lib, q, k, v, out, lse, N, causal, docs_t):
     assert st == 0, pkg.STATUS_NAMES.get(st, st)
 
 
-@pytest.mark.gpu
-def test_noalloc_matches_fused_forward_two_calls_in_a_row():
+def _gpu():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     lib = _lib()
     torch.cuda.set_device(0)
     pkg.cp_get_last_status()                     # start from a clear error word
-    B, S, H, d, N = 1, 2048, 4, 128, 4
+    return lib
+
+
+@pytest.mark.gpu
+def test_noalloc_equals_fused_forward_on_calls_in_a_row():
+    lib = _gpu()
+    B, S, H, d = 1, 2048, 4, 128
     q, k, v = (t.cuda() for t in inputs.make_qkv(B, S, H, d, seed=31, dtype=torch.bfloat16))
-    layouts = [[0, 300, 301, 777, 1500, 2048], [0, 1024, 2048], None]
-    for docs in layouts:
+    calls = [([0, 300, 301, 777, 1500, 2048], 4, True), ([0, 1024, 2048], 8, True),
+             (None, 4, True), ([0, 5, 900, 2048], 1, False), ([0, 2047, 2048], 8, False)]
+    for n, (docs, N, causal) in enumerate(calls):
         docs_t = pkg.doc_offsets_tensor(docs, q.device)
         want_o = torch.empty_like(q)
         want_l = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
-        pkg.cp_ring_attn_fwd(q, k, v, want_o, want_l, N, True, docs_t)
+        pkg.cp_ring_attn_fwd(q, k, v, want_o, want_l, N, causal, docs_t)
+        out = torch.full_like(q, 5.0)
+        lse = torch.full((B, H, S), 5.0, dtype=torch.float32, device=q.device)
+        _call_noalloc(lib, q, k, v, out, lse, N, causal, docs_t)
+        assert pkg.cp_get_last_status() == 0
+        assert torch.equal(out, want_o) and torch.equal(lse, want_l), (docs, N, causal)
+        if n == 0:
+            wo, wl = ref.attention(q.float().cpu().numpy(), k.float().cpu().numpy(),
+                                   v.float().cpu().numpy(), causal, docs)
+            e = np.abs(out.float().cpu().numpy() - wo)
+            assert e.max() <= BF16_MAX and e.mean() <= BF16_MEAN
+            assert np.abs(lse.cpu().numpy() - wl).max() <= BF16_MAX
+
+
+@pytest.mark.gpu
+def test_noalloc_rejects_malformed_documents_and_keeps_outputs():
+    lib = _gpu()
+    B, S, H, d, N = 1, 2048, 2, 128, 4
+    q, k, v = (t.cuda() for t in inputs.make_qkv(B, S, H, d, seed=33, dtype=torch.bfloat16))
+    for docs in ([0, 300, 300, 2048], [0, 700, 600, 2048], [1, 700, 2048], [0, 700, 4096]):
+        docs_t = pkg.doc_offsets_tensor(docs, q.device)
         out = torch.full_like(q, 5.0)
         lse = torch.full((B, H, S), 5.0, dtype=torch.float32, device=q.device)
         _call_noalloc(lib, q, k, v, out, lse, N, True, docs_t)
-        assert pkg.cp_get_last_status() == 0
-        e = (out.float() - want_o.float()).abs()
-        assert e.max().item() <= BF16_MAX and e.mean().item() <= BF16_MEAN, docs
-        assert (lse - want_l).abs().max().item() <= BF16_MAX, docs
+        assert pkg.cp_get_last_status() == pkg.STATUS_CODES["CP_ERR_DOC_OFFSETS"], docs
+        assert torch.all(out == 5.0) and torch.all(lse == 5.0), docs
+    # the next well-formed call is unaffected
+    docs_t = pkg.doc_offsets_tensor([0, 300, 2048], q.device)
+    want_o, want_l = pkg.ring_attn_fwd(q, k, v, N, True, [0, 300, 2048])
+    _call_noalloc(lib, q, k, v, out, lse, N, True, docs_t)
+    assert pkg.cp_get_last_status() == 0
+    assert torch.equal(out, want_o) and torch.equal(lse, want_l)
 
 
 @pytest.mark.gpu
 def test_noalloc_rejects_more_documents_than_its_scratch_holds():
-    if not torch.cuda.is_available():
-        pytest.skip("no CUDA device")
-    lib = _lib()
-    torch.cuda.set_device(0)
-    pkg.cp_get_last_status()
+    lib = _gpu()
     B, S, H, d, N = 1, 65540, 1, 64, 1
     q, k, v = (t.cuda() for t in inputs.make_qkv(B, S, H, d, seed=32, dtype=torch.bfloat16))
     docs = list(range(0, 65537)) + [S]           # 65,537 documents: two more than the limit
@@ -89,12 +123,17 @@ def test_noalloc_rejects_more_documents_than_its_scratch_holds():
     _call_noalloc(lib, q, k, v, out, lse, N, True, docs_t)
     assert pkg.cp_get_last_status() == pkg.STATUS_CODES["CP_ERR_SCRATCH"]
     assert torch.all(out == 5.0) and torch.all(lse == 5.0)
+    # exactly the limit is accepted
+    docs = list(range(0, 65535)) + [S]           # 65,535 documents
+    docs_t = pkg.doc_offsets_tensor(docs, q.device)
+    want_o, want_l = pkg.ring_attn_fwd(q, k, v, N, True, docs)
+    _call_noalloc(lib, q, k, v, out, lse, N, True, docs_t)
+    assert pkg.cp_get_last_status() == 0
+    assert torch.equal(out, want_o) and torch.equal(lse, want_l)
     # the array is reusable right after a rejected call
     docs = [0, 40000, S]
     docs_t = pkg.doc_offsets_tensor(docs, q.device)
     want_o, want_l = pkg.ring_attn_fwd(q, k, v, N, True, docs)
     _call_noalloc(lib, q, k, v, out, lse, N, True, docs_t)
     assert pkg.cp_get_last_status() == 0
-    e = (out.float() - want_o.float()).abs()
-    assert e.max().item() <= BF16_MAX and e.mean().item() <= BF16_MEAN
-    assert np.isfinite(lse.cpu().numpy()).all()
+    assert torch.equal(out, want_o) and torch.equal(lse, want_l)
