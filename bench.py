@@ -440,15 +440,18 @@ def run_ours(args, w, rank, world, local):
         barrier(world, dev)
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
+        marks = [t0]
         for _ in range(args.e2e_steps):
             pkg.ring_attn_fwd_host(hq, hk, hv, w.n_shards, w.causal, docs, buffers=bufs)
-        dt = time.perf_counter() - t0
+            marks.append(time.perf_counter())
+        dt = marks[-1] - t0
         dt = max_over_ranks(dt, world, dev)
         elem = hq.numel() * hq.element_size()
         e2e = {"value": flops * world * args.e2e_steps / dt / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": 3 * elem,
                "d2h_bytes_per_step": elem + w.B * w.H * w.S * 4,
                "ms_per_step": 1e3 * dt / args.e2e_steps, "steps": args.e2e_steps,
+               "ms_each": [1e3 * (b - a) for a, b in zip(marks[:-1], marks[1:])],
                "entry_point": "cp_ring_attn_fwd_host"}
         if docs is not None:
             e2e["doc_offsets"] = "resident on the device, as the C ABI takes them"

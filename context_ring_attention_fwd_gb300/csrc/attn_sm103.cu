@@ -37,12 +37,15 @@
 //
 // FP8 form (ring_attn_fp8_kernel).  Q and K arrive as E4M3 [B, S, H, d] and
 // V as E4M3 [B, H, d, S] (keys contiguous, so V is K-major for the PV MMA),
-// each with one fp32 descale per (b, h).  Both MMAs run as kind::f8f6f4; the
-// softmax writes P as E4M3 (four per TMEM column) and always keeps P <= 2^8
-// (the row max is taken every tile), inside E4M3's range of 448.  The
-// descales enter as the score scale (q_descale * k_descale) and the output
-// scale (v_descale).  The communication-volume note of the first page ties
-// the bytes moved to FP8 transfer; this form halves the K/V bytes.
+// each with one fp32 descale per (b, h).  Both MMAs run as kind::f8f6f4 with
+// both operands in shared memory: the softmax writes P as E4M3 into one of
+// two shared-memory buffers of its query tile and keeps every P <= 2^8,
+// inside E4M3's range of 448.  Because P does not overwrite S in TMEM, the
+// next key tile's S is computed while the softmax still works on the
+// current one.  The descales enter as the score scale (q_descale *
+// k_descale) and the output scale (v_descale).  The communication-volume
+// note of the first page ties the bytes moved to FP8 transfer; this form
+// halves the K/V bytes.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -52,6 +55,7 @@
 #include <cstdio>
 #include <atomic>
 #include <mutex>
+#include <type_traits>
 
 #include "attn_common.cuh"
 #include "internal.h"
@@ -79,6 +83,9 @@ constexpr float kRescaleLog2 = 8.0f;
 //                          this many rounds of the grid (see head_group) ...
 //  CPRING_GROUP_MIN_ROUNDS ... when the launch has at least this many rounds;
 //                          shorter launches deal every item from one pool.
+//  CPRING_GROUP_DOCS       launches with documents group heads too.
+//  CPRING_DYNAMIC          CTAs claim items from the launch's counter (1) or
+//                          take them in a fixed snake order (0).
 //  CPRING_FUSED_NOMAX      fused forward only: after the first tile, skip the
 //                          row max and redo a tile only if its first 64 keys'
 //                          row sum or its last 64 keys' row max shows an
@@ -91,11 +98,21 @@ constexpr float kRescaleLog2 = 8.0f;
 //  CPRING_FP8_FAST         the FP8 kernel uses the same no-max fast pass, with
 //                          the guards at 2^8 so that every P it keeps is at
 //                          most 2^8, inside E4M3's range (448).
+//  CPRING_FP8_EARLY_SFREE  the FP8 softmax releases a tile's S columns as
+//                          soon as it has loaded them (the rare redo then
+//                          works from the scores kept in registers) instead
+//                          of after its exponentials.
 #ifndef CPRING_BALANCE
 #define CPRING_BALANCE 2
 #endif
 #ifndef CPRING_GROUP_MIN_ROUNDS
 #define CPRING_GROUP_MIN_ROUNDS 16
+#endif
+#ifndef CPRING_GROUP_DOCS
+#define CPRING_GROUP_DOCS 0
+#endif
+#ifndef CPRING_DYNAMIC
+#define CPRING_DYNAMIC 1
 #endif
 #ifndef CPRING_FUSED_NOMAX
 #define CPRING_FUSED_NOMAX 1
@@ -105,6 +122,9 @@ constexpr float kRescaleLog2 = 8.0f;
 #endif
 #ifndef CPRING_FP8_FAST
 #define CPRING_FP8_FAST 1
+#endif
+#ifndef CPRING_FP8_EARLY_SFREE
+#define CPRING_FP8_EARLY_SFREE 0
 #endif
 constexpr int kPReadyCount = 128;
 constexpr float kOverflowGuard = 18446744073709551616.0f;  // 2^64
@@ -122,7 +142,8 @@ struct Layout {
   static constexpr int kKOff = kQOff + kQTiles * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kStages * kTileBytes;
-  static constexpr int kBytes = kBarOff + 256;
+  static constexpr int kRingOff = kBarOff + 256;  // the item ring
+  static constexpr int kBytes = kRingOff + 256;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024 B
 };
 
@@ -166,6 +187,8 @@ struct KParams {
   int kv_row0;       // key index of row 0 of the K/V tensors (0 unless a block)
   int head_group;    // (b, h) heads whose items are dealt out together
   const int32_t* slot_perm;  // or null: slots heaviest first by measured cost
+  unsigned long long* work_slot;  // this launch's claim counter (see claim_item)
+  uint32_t epoch;                 // this launch's tag in that counter
   const float* q_descale;  // FP8 form: [B * H] each
   const float* k_descale;
   const float* v_descale;
@@ -180,10 +203,11 @@ struct Item {
   int klo, khi;                      // key range this launch may use
 };
 
-// Work item w: (b, h, query shard, pair of 128-row tiles).  Items are dealt
-// head group by head group (p.head_group (b, h) heads at a time), and inside
-// a group heaviest first, so that the CTAs running at any moment stream the
-// K/V of few heads and reuse each K/V tile from L2.
+// Work item w: (b, h, query shard, pair of 128-row tiles).  Items are laid
+// out head group by head group (p.head_group (b, h) heads at a time), and
+// inside a group heaviest first; CTAs claim them in that order, so the CTAs
+// running at any moment stream the K/V of few heads and reuse each K/V tile
+// from L2, and the lightest items come last.
 // A tile's visible keys are [max(doc_start(q_first), klo), min(h(q_last), khi)]
 // with h(q) = q (causal) or doc_end(q) - 1: every key of that interval is
 // seen by at least one row of the tile, so the K/V tiles it touches are
@@ -234,6 +258,83 @@ __device__ __forceinline__ void decode_item(const KParams& p, int n_docs, int w,
       }
     }
   }
+}
+
+// ---------------------------------------------------------------- work queue
+// Work items are claimed at run time.  CTA c starts with item c; every later
+// item comes from a counter the launch's CTAs share, in the order
+// decode_item lays out (head group by head group, heaviest first inside
+// each), so a CTA that finishes early takes more work and the tail stays
+// short whatever the items cost.  The counter is one of kWorkSlots 64-bit
+// slots of a device array that launches use in turn; a slot holds
+// (launch epoch << 32 | next index), and the first claim of a launch that
+// finds another epoch there restarts it, so no launch clears it and no
+// launch allocates it.  At most kWorkSlots launches can run at once on a
+// device before one would reuse the slot of another still running.
+constexpr int kWorkSlots = 256;
+__device__ unsigned long long g_work_slots[kWorkSlots];
+
+// The next index of this launch's counter (0, 1, 2, ...).  A lock-free retry:
+// each failed compare-and-swap means another CTA claimed one, so the loop
+// ends; the bound only guards against a slot shared with a runaway launch.
+__device__ __forceinline__ int claim_item(unsigned long long* slot, uint32_t epoch, int* err) {
+  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(slot);
+  for (int attempt = 0; attempt < (1 << 20); ++attempt) {
+    const bool mine = static_cast<uint32_t>(cur >> 32) == epoch;
+    const unsigned long long want =
+        mine ? cur + 1 : ((static_cast<unsigned long long>(epoch) << 32) | 1ull);
+    const unsigned long long prev = atomicCAS(slot, cur, want);
+    if (prev == cur) return mine ? static_cast<int>(cur & 0xffffffffull) : 0;
+    cur = prev;
+  }
+  atomicOr(err, kErrTimeout);
+  return INT_MAX / 2;  // past every item: the CTA stops
+}
+
+// The CTA's ring of claimed item indices: the producer publishes each item
+// it claims (its k-th item in slot k % kRing); the MMA warp and the eight
+// softmax warps read them in the same order, so every role walks the same
+// items.  Full barriers take the producer's arrival, empty ones one arrival
+// per reading warp.
+constexpr int kRing = 4;
+constexpr int kRingReaders = 9;  // the MMA warp and the eight softmax warps
+constexpr int kRingBytes = 2 * kRing * 8 + kRing * 4;
+static_assert(kRingBytes <= 256, "the item ring's shared-memory block");
+
+struct ItemRing {
+  uint32_t bars;      // shared address: kRing full barriers, then kRing empty barriers
+  volatile int* idx;  // kRing item indices
+  __device__ uint32_t full(int s) const { return bars + 8u * static_cast<uint32_t>(s); }
+  __device__ uint32_t empty(int s) const { return bars + 8u * static_cast<uint32_t>(kRing + s); }
+};
+
+__device__ __forceinline__ void ring_init(const ItemRing& r) {
+  for (int s = 0; s < kRing; ++s) {
+    ptx::mbar_init(r.full(s), 1);
+    ptx::mbar_init(r.empty(s), kRingReaders);
+  }
+}
+
+// Producer (one thread): publish w as the CTA's k-th item.
+__device__ __forceinline__ bool ring_put(const ItemRing& r, uint32_t k, int w,
+                                         volatile uint32_t* abort_flag, const KParams& p) {
+  const int s = static_cast<int>(k % kRing);
+  const uint32_t use = k / kRing;
+  if (use > 0 && !wait1(r.empty(s), (use - 1) & 1u, abort_flag, p)) return false;
+  r.idx[s] = w;
+  ptx::mbar_arrive(r.full(s));
+  return true;
+}
+
+// A reading warp (every lane): the CTA's k-th item, or -1 if the wait gave up.
+__device__ __forceinline__ int ring_get(const ItemRing& r, uint32_t k,
+                                        volatile uint32_t* abort_flag, const KParams& p) {
+  const int s = static_cast<int>(k % kRing);
+  if (!wait_warp(r.full(s), (k / kRing) & 1u, abort_flag, p)) return -1;
+  const int w = r.idx[s];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(r.empty(s));
+  return w;
 }
 
 // ---------------------------------------------------------------- softmax pieces
@@ -437,11 +538,10 @@ __device__ __forceinline__ void store_p_half(uint32_t tS, const uint32_t (&pk)[2
 
 // ---------------------------------------------------------------- kernel
 // The body shared by the bf16 and the FP8 kernels (see the wrappers below).
-template <int D, bool kPartial, bool kFp8>
+template <int D, bool kPartial>
 __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
                                           const CUtensorMap& tmap_v, const KParams& p) {
-  static_assert(!(kFp8 && kPartial), "the FP8 form has no step epilogue");
-  using Lay = Layout<D, kFp8 ? 1 : 2>;
+  using Lay = Layout<D, 2>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -451,6 +551,8 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kBarOff + kTmemSlot);
   volatile uint32_t* abort_flag =
       reinterpret_cast<volatile uint32_t*>(smem + Lay::kBarOff + kAbortSlot);
+  const ItemRing ring{sbase + Lay::kRingOff,
+                      reinterpret_cast<volatile int*>(smem + Lay::kRingOff + 2 * kRing * 8)};
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -477,6 +579,7 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
       ptx::mbar_init(bar(kOBar + t), 1);
     }
     ptx::mbar_init(bar(kDrain), 1);
+    ring_init(ring);
     *abort_flag = 0u;
     ptx::fence_barrier_init();
   }
@@ -507,7 +610,9 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
       bool dropped = false;
       bool ok = true;
       for (int k = 0; ok; ++k) {
-        const int w = item_of(k, c, G);
+        const int w = !CPRING_DYNAMIC ? item_of(k, c, G)
+                      : (k == 0) ? c : G + claim_item(p.work_slot, p.epoch, p.err);
+        if (!ring_put(ring, static_cast<uint32_t>(k), w, abort_flag, p)) { ok = false; break; }
         if (w >= p.n_items) break;
         Item it;
         decode_item(p, n_docs, w, it);
@@ -541,16 +646,10 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
           }
           if (!wait1(bar(kVEmpty + st), ph ^ 1u, abort_flag, p)) { ok = false; break; }
           ptx::mbar_arrive_expect_tx(bar(kVFull + st), Lay::kTileBytes);
-          if constexpr (kFp8) {
-            // V^T [B, H, d, S]: one box of 128 keys x D rows (keys contiguous)
-            ptx::tma_load_4d(sbase + Lay::kVOff + st * Lay::kTileBytes, &tmap_v,
-                             bar(kVFull + st), ks - p.kv_row0, 0, it.h, it.b);
-          } else {
-            for (int pn = 0; pn < Lay::kPanels; ++pn)
-              ptx::tma_load_4d(sbase + Lay::kVOff + st * Lay::kTileBytes + pn * Lay::kPanelBytes,
-                               &tmap_v, bar(kVFull + st), pn * Lay::kPanelCols, it.h,
-                               ks - p.kv_row0, it.b);
-          }
+          for (int pn = 0; pn < Lay::kPanels; ++pn)
+            ptx::tma_load_4d(sbase + Lay::kVOff + st * Lay::kTileBytes + pn * Lay::kPanelBytes,
+                             &tmap_v, bar(kVFull + st), pn * Lay::kPanelCols, it.h,
+                             ks - p.kv_row0, it.b);
           if (st == 0) ++v_armed0; else ++v_armed1;
           ++kv_iter;
         }
@@ -568,11 +667,9 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
     // commit is issued by one lane that elect.sync picks (the warp-collective
     // forms in ptx.cuh), and every wait is the warp-uniform one.
     {
-      constexpr uint32_t kIdescQK =
-          kFp8 ? ptx::idesc_e4m3_f32(kBM, kBN) : ptx::idesc_bf16_f32(kBM, kBN, false);
-      constexpr uint32_t kIdescPV =
-          kFp8 ? ptx::idesc_e4m3_f32(kBM, D) : ptx::idesc_bf16_f32(kBM, D, true);
-      constexpr int kKStep = 32 / (kFp8 ? 1 : 2);  // K elements per MMA (32 bytes)
+      constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(kBM, kBN, false);
+      constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kBM, D, true);
+      constexpr int kKStep = 16;  // K elements per MMA (32 bytes)
       uint32_t kv_iter = 0, q_iter = 0;
       uint32_t p_cnt0 = 0, p_cnt1 = 0;
       bool ok = true;
@@ -584,27 +681,17 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
       // never carries into the offsets above it.)
       const uint64_t d_qk = ptx::smem_desc_sw128(sbase, 16, 1024);
       const uint64_t d_v = ptx::smem_desc_sw128(sbase, Lay::kPanelBytes, 1024);
-      // O_t (+)= P_t V: P_t from TMEM (8 columns per K step in both forms),
-      // V MN-major (bf16) or V^T K-major (FP8) from the given stage.
-      // Half `part` of the K steps: keys 0-63 (part 0) or 64-127 (part 1),
-      // whose P the softmax signals separately.
+      // O_t (+)= P_t V: P_t from TMEM (8 columns per K step), V MN-major from
+      // the given stage.  Half `part` of the K steps: keys 0-63 (part 0) or
+      // 64-127 (part 1), whose P the softmax signals separately.
       auto issue_pv = [&](int t, uint32_t st, bool first, int part) {
         constexpr int kHalfSteps = kBN / kKStep / 2;
-        if constexpr (kFp8) {
-          const uint64_t dv = d_qk + ((Lay::kVOff + st * Lay::kTileBytes) >> 4);
+        const uint64_t dv = d_v + ((Lay::kVOff + st * Lay::kTileBytes) >> 4);
 #pragma unroll
-          for (int s = part * kHalfSteps; s < (part + 1) * kHalfSteps; ++s)
-            ptx::mma_ts_f8_w(tmem_base + 256 + t * D, tmem_base + t * 128 + s * 8,
-                           dv + static_cast<uint64_t>((s * 32) >> 4), kIdescPV,
-                           (first && s == 0) ? 0u : 1u);
-        } else {
-          const uint64_t dv = d_v + ((Lay::kVOff + st * Lay::kTileBytes) >> 4);
-#pragma unroll
-          for (int s = part * kHalfSteps; s < (part + 1) * kHalfSteps; ++s) {
-            ptx::mma_ts_w(tmem_base + 256 + t * D, tmem_base + t * 128 + s * 8,
+        for (int s = part * kHalfSteps; s < (part + 1) * kHalfSteps; ++s) {
+          ptx::mma_ts_w(tmem_base + 256 + t * D, tmem_base + t * 128 + s * 8,
                         dv + static_cast<uint64_t>((s * 16 * 128) >> 4), kIdescPV,
                         (first && s == 0) ? 0u : 1u);
-          }
         }
       };
       // S_t = Q_t K^T (both K-major, 128-byte swizzled panels; a K step is
@@ -615,15 +702,13 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
 #pragma unroll
         for (int s = 0; s < D / kKStep; ++s) {
           const uint64_t step = static_cast<uint64_t>(((s >> 2) * Lay::kPanelBytes + (s & 3) * 32) >> 4);
-          if constexpr (kFp8)
-            ptx::mma_ss_f8_w(tmem_base + t * 128, dq + step, dk + step, kIdescQK, s > 0 ? 1u : 0u);
-          else
-            ptx::mma_ss_w(tmem_base + t * 128, dq + step, dk + step, kIdescQK, s > 0 ? 1u : 0u);
+          ptx::mma_ss_w(tmem_base + t * 128, dq + step, dk + step, kIdescQK, s > 0 ? 1u : 0u);
         }
         ptx::mma_commit_w(bar(kSFull + t));
       };
       for (int k = 0; ok; ++k) {
-        const int w = item_of(k, c, G);
+        const int w = ring_get(ring, static_cast<uint32_t>(k), abort_flag, p);
+        if (w < 0) { ok = false; break; }
         if (w >= p.n_items) break;
         Item it;
         decode_item(p, n_docs, w, it);
@@ -707,11 +792,12 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem_base + lane_off + static_cast<uint32_t>(t * 128);
     const uint32_t tO = tmem_base + lane_off + 256u + static_cast<uint32_t>(t * D);
-    float sc = p.scale_log2;
+    const float sc = p.scale_log2;
     uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const int w = item_of(k, c, G);
+      const int w = ring_get(ring, static_cast<uint32_t>(k), abort_flag, p);
+      if (w < 0) { ok = false; break; }
       if (w >= p.n_items) break;
       Item it;
       decode_item(p, n_docs, w, it);
@@ -720,8 +806,6 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
       const int f_lo = t ? it.f_lo[1] : it.f_lo[0];
       const int f_hi = t ? it.f_hi[1] : it.f_hi[0];
       if (rows == 0) continue;
-      const int bh = it.b * p.H + it.h;
-      if constexpr (kFp8) sc = p.scale_log2 * __ldg(p.q_descale + bh) * __ldg(p.k_descale + bh);
       const bool row_valid = row_in_tile < rows;
       const int r = (t ? it.q0[1] : it.q0[0]) + row_in_tile;
       int klo_r = 0, khi_r = -1;
@@ -758,77 +842,47 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
         float lsum, mx;
         float alpha = 1.f;
         bool rescale_o = false;
-        const bool fast = CPRING_FUSED_NOMAX && !kPartial && (!kFp8 || CPRING_FP8_FAST) &&
+        const bool fast = CPRING_FUSED_NOMAX && !kPartial &&
                           !__any_sync(0xffffffffu, m_used == -INFINITY);
         if (fast) {
-          if constexpr (kFp8) {
-            // One pass over the 128 keys; a row sum above 2^8 sends the tile
-            // to the redo below, which keeps every P inside E4M3's range
-            // (448).  (Its P V is only four MMAs, too short to gain from the
-            // split that the bf16 form uses.)
-            load_scores(tS, c_lo, c_hi, sv);
-            {
-              uint64_t acc = 0;  // two fp32 zeros
-              exp_chunks_f8(sv, 0, sc, m_used, pk, acc);
-              exp_chunks_f8(sv, 1, sc, m_used, pk, acc);
-              lsum = sum2(acc);
+          // P in two halves of 64 keys: the first half is stored and
+          // signalled (kPReady + t) before the second half's exponentials
+          // run, so the MMA warp starts that half of P V meanwhile.  Both
+          // halves use the current reference; before anything is stored the
+          // first half's row sum and the second half's row max are checked
+          // against the guard (2^64, as a sum and as an exponent).
+          load_scores(tS, c_lo, c_hi, sv);
+          const float lsum1 = exp_half(sv, 0, sc, m_used, pk);
+          const float mx2 = half_max(sv, 1);
+          const bool in_range =
+              (lsum1 <= kOverflowGuard) & (mx2 * sc <= m_used + kOverflowGuardLog2);
+          if (__all_sync(0xffffffffu, in_range)) {
+            store_p_half(tS, pk, 0);
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(kPReady + t));
+            const float lsum2 = exp_half(sv, 1, sc, m_used, pk);
+            l_run += lsum1 + lsum2;
+            store_p_half(tS, pk, 1);
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(kPReadyB + t));
+            continue;
+          }
+          // Rare: a row ran past the guard, so this tile's max is above the
+          // reference (64 entries of at most 1 sum to 64 or less).  Nothing
+          // is stored yet and sv still holds the scores: move the reference
+          // of those rows to this tile's max and let every lane recompute
+          // (lanes that keep theirs get the same P).
+          {
+            const float m_tile = row_max(sv) * sc;
+            if (!in_range && m_tile > m_used) {
+              rescale_o = true;
+              alpha = ptx::ex2(m_used - m_tile);
+              l_run *= alpha;
+              m_used = m_tile;
             }
-            const bool redo = !(lsum <= kOverflowGuardFp8);
-            if (__any_sync(0xffffffffu, redo)) {
-              // Rare: a sum above the guard means this tile's max is above
-              // the reference (128 entries of at most 1 sum to 128 or less).
-              // Reload S (P is not yet written), move the reference of those
-              // rows to this tile's max and let every lane recompute.
-              load_scores(tS, c_lo, c_hi, sv);
-              const float m_tile = row_max(sv) * sc;
-              if (redo && m_tile > m_used) {
-                rescale_o = true;
-                alpha = ptx::ex2(m_used - m_tile);
-                l_run *= alpha;
-                m_used = m_tile;
-              }
-              exponentials<kFp8, kPartial>(sv, sc, m_used, pk, lsum, mx);
-            }
-          } else {
-            // P in two halves of 64 keys: the first half is stored and
-            // signalled (kPReady + t) before the second half's exponentials
-            // run, so the MMA warp starts that half of P V meanwhile.  Both
-            // halves use the current reference; before anything is stored the
-            // first half's row sum and the second half's row max are checked
-            // against the guard (2^64, as a sum and as an exponent).
-            load_scores(tS, c_lo, c_hi, sv);
-            const float lsum1 = exp_half(sv, 0, sc, m_used, pk);
-            const float mx2 = half_max(sv, 1);
-            const bool in_range =
-                (lsum1 <= kOverflowGuard) & (mx2 * sc <= m_used + kOverflowGuardLog2);
-            if (__all_sync(0xffffffffu, in_range)) {
-              store_p_half(tS, pk, 0);
-              ptx::tmem_wait_st();
-              ptx::tc_fence_before();
-              ptx::mbar_arrive(bar(kPReady + t));
-              const float lsum2 = exp_half(sv, 1, sc, m_used, pk);
-              l_run += lsum1 + lsum2;
-              store_p_half(tS, pk, 1);
-              ptx::tmem_wait_st();
-              ptx::tc_fence_before();
-              ptx::mbar_arrive(bar(kPReadyB + t));
-              continue;
-            }
-            // Rare: a row ran past the guard, so this tile's max is above the
-            // reference (64 entries of at most 1 sum to 64 or less).  Nothing
-            // is stored yet and sv still holds the scores: move the reference
-            // of those rows to this tile's max and let every lane recompute
-            // (lanes that keep theirs get the same P).
-            {
-              const float m_tile = row_max(sv) * sc;
-              if (!in_range && m_tile > m_used) {
-                rescale_o = true;
-                alpha = ptx::ex2(m_used - m_tile);
-                l_run *= alpha;
-                m_used = m_tile;
-              }
-              exponentials<kFp8, kPartial>(sv, sc, m_used, pk, lsum, mx);
-            }
+            exponentials<false, kPartial>(sv, sc, m_used, pk, lsum, mx);
           }
         } else {
         load_scores(tS, c_lo, c_hi, sv);
@@ -843,7 +897,7 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
             l_run *= alpha;
             m_used = m_tile;
           }
-          exponentials<kFp8, kPartial>(sv, sc, (m_used == -INFINITY) ? 0.f : m_used, pk, lsum, mx);
+          exponentials<false, kPartial>(sv, sc, (m_used == -INFINITY) ? 0.f : m_used, pk, lsum, mx);
         } else if constexpr (kPartial) {
           // Step kernel: the exact row max first (its epilogue exports it),
           // then P in two halves of 64 keys, each signalled once stored, as
@@ -872,13 +926,13 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
             ptx::mbar_arrive(bar(kPReadyB + t));
             continue;
           }
-          exponentials<kFp8, kPartial>(sv, sc, m_used, pk, lsum, mx);
+          exponentials<false, kPartial>(sv, sc, m_used, pk, lsum, mx);
         } else {
           // Exponentials against the current reference; the row max is
           // taken in the same pass and only forces a redo (rare) when it
           // moved more than 2^8 above the reference.
           {
-            exponentials<kFp8, kPartial>(sv, sc, m_used, pk, lsum, mx);
+            exponentials<false, kPartial>(sv, sc, m_used, pk, lsum, mx);
             const float m_tile = mx * sc;
             m_true = fmaxf(m_true, m_tile);
             const bool redo = m_tile > m_used + kRescaleLog2;
@@ -890,14 +944,14 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
                 m_used = m_tile;
               }
               load_scores(tS, c_lo, c_hi, sv);  // S is still in TMEM: P not yet written
-              exponentials<kFp8, kPartial>(sv, sc, m_used, pk, lsum, mx);
+              exponentials<false, kPartial>(sv, sc, m_used, pk, lsum, mx);
             }
           }
         }
         }
         l_run += lsum;
         ptx::tmem_st32(tS, pk[0]);
-        if constexpr (!kFp8) ptx::tmem_st32(tS + 32, pk[1]);
+        ptx::tmem_st32(tS + 32, pk[1]);
         if (__any_sync(0xffffffffu, rescale_o)) {
           // O_t already holds the sum up to the previous tile: the MMA warp
           // issued that PV before this tile's S, and the commit this warp
@@ -924,7 +978,7 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
       ++o_cnt;
       ptx::tc_fence_after();
       if (!kPartial) {
-        const float inv_l = (kFp8 ? __ldg(p.v_descale + bh) : 1.f) / l_run;
+        const float inv_l = 1.f / l_run;
         uint4* dst = reinterpret_cast<uint4*>(
             p.out + ((static_cast<size_t>(it.b) * p.S + r) * p.H + it.h) * D);
 #pragma unroll
@@ -991,12 +1045,472 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
   }
 }
 
+// ---------------------------------------------------------------- FP8 kernel
+// The FP8 form hands P to the PV product through shared memory instead of
+// TMEM.  P in E4M3 is 16 KB per 128 x 128 tile, so two buffers per query tile
+// fit beside the FP8 Q/K/V tiles.  With P out of TMEM, the S columns of a
+// query tile are free as soon as its softmax has loaded them, so the MMA warp
+// issues S = Q K^T of the next key tile right then, while the softmax is
+// still exponentiating the current one: a softmax warpgroup never waits for
+// its own PV and next S in turn, which is what bound the FP8 form (its
+// products run at twice the bf16 rate; the exponentials do not).
+constexpr int kStages8 = 3;  // K/V ring depth of the FP8 kernel
+
+struct Fp8Layout {
+  static constexpr int kTileBytes = kBM * 128;  // 128 rows x 128 E4M3 = one swizzle panel
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + kQTiles * kTileBytes;
+  static constexpr int kVOff = kKOff + kStages8 * kTileBytes;
+  static constexpr int kPOff = kVOff + kStages8 * kTileBytes;   // [tile][buffer] P tiles
+  static constexpr int kBarOff = kPOff + kQTiles * 2 * kTileBytes;
+  static constexpr int kRingOff = kBarOff + 256;  // the item ring
+  static constexpr int kBytes = kRingOff + 256;
+  static constexpr int kAlloc = kBytes + 1024;
+};
+
+enum Bar8 : int {
+  k8QFull = 0,
+  k8QEmpty = 1,
+  k8KFull = 2,    // + stage
+  k8VFull = 5,    // + stage
+  k8KEmpty = 8,   // + stage: K tile read by both S products
+  k8VEmpty = 11,  // + stage: V tile read by both PV products
+  k8SFull = 14,   // + tile: S of the tile's next key tile in TMEM
+  k8SFree = 16,   // + tile: the softmax has loaded that S (its columns may be reused)
+  k8PReady = 18,  // + 2 * tile + buffer: P stored in that shared-memory buffer
+  k8PFree = 22,   // + 2 * tile + buffer: the PV that read that buffer is done
+  k8OBar = 26,    // + tile: every PV of tile t in the item done (once per item)
+  k8Drain = 28,
+  k8NumBars = 29
+};
+static_assert(k8NumBars * 8 + 8 <= 256, "FP8 barrier block");
+constexpr int kTmemSlot8 = k8NumBars * 8;
+constexpr int kAbortSlot8 = k8NumBars * 8 + 4;
+
+template <int D>
+__device__ __forceinline__ void attn_body_fp8(const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
+                                              const CUtensorMap& tmap_v, const KParams& p) {
+  static_assert(D == 128, "the FP8 form takes d = 128");
+  using Lay = Fp8Layout;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_u32(smem);
+  const uint32_t bars = sbase + Lay::kBarOff;
+  auto bar = [&](int idx) -> uint32_t { return bars + 8u * static_cast<uint32_t>(idx); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kBarOff + kTmemSlot8);
+  volatile uint32_t* abort_flag =
+      reinterpret_cast<volatile uint32_t*>(smem + Lay::kBarOff + kAbortSlot8);
+  const ItemRing ring{sbase + Lay::kRingOff,
+                      reinterpret_cast<volatile int*>(smem + Lay::kRingOff + 2 * kRing * 8)};
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  int n_docs = 1;
+  if (p.doc_offsets != nullptr) {
+    n_docs = __ldg(p.doc_info);
+    if (n_docs <= 0) return;  // malformed doc_offsets: the scan already flagged it
+  }
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar(k8QFull), 1);
+    ptx::mbar_init(bar(k8QEmpty), 1);
+    for (int s = 0; s < kStages8; ++s) {
+      ptx::mbar_init(bar(k8KFull + s), 1);
+      ptx::mbar_init(bar(k8VFull + s), 1);
+      ptx::mbar_init(bar(k8KEmpty + s), 1);
+      ptx::mbar_init(bar(k8VEmpty + s), 1);
+    }
+    for (int t = 0; t < kQTiles; ++t) {
+      ptx::mbar_init(bar(k8SFull + t), 1);
+      ptx::mbar_init(bar(k8SFree + t), kPReadyCount);
+      ptx::mbar_init(bar(k8OBar + t), 1);
+      for (int b = 0; b < 2; ++b) {
+        ptx::mbar_init(bar(k8PReady + 2 * t + b), kPReadyCount);
+        ptx::mbar_init(bar(k8PFree + 2 * t + b), 1);
+      }
+    }
+    ptx::mbar_init(bar(k8Drain), 1);
+    ring_init(ring);
+    *abort_flag = 0u;
+    ptx::fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int G = gridDim.x;
+  const int c = blockIdx.x;
+
+  if (warp >= kProducerWarp) {
+   ptx::setmaxnreg_dec<kControlRegs>();
+   if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      ptx::tma_prefetch_desc(&tmap_q);
+      ptx::tma_prefetch_desc(&tmap_k);
+      ptx::tma_prefetch_desc(&tmap_v);
+      uint32_t kv_iter = 0, q_iter = 0;
+      // Loads started into each stage (the n-th completes phase n - 1), held
+      // in registers: a runtime index into a local array would live in memory.
+      uint32_t k_armed0 = 0, k_armed1 = 0, k_armed2 = 0;
+      uint32_t v_armed0 = 0, v_armed1 = 0, v_armed2 = 0;
+      auto bump = [](uint32_t st, uint32_t& a0, uint32_t& a1, uint32_t& a2) {
+        if (st == 0) ++a0; else if (st == 1) ++a1; else ++a2;
+      };
+      bool dropped = false;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int w = !CPRING_DYNAMIC ? item_of(k, c, G)
+                      : (k == 0) ? c : G + claim_item(p.work_slot, p.epoch, p.err);
+        if (!ring_put(ring, static_cast<uint32_t>(k), w, abort_flag, p)) { ok = false; break; }
+        if (w >= p.n_items) break;
+        Item it;
+        decode_item(p, n_docs, w, it);
+        if (it.F_lo > it.F_hi) continue;
+        if (!wait1(bar(k8QEmpty), (q_iter & 1u) ^ 1u, abort_flag, p)) { ok = false; break; }
+        ptx::mbar_arrive_expect_tx(bar(k8QFull), kQTiles * Lay::kTileBytes);
+#pragma unroll
+        for (int t = 0; t < kQTiles; ++t)
+          ptx::tma_load_4d(sbase + Lay::kQOff + t * Lay::kTileBytes, &tmap_q, bar(k8QFull), 0,
+                           it.h, it.q0[t], it.b);
+        ++q_iter;
+        for (int f = it.F_lo; f <= it.F_hi; ++f) {
+          const uint32_t st = kv_iter % kStages8;
+          const uint32_t ph = (kv_iter / kStages8) & 1u;
+          int ks, ke;
+          tile_keys(p, f, ks, ke);
+          if (!wait1(bar(k8KEmpty + st), ph ^ 1u, abort_flag, p)) { ok = false; break; }
+          if (p.fault_drop_k && c == 0 && !dropped) {
+            // Test hook: this K tile is never loaded, so the MMA warp's
+            // bounded wait for it runs out and the CTA takes its abort path.
+            dropped = true;
+          } else {
+            ptx::mbar_arrive_expect_tx(bar(k8KFull + st), Lay::kTileBytes);
+            ptx::tma_load_4d(sbase + Lay::kKOff + st * Lay::kTileBytes, &tmap_k, bar(k8KFull + st),
+                             0, it.h, ks - p.kv_row0, it.b);
+            bump(st, k_armed0, k_armed1, k_armed2);
+          }
+          if (!wait1(bar(k8VEmpty + st), ph ^ 1u, abort_flag, p)) { ok = false; break; }
+          ptx::mbar_arrive_expect_tx(bar(k8VFull + st), Lay::kTileBytes);
+          // V^T [B, H, d, S]: one box of 128 keys x D rows (keys contiguous)
+          ptx::tma_load_4d(sbase + Lay::kVOff + st * Lay::kTileBytes, &tmap_v, bar(k8VFull + st),
+                           ks - p.kv_row0, 0, it.h, it.b);
+          bump(st, v_armed0, v_armed1, v_armed2);
+          ++kv_iter;
+        }
+      }
+      // Let every copy this thread started land before the CTA can exit.
+      if (q_iter > 0) wait1(bar(k8QFull), (q_iter - 1) & 1u, abort_flag, p, false);
+      const uint32_t k_armed[kStages8] = {k_armed0, k_armed1, k_armed2};
+      const uint32_t v_armed[kStages8] = {v_armed0, v_armed1, v_armed2};
+#pragma unroll
+      for (int s = 0; s < kStages8; ++s) {
+        if (k_armed[s] > 0) wait1(bar(k8KFull + s), (k_armed[s] - 1) & 1u, abort_flag, p, false);
+        if (v_armed[s] > 0) wait1(bar(k8VFull + s), (v_armed[s] - 1) & 1u, abort_flag, p, false);
+      }
+    }
+   } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    // Per key tile f: S(f) of both query tiles as soon as each softmax has
+    // loaded its previous S, then PV(f - 1) of both tiles as each P lands in
+    // shared memory.  The whole warp runs the loop; elect.sync picks the lane
+    // that issues each MMA and commit.
+    {
+      constexpr uint32_t kIdesc = ptx::idesc_e4m3_f32(kBM, kBN);  // S and PV: 128 x 128
+      static_assert(kBN == D, "one instruction descriptor for both products");
+      // Per-tile state in scalars (a runtime index into a local array would
+      // put it in memory).
+      uint32_t kv_iter = 0, q_iter = 0;
+      uint32_t s_issued0 = 0, s_issued1 = 0;   // S products issued, per query tile
+      uint32_t pv_issued0 = 0, pv_issued1 = 0; // PV products issued, per query tile
+      bool ok = true;
+      const uint64_t d_sw = ptx::smem_desc_sw128(sbase, 16, 1024);
+      // O_t (+)= P_t V: P from its shared-memory buffer, V^T K-major; a K step
+      // is 32 E4M3 (32 bytes) along the 128-byte swizzled rows of both.
+      auto issue_pv = [&](int t, uint32_t& n_pv, uint32_t st, bool& first, bool last) -> bool {
+        const uint32_t n = n_pv;
+        const int b = static_cast<int>(n & 1u);
+        if (!wait_warp(bar(k8PReady + 2 * t + b), (n >> 1) & 1u, abort_flag, p)) return false;
+        ptx::tc_fence_after();
+        const uint64_t dp = d_sw + ((Lay::kPOff + (2 * t + b) * Lay::kTileBytes) >> 4);
+        const uint64_t dv = d_sw + ((Lay::kVOff + st * Lay::kTileBytes) >> 4);
+#pragma unroll
+        for (int s = 0; s < kBN / 32; ++s)
+          ptx::mma_ss_f8_w(tmem_base + 256 + t * D, dp + static_cast<uint64_t>(2 * s),
+                           dv + static_cast<uint64_t>(2 * s), kIdesc, (first && s == 0) ? 0u : 1u);
+        ptx::mma_commit_w(bar(k8PFree + 2 * t + b));
+        if (last) ptx::mma_commit_w(bar(k8OBar + t));
+        first = false;
+        n_pv = n + 1;
+        return true;
+      };
+      // S_t = Q_t K^T (both K-major, one 128-byte swizzled panel each), once
+      // the softmax has loaded the tile's previous S.
+      auto issue_s = [&](int t, uint32_t& n_s, uint32_t st) -> bool {
+        if (n_s > 0) {
+          if (!wait_warp(bar(k8SFree + t), (n_s - 1) & 1u, abort_flag, p)) return false;
+          ptx::tc_fence_after();
+        }
+        const uint64_t dq = d_sw + ((Lay::kQOff + t * Lay::kTileBytes) >> 4);
+        const uint64_t dk = d_sw + ((Lay::kKOff + st * Lay::kTileBytes) >> 4);
+#pragma unroll
+        for (int s = 0; s < D / 32; ++s)
+          ptx::mma_ss_f8_w(tmem_base + t * 128, dq + static_cast<uint64_t>(2 * s),
+                           dk + static_cast<uint64_t>(2 * s), kIdesc, s > 0 ? 1u : 0u);
+        ptx::mma_commit_w(bar(k8SFull + t));
+        ++n_s;
+        return true;
+      };
+      for (int k = 0; ok; ++k) {
+        const int w = ring_get(ring, static_cast<uint32_t>(k), abort_flag, p);
+        if (w < 0) { ok = false; break; }
+        if (w >= p.n_items) break;
+        Item it;
+        decode_item(p, n_docs, w, it);
+        if (it.F_lo > it.F_hi) continue;
+        if (!wait_warp(bar(k8QFull), q_iter & 1u, abort_flag, p)) { ok = false; break; }
+        ++q_iter;
+        ptx::tc_fence_after();
+        bool pend0 = false, pend1 = false;    // S issued whose PV is still owed
+        bool first0 = true, first1 = true;    // next PV overwrites O
+        uint32_t prev_st = 0, prev_ph = 0;
+        bool have_prev = false;
+        // Owed PVs on the previous K/V stage (V(f_prev)); then release it.
+        auto flush = [&](int f_prev) -> bool {
+          if (pend0 || pend1) {
+            if (!wait_warp(bar(k8VFull + prev_st), prev_ph, abort_flag, p)) return false;
+          }
+          if (pend0 && !issue_pv(0, pv_issued0, prev_st, first0, f_prev == it.f_hi[0]))
+            return false;
+          if (pend1 && !issue_pv(1, pv_issued1, prev_st, first1, f_prev == it.f_hi[1]))
+            return false;
+          pend0 = pend1 = false;
+          ptx::mma_commit_w(bar(k8VEmpty + prev_st));
+          return true;
+        };
+        for (int f = it.F_lo; f <= it.F_hi; ++f) {
+          const uint32_t st = kv_iter % kStages8;
+          const uint32_t ph = (kv_iter / kStages8) & 1u;
+          if (!wait_warp(bar(k8KFull + st), ph, abort_flag, p)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const bool now0 = (f >= it.f_lo[0] && f <= it.f_hi[0]);
+          const bool now1 = (f >= it.f_lo[1] && f <= it.f_hi[1]);
+          if (now0 && !issue_s(0, s_issued0, st)) { ok = false; break; }
+          if (now1 && !issue_s(1, s_issued1, st)) { ok = false; break; }
+          ptx::mma_commit_w(bar(k8KEmpty + st));  // K(f) read by every S
+          if (have_prev && !flush(f - 1)) { ok = false; break; }
+          pend0 = now0;
+          pend1 = now1;
+          prev_st = st;
+          prev_ph = ph;
+          have_prev = true;
+          ++kv_iter;
+        }
+        if (!ok) break;
+        ptx::mma_commit_w(bar(k8QEmpty));  // every S of this item has been issued
+        if (have_prev && !flush(it.F_hi)) { ok = false; break; }
+      }
+      // Wait until every MMA this warp issued has finished.
+      ptx::mma_commit_w(bar(k8Drain));
+      wait_warp(bar(k8Drain), 0u, abort_flag, p, false);
+    }
+   }
+  } else {
+    ptx::setmaxnreg_inc<kSoftmaxRegs>();
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;  // query tile of this warpgroup
+    const int wq = warp & 3;  // TMEM lane quarter
+    const int row_in_tile = wq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem_base + lane_off + static_cast<uint32_t>(t * 128);
+    const uint32_t tO = tmem_base + lane_off + 256u + static_cast<uint32_t>(t * D);
+    // this thread's row of a P buffer: 128 bytes, 16-byte chunk c stored at
+    // chunk c ^ (row % 8) of its row (the 128-byte swizzle the MMA reads)
+    const uint32_t p_row = sbase + Lay::kPOff + static_cast<uint32_t>(2 * t * Lay::kTileBytes) +
+                           static_cast<uint32_t>((row_in_tile >> 3) * 1024 + (row_in_tile & 7) * 128);
+    const uint32_t r8 = static_cast<uint32_t>(row_in_tile & 7);
+    uint32_t s_cnt = 0, p_cnt = 0, o_cnt = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int w = ring_get(ring, static_cast<uint32_t>(k), abort_flag, p);
+      if (w < 0) { ok = false; break; }
+      if (w >= p.n_items) break;
+      Item it;
+      decode_item(p, n_docs, w, it);
+      const int rows = t ? it.rows[1] : it.rows[0];
+      const int f_lo = t ? it.f_lo[1] : it.f_lo[0];
+      const int f_hi = t ? it.f_hi[1] : it.f_hi[0];
+      if (rows == 0 || f_lo > f_hi) continue;
+      const int bh = it.b * p.H + it.h;
+      const float sc = p.scale_log2 * __ldg(p.q_descale + bh) * __ldg(p.k_descale + bh);
+      const bool row_valid = row_in_tile < rows;
+      const int r = (t ? it.q0[1] : it.q0[0]) + row_in_tile;
+      int klo_r = 0, khi_r = -1;
+      if (row_valid) {
+        const int2 ds = doc_span(p, n_docs, r);
+        klo_r = max(ds.x, it.klo);
+        khi_r = min(p.causal ? r : ds.y - 1, it.khi);
+      }
+      float m_used = -INFINITY, l_run = 0.f;
+      for (int f = f_lo; f <= f_hi; ++f) {
+        if (!wait_warp(bar(k8SFull + t), s_cnt & 1u, abort_flag, p)) { ok = false; break; }
+        ++s_cnt;
+        ptx::tc_fence_after();
+        int ks, ke;
+        tile_keys(p, f, ks, ke);
+        const int c_lo = klo_r - ks;
+        const int c_hi = min(khi_r, ke - 1) - ks;
+        uint32_t sv[4][32];
+        uint32_t pk[2][32];
+        load_scores(tS, c_lo, c_hi, sv);
+        if (CPRING_FP8_EARLY_SFREE) {
+          // S is in registers: its TMEM columns may take the next key tile's S.
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(k8SFree + t));
+        }
+        float lsum = 0.f, mx;
+        float alpha = 1.f;
+        bool rescale_o = false;
+        if (CPRING_FP8_FAST && !__any_sync(0xffffffffu, m_used == -INFINITY)) {
+          // One pass over the 128 keys against the current reference; a row
+          // sum above 2^8 sends the tile to the redo below, which keeps every
+          // P inside E4M3's range (448).
+          uint64_t acc = 0;  // two fp32 zeros
+          exp_chunks_f8(sv, 0, sc, m_used, pk, acc);
+          exp_chunks_f8(sv, 1, sc, m_used, pk, acc);
+          lsum = sum2(acc);
+          const bool redo = !(lsum <= kOverflowGuardFp8);
+          if (__any_sync(0xffffffffu, redo)) {
+            // Rare: a sum above the guard means this tile's max is above the
+            // reference (128 entries of at most 1 sum to 128 or less).  Move
+            // the reference of those rows to this tile's max and recompute
+            // (from the registers, or from S still held in TMEM).
+            if (!CPRING_FP8_EARLY_SFREE) load_scores(tS, c_lo, c_hi, sv);
+            const float m_tile = row_max(sv) * sc;
+            if (redo && m_tile > m_used) {
+              rescale_o = true;
+              alpha = ptx::ex2(m_used - m_tile);
+              l_run *= alpha;
+              m_used = m_tile;
+            }
+            exponentials<true>(sv, sc, m_used, pk, lsum, mx);
+          }
+        } else {
+          // Some row of this warp has no reference yet: row max first.
+          mx = row_max(sv);
+          const float m_tile = mx * sc;
+          if (m_tile > m_used + kRescaleLog2) {
+            rescale_o = (m_used != -INFINITY);
+            alpha = rescale_o ? ptx::ex2(m_used - m_tile) : 0.f;
+            l_run *= alpha;
+            m_used = m_tile;
+          }
+          exponentials<true>(sv, sc, (m_used == -INFINITY) ? 0.f : m_used, pk, lsum, mx);
+        }
+        if (!CPRING_FP8_EARLY_SFREE) {
+          // This tile's S is no longer needed: its TMEM columns may take the
+          // next key tile's S while P goes out and PV runs.
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(k8SFree + t));
+        }
+        l_run += lsum;
+        const uint32_t n = p_cnt++;
+        const uint32_t b = n & 1u;
+        bool rescaled = false;
+        if (__any_sync(0xffffffffu, rescale_o)) {
+          // O_t must hold every earlier PV of this tile before it is scaled:
+          // wait for the PV of the previous key tile (the one before it was
+          // already waited for by the P-buffer reuse below).
+          if (n >= 1 && !wait_warp(bar(k8PFree + 2 * t + ((n - 1) & 1u)), ((n - 1) >> 1) & 1u,
+                                   abort_flag, p)) { ok = false; break; }
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t ov[32];
+            ptx::tmem_ld32(tO + ch * 32, ov);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence(ov);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * alpha);
+            ptx::tmem_st32(tO + ch * 32, ov);
+          }
+          rescaled = true;
+        }
+        // The buffer's previous P (two key tiles back) must have been read.
+        if (n >= 2 && !wait_warp(bar(k8PFree + 2 * t + b), ((n >> 1) - 1) & 1u, abort_flag, p)) {
+          ok = false;
+          break;
+        }
+        const uint32_t dst = p_row + b * static_cast<uint32_t>(Lay::kTileBytes);
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+          ptx::st_shared_v4(dst + ((static_cast<uint32_t>(ch) ^ r8) << 4), pk[0][4 * ch],
+                            pk[0][4 * ch + 1], pk[0][4 * ch + 2], pk[0][4 * ch + 3]);
+        ptx::fence_proxy_async_shared();
+        if (rescaled) ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(k8PReady + 2 * t + b));
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      if (!wait_warp(bar(k8OBar + t), o_cnt & 1u, abort_flag, p)) { ok = false; break; }
+      ++o_cnt;
+      ptx::tc_fence_after();
+      const float inv_l = __ldg(p.v_descale + bh) / l_run;
+      uint4* dst = reinterpret_cast<uint4*>(
+          p.out + ((static_cast<size_t>(it.b) * p.S + r) * p.H + it.h) * D);
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t ov[32];
+        ptx::tmem_ld32(tO + ch * 32, ov);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence(ov);
+        if (row_valid) {
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            uint4 v4;
+            v4.x = ptx::pack_bf16(__uint_as_float(ov[8 * x + 0]) * inv_l,
+                                  __uint_as_float(ov[8 * x + 1]) * inv_l);
+            v4.y = ptx::pack_bf16(__uint_as_float(ov[8 * x + 2]) * inv_l,
+                                  __uint_as_float(ov[8 * x + 3]) * inv_l);
+            v4.z = ptx::pack_bf16(__uint_as_float(ov[8 * x + 4]) * inv_l,
+                                  __uint_as_float(ov[8 * x + 5]) * inv_l);
+            v4.w = ptx::pack_bf16(__uint_as_float(ov[8 * x + 6]) * inv_l,
+                                  __uint_as_float(ov[8 * x + 7]) * inv_l);
+            dst[ch * 4 + x] = v4;
+          }
+        }
+      }
+      if (row_valid) {
+        p.lse[(static_cast<size_t>(it.b) * p.H + it.h) * p.S + r] =
+            (m_used + log2f(l_run)) * 0.69314718055994531f;
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
 template <int D, bool kPartial>
 __global__ void __launch_bounds__(kThreads, 1)
     ring_attn_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q,
                           const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_v, const KParams p) {
-  attn_body<D, kPartial, false>(tmap_q, tmap_k, tmap_v, p);
+  attn_body<D, kPartial>(tmap_q, tmap_k, tmap_v, p);
 }
 
 template <int D>
@@ -1004,7 +1518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ring_attn_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q,
                          const __grid_constant__ CUtensorMap tmap_k,
                          const __grid_constant__ CUtensorMap tmap_v, const KParams p) {
-  attn_body<D, false, true>(tmap_q, tmap_k, tmap_v, p);
+  attn_body_fp8<D>(tmap_q, tmap_k, tmap_v, p);
 }
 
 // ---------------------------------------------------------------- host side
@@ -1025,6 +1539,26 @@ bool make_map_vt8(CUtensorMap* m, const void* base, int B, int S, int H, int D) 
   return r == CUDA_SUCCESS;
 }
 
+// Device address of the claim counters (g_work_slots) for the current
+// device, looked up once per device with that device current.
+unsigned long long* work_slots_address() {
+  static std::mutex mu;
+  static unsigned long long* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_work_slots) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<unsigned long long*>(ptr);
+  }
+  return addr[dev];
+}
+
+// Launch epochs: every tensor-core forward launch gets the next one (never
+// 0, the counters' initial tag) and the counter slot epoch % kWorkSlots.
+std::atomic<uint32_t> g_epoch{0};
+
 // Test hook state (see cp_test_set_wait_fault).
 std::atomic<int> g_fault_drop_k{0};
 std::atomic<unsigned long long> g_wait_limit_ns{kTimeoutNs};
@@ -1032,8 +1566,8 @@ std::atomic<unsigned long long> g_wait_limit_ns{kTimeoutNs};
 // With documents the work of a slot (query shard, pair of query tiles) is
 // its number of visible key tiles, which depends on the layout, not on the
 // position: rank the slots by that cost, heaviest first (ties: later slot
-// first, the order used without documents), so the snake deal balances the
-// CTAs.  Every (b, h) shares the layout, so one block ranks the slots of
+// first, the order used without documents), so the CTAs claim the heavy
+// items first and the tail holds only light ones.  Every (b, h) shares the layout, so one block ranks the slots of
 // (b, h) = (0, 0); O(slots^2) compares, used up to kMaxRankedSlots.
 
 __global__ void __launch_bounds__(1024) slot_order_kernel(KParams p, int32_t* __restrict__ perm) {
@@ -1071,7 +1605,7 @@ __global__ void __launch_bounds__(1024) slot_order_kernel(KParams p, int32_t* __
 
 template <int D, bool kPartial, bool kFp8 = false>
 cudaError_t launch_t(const AttnArgs& a, cudaStream_t stream) {
-  using Lay = Layout<D, kFp8 ? 1 : 2>;
+  using Lay = std::conditional_t<kFp8, Fp8Layout, Layout<D, 2>>;
   static_assert(Lay::kAlloc <= 232448, "shared memory budget");
   void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, KParams);
   if constexpr (kFp8)
@@ -1129,18 +1663,23 @@ cudaError_t launch_t(const AttnArgs& a, cudaStream_t stream) {
   if (!p.err) return cudaErrorInvalidValue;
   p.timeout_ns = g_wait_limit_ns.load();
   p.fault_drop_k = g_fault_drop_k.load();
+  unsigned long long* slots = work_slots_address();
+  if (!slots) return cudaErrorInvalidValue;
+  uint32_t epoch = ++g_epoch;
+  if (epoch == 0) epoch = ++g_epoch;
+  p.epoch = epoch;
+  p.work_slot = slots + epoch % kWorkSlots;
   const int grid = static_cast<int>(std::min<long long>(items, sm_count()));
   // Head groups: fewer heads in flight reuse each K/V tile from L2.  A long
   // launch (many rounds of the grid) takes the smallest group whose items
-  // fill CPRING_BALANCE rounds; a short one keeps a single pool, because the
-  // heaviest-first deal only balances the tail when every item is in it.
-  // With documents the live work per item depends on the layout, which stays
-  // on the device, so the item count says nothing about the rounds: one pool.
+  // fill CPRING_BALANCE rounds; a short one keeps a single pool, so that its
+  // lightest items come last.  With documents the item count says little
+  // about the work (the layout decides it), so CPRING_GROUP_DOCS decides.
   {
     const int BH = a.B * a.H;
     const long long slots = static_cast<long long>(p.n_qshards) * p.pairs_per_shard;
     long long hg = BH;
-    if (a.doc_offsets == nullptr &&
+    if ((a.doc_offsets == nullptr || CPRING_GROUP_DOCS) &&
         items >= static_cast<long long>(CPRING_GROUP_MIN_ROUNDS) * grid) {
       hg = (static_cast<long long>(CPRING_BALANCE) * grid + slots - 1) / slots;
       hg = std::max<long long>(1, std::min<long long>(hg, BH));

@@ -9,9 +9,11 @@
 // log-sum-exp m + log l.
 //
 // Both are elementwise over [B, rows, H, d] fp32 state and bound by HBM
-// bandwidth: one warp per (b, row, h) reads its two scalars (m, l) once and
-// streams the d-vector with 16-byte accesses; the grid is a multiple of the
-// SM count and strides over all rows.
+// bandwidth.  A warp takes 32 consecutive rows of one (b, h): the per-row
+// scalars (m, l, lse) are read and written coalesced along [B, H, rows], and
+// the rows' d-vectors stream with 16-byte accesses, several rows in flight
+// per lane.  The grid is a multiple of the SM count and strides over the
+// work.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -41,44 +43,77 @@ __device__ __forceinline__ void merge_factors(float m, float mp, float& a, float
   c = (mp == -INFINITY) ? 0.f : expf(mp - mn);
 }
 
+// Work unit of both kernels: 32 consecutive rows of one (b, h).  Lane i
+// handles the scalars (m, l, lse) of row r0 + i, so those accesses are
+// coalesced along the [B, H, rows] layout; then the warp streams the rows'
+// d-vectors of O ([B, rows, H, d]: one row is d contiguous floats), with the
+// row's factors broadcast by shuffles and kRowsInFlight rows loaded before any
+// is written, so several loads per lane are in flight.
+constexpr int kRowsInFlight = 4;
+
 __global__ void __launch_bounds__(kMergeThreads)
     lse_merge_kernel(float* __restrict__ o_acc, float* __restrict__ m_acc,
                      float* __restrict__ l_acc, const float* __restrict__ o_part,
                      const float* __restrict__ m_part, const float* __restrict__ l_part, int B,
                      int rows, int H, int d, bool vec4) {
   const int lane = threadIdx.x & 31;
-  const long long n = static_cast<long long>(B) * rows * H;
+  const int chunks = (rows + 31) / 32;
+  const long long n_units = static_cast<long long>(B) * H * chunks;
   const long long wstride = static_cast<long long>(gridDim.x) * (kMergeThreads / 32);
-  for (long long w = static_cast<long long>(blockIdx.x) * (kMergeThreads / 32) + (threadIdx.x >> 5);
-       w < n; w += wstride) {
-    // w enumerates (b, row, h) in memory order of O
-    const int h = static_cast<int>(w % H);
-    const long long br = w / H;
-    const int row = static_cast<int>(br % rows);
-    const int b = static_cast<int>(br / rows);
-    const size_t mi = (static_cast<size_t>(b) * H + h) * rows + row;
-    const float m = m_acc[mi], mp = m_part[mi];
-    float a, c, mn;
-    merge_factors(m, mp, a, c, mn);
-    float* o = o_acc + static_cast<size_t>(w) * d;
-    const float* op = o_part + static_cast<size_t>(w) * d;
+  for (long long u = static_cast<long long>(blockIdx.x) * (kMergeThreads / 32) + (threadIdx.x >> 5);
+       u < n_units; u += wstride) {
+    const int chunk = static_cast<int>(u % chunks);
+    const long long bh = u / chunks;
+    const int h = static_cast<int>(bh % H);
+    const int b = static_cast<int>(bh / H);
+    const int r0 = chunk * 32;
+    const int n_rows = min(32, rows - r0);
+    // this lane's row: merge factors and the new (m, l)
+    float a = 0.f, cf = 0.f;
+    if (lane < n_rows) {
+      const size_t mi = static_cast<size_t>(bh) * rows + r0 + lane;
+      const float m = m_acc[mi], mp = m_part[mi];
+      float mn;
+      merge_factors(m, mp, a, cf, mn);
+      l_acc[mi] = l_acc[mi] * a + l_part[mi] * cf;
+      m_acc[mi] = mn;
+    }
+    const size_t row_stride = static_cast<size_t>(H) * d;  // floats between consecutive rows
+    float* o = o_acc + (static_cast<size_t>(b) * rows + r0) * row_stride + static_cast<size_t>(h) * d;
+    const float* op = o_part + (static_cast<size_t>(b) * rows + r0) * row_stride +
+                      static_cast<size_t>(h) * d;
     if (vec4) {
-      for (int x = lane; x < d / 4; x += 32) {
-        float4 u = reinterpret_cast<float4*>(o)[x];
-        const float4 q = reinterpret_cast<const float4*>(op)[x];
-        u.x = u.x * a + q.x * c;
-        u.y = u.y * a + q.y * c;
-        u.z = u.z * a + q.z * c;
-        u.w = u.w * a + q.w * c;
-        reinterpret_cast<float4*>(o)[x] = u;
+      const int nv = d / 4;
+      for (int j0 = 0; j0 < n_rows; j0 += kRowsInFlight) {
+        float4 u4[kRowsInFlight], q4[kRowsInFlight];
+#pragma unroll
+        for (int j = 0; j < kRowsInFlight; ++j) {
+          if (j0 + j < n_rows && lane < nv) {
+            u4[j] = reinterpret_cast<const float4*>(o + (j0 + j) * row_stride)[lane];
+            q4[j] = reinterpret_cast<const float4*>(op + (j0 + j) * row_stride)[lane];
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kRowsInFlight; ++j) {
+          const float aj = __shfl_sync(0xffffffffu, a, (j0 + j) & 31);
+          const float cj = __shfl_sync(0xffffffffu, cf, (j0 + j) & 31);
+          if (j0 + j < n_rows && lane < nv) {
+            float4 v = u4[j];
+            v.x = v.x * aj + q4[j].x * cj;
+            v.y = v.y * aj + q4[j].y * cj;
+            v.z = v.z * aj + q4[j].z * cj;
+            v.w = v.w * aj + q4[j].w * cj;
+            reinterpret_cast<float4*>(o + (j0 + j) * row_stride)[lane] = v;
+          }
+        }
       }
     } else {
-      for (int x = lane; x < d; x += 32) o[x] = o[x] * a + op[x] * c;
-    }
-    __syncwarp();
-    if (lane == 0) {
-      l_acc[mi] = l_acc[mi] * a + l_part[mi] * c;
-      m_acc[mi] = mn;
+      for (int j = 0; j < n_rows; ++j) {
+        const float aj = __shfl_sync(0xffffffffu, a, j);
+        const float cj = __shfl_sync(0xffffffffu, cf, j);
+        for (int x = lane; x < d; x += 32)
+          o[j * row_stride + x] = o[j * row_stride + x] * aj + op[j * row_stride + x] * cj;
+      }
     }
   }
 }
@@ -90,50 +125,72 @@ __global__ void __launch_bounds__(kMergeThreads)
                         float* __restrict__ lse, int B, int rows, int H, int d, bool vec4,
                         long long out_bstride, long long lse_bstride, long long lse_hstride) {
   const int lane = threadIdx.x & 31;
-  const long long n = static_cast<long long>(B) * rows * H;
+  const int chunks = (rows + 31) / 32;
+  const long long n_units = static_cast<long long>(B) * H * chunks;
   const long long wstride = static_cast<long long>(gridDim.x) * (kMergeThreads / 32);
-  for (long long w = static_cast<long long>(blockIdx.x) * (kMergeThreads / 32) + (threadIdx.x >> 5);
-       w < n; w += wstride) {
-    const int h = static_cast<int>(w % H);
-    const long long br = w / H;
-    const int row = static_cast<int>(br % rows);
-    const int b = static_cast<int>(br / rows);
-    const size_t mi = (static_cast<size_t>(b) * H + h) * rows + row;
-    const float l = l_acc[mi];
-    const float inv = (l > 0.f) ? 1.f / l : 0.f;
-    const float* o = o_acc + static_cast<size_t>(w) * d;
-    const size_t orow = static_cast<size_t>(b) * out_bstride + (static_cast<size_t>(row) * H + h) * d;
-    if (kBf16) {
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(out) + orow;
-      if (vec4) {
-        for (int x = lane; x < d / 4; x += 32) {
-          const float4 u = reinterpret_cast<const float4*>(o)[x];
-          __nv_bfloat162 lo = __floats2bfloat162_rn(u.x * inv, u.y * inv);
-          __nv_bfloat162 hi = __floats2bfloat162_rn(u.z * inv, u.w * inv);
-          reinterpret_cast<__nv_bfloat162*>(dst)[2 * x] = lo;
-          reinterpret_cast<__nv_bfloat162*>(dst)[2 * x + 1] = hi;
+  for (long long u = static_cast<long long>(blockIdx.x) * (kMergeThreads / 32) + (threadIdx.x >> 5);
+       u < n_units; u += wstride) {
+    const int chunk = static_cast<int>(u % chunks);
+    const long long bh = u / chunks;
+    const int h = static_cast<int>(bh % H);
+    const int b = static_cast<int>(bh / H);
+    const int r0 = chunk * 32;
+    const int n_rows = min(32, rows - r0);
+    float inv = 0.f;
+    if (lane < n_rows) {
+      const size_t mi = static_cast<size_t>(bh) * rows + r0 + lane;
+      const float l = l_acc[mi];
+      inv = (l > 0.f) ? 1.f / l : 0.f;
+      lse[static_cast<size_t>(b) * lse_bstride + static_cast<size_t>(h) * lse_hstride + r0 + lane] =
+          (l > 0.f) ? m_acc[mi] + logf(l) : -INFINITY;
+    }
+    const size_t row_stride = static_cast<size_t>(H) * d;
+    const float* o = o_acc + (static_cast<size_t>(b) * rows + r0) * row_stride +
+                     static_cast<size_t>(h) * d;
+    const size_t orow0 = static_cast<size_t>(b) * out_bstride +
+                         (static_cast<size_t>(r0) * H + h) * d;
+    if (vec4) {
+      const int nv = d / 4;
+      for (int j0 = 0; j0 < n_rows; j0 += kRowsInFlight) {
+        float4 u4[kRowsInFlight];
+#pragma unroll
+        for (int j = 0; j < kRowsInFlight; ++j)
+          if (j0 + j < n_rows && lane < nv)
+            u4[j] = reinterpret_cast<const float4*>(o + (j0 + j) * row_stride)[lane];
+#pragma unroll
+        for (int j = 0; j < kRowsInFlight; ++j) {
+          const float ij = __shfl_sync(0xffffffffu, inv, (j0 + j) & 31);
+          if (j0 + j < n_rows && lane < nv) {
+            const size_t orow = orow0 + (j0 + j) * row_stride;
+            if (kBf16) {
+              __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(out) + orow;
+              __nv_bfloat162 lo = __floats2bfloat162_rn(u4[j].x * ij, u4[j].y * ij);
+              __nv_bfloat162 hi = __floats2bfloat162_rn(u4[j].z * ij, u4[j].w * ij);
+              uint2 pk;
+              pk.x = *reinterpret_cast<uint32_t*>(&lo);
+              pk.y = *reinterpret_cast<uint32_t*>(&hi);
+              reinterpret_cast<uint2*>(dst)[lane] = pk;
+            } else {
+              float* dst = static_cast<float*>(out) + orow;
+              reinterpret_cast<float4*>(dst)[lane] =
+                  make_float4(u4[j].x * ij, u4[j].y * ij, u4[j].z * ij, u4[j].w * ij);
+            }
+          }
         }
-      } else {
-        for (int x = lane; x < d; x += 32) dst[x] = __float2bfloat16_rn(o[x] * inv);
       }
     } else {
-      float* dst = static_cast<float*>(out) + orow;
-      if (vec4) {
-        for (int x = lane; x < d / 4; x += 32) {
-          float4 u = reinterpret_cast<const float4*>(o)[x];
-          u.x *= inv;
-          u.y *= inv;
-          u.z *= inv;
-          u.w *= inv;
-          reinterpret_cast<float4*>(dst)[x] = u;
+      for (int j = 0; j < n_rows; ++j) {
+        const float ij = __shfl_sync(0xffffffffu, inv, j);
+        const size_t orow = orow0 + j * row_stride;
+        for (int x = lane; x < d; x += 32) {
+          const float val = o[j * row_stride + x] * ij;
+          if (kBf16)
+            static_cast<__nv_bfloat16*>(out)[orow + x] = __float2bfloat16_rn(val);
+          else
+            static_cast<float*>(out)[orow + x] = val;
         }
-      } else {
-        for (int x = lane; x < d; x += 32) dst[x] = o[x] * inv;
       }
     }
-    if (lane == 0)
-      lse[static_cast<size_t>(b) * lse_bstride + static_cast<size_t>(h) * lse_hstride + row] =
-          (l > 0.f) ? m_acc[mi] + logf(l) : -INFINITY;
   }
 }
 
@@ -231,7 +288,7 @@ cudaError_t launch_doc_scan(const int32_t* doc_offsets, int S, int32_t* doc_info
 cudaError_t launch_merge(float* o_acc, float* m_acc, float* l_acc, const float* o_part,
                          const float* m_part, const float* l_part, int B, int rows, int H, int d,
                          cudaStream_t stream) {
-  const long long n = static_cast<long long>(B) * rows * H;
+  const long long n = static_cast<long long>(B) * H * ((rows + 31) / 32);  // warp units
   const bool vec4 = (d % 4 == 0) && ((reinterpret_cast<uintptr_t>(o_acc) |
                                        reinterpret_cast<uintptr_t>(o_part)) % 16 == 0);
   lse_merge_kernel<<<grid_for(n), kMergeThreads, 0, stream>>>(o_acc, m_acc, l_acc, o_part, m_part,
@@ -244,7 +301,7 @@ cudaError_t launch_finalize_strided(const float* o_acc, const float* m_acc, cons
                                     void* out, float* lse, int B, int rows, int H, int d,
                                     int out_is_bf16, long long out_bstride, long long lse_bstride,
                                     long long lse_hstride, cudaStream_t stream) {
-  const long long n = static_cast<long long>(B) * rows * H;
+  const long long n = static_cast<long long>(B) * H * ((rows + 31) / 32);  // warp units
   const size_t esz = out_is_bf16 ? 2 : 4;
   const bool vec4 = (d % 4 == 0) &&
                     ((reinterpret_cast<uintptr_t>(o_acc) | reinterpret_cast<uintptr_t>(out)) % 16 == 0) &&

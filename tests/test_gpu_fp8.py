@@ -176,9 +176,9 @@ def test_fp8_deterministic_and_shard_count_within_tolerance():
 
 
 def test_fp8_workload_causal_128k_sampled():
-    """bf16 causal 128K (B=1 S=131072 H=32 d=128 N=4) stored as FP8: seeded
-    query rows of every eighth head against the oracle, and Q = 0 against the
-    prefix mean on the same heads."""
+    """bf16 causal 128K (B=1 S=131072 H=32 d=128 N=4) stored as FP8: 512
+    seeded query rows of every head against the oracle, and Q = 0 against the
+    prefix mean on every row of every fourth head."""
     w = inputs.BY_NAME["bf16_causal_128k"]
     q, k, v = inputs.make_qkv(w.B, w.S, w.H, w.d, w.seed, torch.bfloat16, w.scale, device=DEV)
     fp8 = pkg.fp8_quantize_qkv(q, k, v)
@@ -191,17 +191,19 @@ def test_fp8_workload_causal_128k_sampled():
     qdn, kdn, vdn = _np(qd), _np(kd), _np(vd)
     del q, k, v, zero
     errs_l = []
-    for h in range(0, w.H, 8):
+    for h in range(w.H):
         one = lambda x8, s: ref.fp8_dequantize(x8[None, :, None, :], np.array([[s]], np.float32))
         qh = one(_values(q8[0, :, h, :]), qdn[0, h])
         kh = one(_values(k8[0, :, h, :]), kdn[0, h])
         vh = one(np.ascontiguousarray(_values(v8t[0, h]).T), vdn[0, h])
-        rows = inputs.sample_rows(w.S, 256, seed=w.seed * 100 + h)
+        rows = inputs.sample_rows(w.S, 512, seed=w.seed * 100 + h)
         wo, wl = ref.attention_rows(qh, kh, vh, 0, 0, rows, w.causal, None)
         vmax = np.abs(vh).max()
         e = np.abs(on[0, rows, h] - wo)
         assert e.max() <= FP8_MAX_REL * vmax and e.mean() <= FP8_MEAN_REL * vmax, (h, e.max())
         errs_l.append(np.abs(ln[0, h, rows] - wl).max())
+        if h % 4:
+            continue
         cf_o, cf_l = ref.zero_query_closed_form(vh, w.causal, None)
         e0 = np.abs(on0[0, :, h] - cf_o[0, :, 0])
         assert e0.max() <= BF16_MAX and e0.mean() <= BF16_MEAN, (h, e0.max())
