@@ -84,7 +84,8 @@ struct BLayout {
   static constexpr int kX1 = kX0 + kX0Slots * kTileBytes;
   static constexpr int kVec = kX1 + kX1Slots * kTileBytes;    // kDKDV: [2][-lse2, -D][128] fp32
   static constexpr int kBar = kVec + (kDKDV ? 2 * 2 * kT * 4 : 0);
-  static constexpr int kBytes = kBar + 256;
+  static constexpr int kRingOff = kBar + 256;  // the item ring
+  static constexpr int kBytes = kRingOff + 256;
   static constexpr int kAlloc = kBytes + 1024;
   __host__ __device__ static constexpr int x0(int slot) { return kX0 + slot * kTileBytes; }
   __host__ __device__ static constexpr int x1(int slot) { return kX1 + slot * kTileBytes; }
@@ -129,6 +130,8 @@ struct BParams {
   int* err;
   unsigned long long timeout_ns;
   int fault_drop;       // test hook: CTA 0 never loads its first streamed X0 tile
+  unsigned long long* work_slot;  // this launch's claim counter (see claim_first)
+  uint32_t epoch;                 // this launch's tag in that counter
 };
 
 struct BItem {
@@ -137,11 +140,11 @@ struct BItem {
   int x_lo, x_hi;    // flattened streamed tile range
 };
 
-// Item w: items are dealt head group by head group (head_group (b, h) heads
-// at a time, so the CTAs in flight stream the tiles of few heads and re-read
-// them from L2), and inside a group heaviest slot first (under causality the
-// last query tiles see the most keys and the first key tiles are seen by the
-// most queries).
+// Item w: items are laid out head group by head group (head_group (b, h)
+// heads at a time, so the CTAs in flight stream the tiles of few heads and
+// re-read them from L2), and inside a group heaviest slot first (under
+// causality the last query tiles see the most keys and the first key tiles
+// are seen by the most queries); CTAs claim them in that order.
 template <bool kDKDV>
 __device__ __forceinline__ void decode_bitem(const BParams& p, int n_docs, int w, BItem& it) {
   const int BH = p.B * p.H;
@@ -183,6 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kBar + kTmemSlot);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Lay::kBar + kAbortSlot);
   float* vec = reinterpret_cast<float*>(smem + Lay::kVec);
+  const ItemRing ring{sbase + Lay::kRingOff,
+                      reinterpret_cast<volatile int*>(smem + Lay::kRingOff + 2 * kRing * 8)};
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -217,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(bar(kPReadyS), kSoftmaxThreads);
     ptx::mbar_init(bar(kPReadyS + 1), kSoftmaxThreads);
     ptx::mbar_init(bar(kDrain), 1);
+    ring_init(ring);
     *abort_flag = 0u;
     ptx::fence_barrier_init();
   }
@@ -244,11 +250,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tma_prefetch_desc(&tm_x1);
       uint32_t x_iter = 0, fix_iter = 0;
       uint32_t armed0[3] = {0u, 0u, 0u}, armed1[2] = {0u, 0u};  // loads started per slot
+      unsigned long long ahead = 0;  // the claim of the CTA's next item
       bool dropped = false;
       bool ok = true;
       for (int k = 0; ok; ++k) {
-        const int w = item_of(k, c, G);
+        const int w = !CPRING_DYNAMIC ? item_of(k, c, G)
+                      : (k == 0) ? c : G + claimed_index(ahead, p.epoch, p.err);
+        if (!ring_put(ring, static_cast<uint32_t>(k), w, abort_flag, p)) { ok = false; break; }
         if (w >= p.n_items) break;
+        if (CPRING_DYNAMIC)  // claim the CTA's next item now; it is read when that item starts
+          ahead = (k == 0) ? claim_first(p.work_slot, p.epoch) : claim_next(p.work_slot);
         BItem it;
         decode_bitem<kDKDV>(p, n_docs, w, it);
         if (!wait1(bar(kFixEmpty), (fix_iter & 1u) ^ 1u, abort_flag, p)) { ok = false; break; }
@@ -352,7 +363,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       for (int k = 0; ok; ++k) {
-        const int w = item_of(k, c, G);
+        const int w = ring_get(ring, static_cast<uint32_t>(k), abort_flag, p);
+        if (w < 0) { ok = false; break; }
         if (w >= p.n_items) break;
         BItem it;
         decode_bitem<kDKDV>(p, n_docs, w, it);
@@ -463,7 +475,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t s_cnt = 0, item_cnt = 0, h_cnt = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const int w = item_of(k, c, G);
+      const int w = ring_get(ring, static_cast<uint32_t>(k), abort_flag, p);
+      if (w < 0) { ok = false; break; }
       if (w >= p.n_items) break;
       BItem it;
       decode_bitem<kDKDV>(p, n_docs, w, it);
@@ -776,10 +789,16 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
   if (!p.err) return cudaErrorInvalidValue;
   p.timeout_ns = test_wait_limit_ns();
   p.fault_drop = test_fault_drop();
+  unsigned long long* slots = work_slots_address();
+  if (!slots) return cudaErrorInvalidValue;
+  const uint32_t epoch = next_epoch(slots);
+  if (epoch == 0) return cudaErrorInvalidValue;
+  p.epoch = epoch;
+  p.work_slot = slots + epoch % kWorkSlots;
   const int grid = static_cast<int>(std::min<long long>(items, sm_count()));
   // Head groups as in the forward: a launch with at least 16 rounds of the
   // grid and no document layout takes the smallest group whose items fill
-  // two rounds; otherwise one pool keeps the heaviest-first deal balanced.
+  // two rounds; otherwise one pool, so that the lightest items come last.
   {
     const int BH = a.B * a.H;
     long long hg = BH;

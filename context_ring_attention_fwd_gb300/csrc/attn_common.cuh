@@ -1,14 +1,16 @@
 // Device helpers shared by the tcgen05 attention kernels (forward and
 // backward): the shard-aligned tiling of the sequence, the document of a
-// token, the snake deal of work items to persistent CTAs, and the bounded
-// mbarrier waits.  Templates over the kernel's parameter struct, which must
-// provide S, L (shard length), tiles_per_shard, doc_offsets, timeout_ns and
-// err.
+// token, the claiming of work items by persistent CTAs (and the fixed snake
+// deal it replaced), and the bounded mbarrier waits.  Templates over the
+// kernel's parameter struct, which must provide S, L (shard length),
+// tiles_per_shard, doc_offsets, timeout_ns and err.
 #pragma once
 
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <climits>
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -107,6 +109,100 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity,
   }
 }
 
+// ---------------------------------------------------------------- work queue
+// Work items of the persistent tcgen05 kernels are claimed at run time.  CTA
+// c starts with item c; every later item comes from a counter the launch's
+// CTAs share, in the order the kernel lays its items out (heaviest first),
+// so a CTA that finishes early takes more work and the tail stays short
+// whatever the items cost.  The counter is one of kWorkSlots 64-bit
+// slots of a device array that launches use in turn; a slot holds
+// (launch epoch << 32 | next index), and epochs only grow, so no launch
+// clears it and none allocates it.  At most kWorkSlots launches can run at
+// once on a device before one would reuse the slot of another still running.
+constexpr int kWorkSlots = 256;
+__device__ unsigned long long g_work_slots[kWorkSlots];
+// Tuning switch: CTAs claim items from the launch's counter (1) or take them
+// in the fixed snake order of item_of (0).
+#ifndef CPRING_DYNAMIC
+#define CPRING_DYNAMIC 1
+#endif
+
+// A CTA's first claim of a launch: raise the slot to (epoch << 32 | 0) if it
+// still holds an older launch's tag (an atomic max leaves this launch's
+// running count alone), then take the next index with one atomic add.  Both
+// are single atomics to one address, so 152 CTAs claiming at once cost no
+// retries.  The result is read only when the item starts.
+__device__ __forceinline__ unsigned long long claim_first(unsigned long long* slot, uint32_t epoch) {
+  atomicMax(slot, static_cast<unsigned long long>(epoch) << 32);
+  return atomicAdd(slot, 1ull);
+}
+
+// A CTA's later claims: the slot carries this launch's tag already.  The
+// producer issues each one item ahead, so the atomic's latency hides behind
+// the current item's loads.
+__device__ __forceinline__ unsigned long long claim_next(unsigned long long* slot) {
+  return atomicAdd(slot, 1ull);
+}
+
+// The item index of a claim, or past every item (with the error word set)
+// if the slot did not carry this launch's tag, which only another launch
+// using the same slot at the same time could cause.
+__device__ __forceinline__ int claimed_index(unsigned long long v, uint32_t epoch, int* err) {
+  if (static_cast<uint32_t>(v >> 32) != epoch) {
+    atomicOr(err, kErrTimeout);
+    return INT_MAX / 2;
+  }
+  return static_cast<int>(v & 0xffffffffull);
+}
+
+// The CTA's ring of claimed item indices: the producer publishes each item
+// it claims (its k-th item in slot k % kRing); the MMA warp and the eight
+// softmax warps read them in the same order, so every role walks the same
+// items.  Full barriers take the producer's arrival, empty ones one arrival
+// per reading warp.
+constexpr int kRing = 4;
+constexpr int kRingReaders = 9;  // the MMA warp and the eight softmax warps
+constexpr int kRingBytes = 2 * kRing * 8 + kRing * 4;
+static_assert(kRingBytes <= 256, "the item ring's shared-memory block");
+
+struct ItemRing {
+  uint32_t bars;      // shared address: kRing full barriers, then kRing empty barriers
+  volatile int* idx;  // kRing item indices
+  __device__ uint32_t full(int s) const { return bars + 8u * static_cast<uint32_t>(s); }
+  __device__ uint32_t empty(int s) const { return bars + 8u * static_cast<uint32_t>(kRing + s); }
+};
+
+__device__ __forceinline__ void ring_init(const ItemRing& r) {
+  for (int s = 0; s < kRing; ++s) {
+    ptx::mbar_init(r.full(s), 1);
+    ptx::mbar_init(r.empty(s), kRingReaders);
+  }
+}
+
+// Producer (one thread): publish w as the CTA's k-th item.
+template <class P>
+__device__ __forceinline__ bool ring_put(const ItemRing& r, uint32_t k, int w,
+                                         volatile uint32_t* abort_flag, const P& p) {
+  const int s = static_cast<int>(k % kRing);
+  const uint32_t use = k / kRing;
+  if (use > 0 && !wait1(r.empty(s), (use - 1) & 1u, abort_flag, p)) return false;
+  r.idx[s] = w;
+  ptx::mbar_arrive(r.full(s));
+  return true;
+}
+
+// A reading warp (every lane): the CTA's k-th item, or -1 if the wait gave up.
+template <class P>
+__device__ __forceinline__ int ring_get(const ItemRing& r, uint32_t k,
+                                        volatile uint32_t* abort_flag, const P& p) {
+  const int s = static_cast<int>(k % kRing);
+  if (!wait_warp(r.full(s), (k / kRing) & 1u, abort_flag, p)) return -1;
+  const int w = r.idx[s];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(r.empty(s));
+  return w;
+}
+
 // ---------------------------------------------------------------- host side
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link
 // against libcuda).
@@ -146,6 +242,45 @@ bool make_map(CUtensorMap* m, const void* base, int B, int S, int H, int D, int 
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// Device address of the claim counters (g_work_slots) for the current
+// device, looked up once per device with that device current.
+unsigned long long* work_slots_address() {
+  static std::mutex mu;
+  static unsigned long long* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_work_slots) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<unsigned long long*>(ptr);
+  }
+  return addr[dev];
+}
+
+// Launch epochs, per device: every launch that claims items gets the next one
+// and the counter slot epoch % kWorkSlots.  Epoch 0 is the counters'
+// initial tag and is never handed out; when the count wraps (after 2^32 - 1
+// launches) the device is synchronised and its counters cleared, because a
+// claim can only raise a slot's tag.
+std::atomic<uint32_t> g_epoch[64];
+
+// The next epoch of the current device, or 0 if clearing the counters failed.
+uint32_t next_epoch(unsigned long long* slots) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  uint32_t e = ++g_epoch[dev];
+  if (e == 0) {
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemset(slots, 0, sizeof(unsigned long long) * kWorkSlots) != cudaSuccess)
+      return 0;
+    e = ++g_epoch[dev];
+  }
+  return e;
 }
 
 }  // namespace

@@ -84,8 +84,9 @@ constexpr float kRescaleLog2 = 8.0f;
 //  CPRING_GROUP_MIN_ROUNDS ... when the launch has at least this many rounds;
 //                          shorter launches deal every item from one pool.
 //  CPRING_GROUP_DOCS       launches with documents group heads too.
-//  CPRING_DYNAMIC          CTAs claim items from the launch's counter (1) or
-//                          take them in a fixed snake order (0).
+//  CPRING_DYNAMIC          (attn_common.cuh) CTAs claim items from the
+//                          launch's counter (1) or take them in a fixed snake
+//                          order (0).
 //  CPRING_FUSED_NOMAX      fused forward only: after the first tile, skip the
 //                          row max and redo a tile only if its first 64 keys'
 //                          row sum or its last 64 keys' row max shows an
@@ -98,6 +99,11 @@ constexpr float kRescaleLog2 = 8.0f;
 //  CPRING_FP8_FAST         the FP8 kernel uses the same no-max fast pass, with
 //                          the guards at 2^8 so that every P it keeps is at
 //                          most 2^8, inside E4M3's range (448).
+//  CPRING_FP8_EVENT        the FP8 MMA warp issues each query tile's S and PV
+//                          as soon as that tile's inputs are ready, polling
+//                          both tiles, instead of in a fixed interleaved
+//                          order (the tiles then drift apart by up to the
+//                          K/V ring's depth).
 //  CPRING_FP8_EARLY_SFREE  the FP8 softmax releases a tile's S columns as
 //                          soon as it has loaded them (the rare redo then
 //                          works from the scores kept in registers) instead
@@ -111,9 +117,6 @@ constexpr float kRescaleLog2 = 8.0f;
 #ifndef CPRING_GROUP_DOCS
 #define CPRING_GROUP_DOCS 0
 #endif
-#ifndef CPRING_DYNAMIC
-#define CPRING_DYNAMIC 1
-#endif
 #ifndef CPRING_FUSED_NOMAX
 #define CPRING_FUSED_NOMAX 1
 #endif
@@ -125,6 +128,9 @@ constexpr float kRescaleLog2 = 8.0f;
 #endif
 #ifndef CPRING_FP8_EARLY_SFREE
 #define CPRING_FP8_EARLY_SFREE 0
+#endif
+#ifndef CPRING_FP8_EVENT
+#define CPRING_FP8_EVENT 0
 #endif
 constexpr int kPReadyCount = 128;
 constexpr float kOverflowGuard = 18446744073709551616.0f;  // 2^64
@@ -187,7 +193,7 @@ struct KParams {
   int kv_row0;       // key index of row 0 of the K/V tensors (0 unless a block)
   int head_group;    // (b, h) heads whose items are dealt out together
   const int32_t* slot_perm;  // or null: slots heaviest first by measured cost
-  unsigned long long* work_slot;  // this launch's claim counter (see claim_item)
+  unsigned long long* work_slot;  // this launch's claim counter (see claim_first)
   uint32_t epoch;                 // this launch's tag in that counter
   const float* q_descale;  // FP8 form: [B * H] each
   const float* k_descale;
@@ -258,83 +264,6 @@ __device__ __forceinline__ void decode_item(const KParams& p, int n_docs, int w,
       }
     }
   }
-}
-
-// ---------------------------------------------------------------- work queue
-// Work items are claimed at run time.  CTA c starts with item c; every later
-// item comes from a counter the launch's CTAs share, in the order
-// decode_item lays out (head group by head group, heaviest first inside
-// each), so a CTA that finishes early takes more work and the tail stays
-// short whatever the items cost.  The counter is one of kWorkSlots 64-bit
-// slots of a device array that launches use in turn; a slot holds
-// (launch epoch << 32 | next index), and the first claim of a launch that
-// finds another epoch there restarts it, so no launch clears it and no
-// launch allocates it.  At most kWorkSlots launches can run at once on a
-// device before one would reuse the slot of another still running.
-constexpr int kWorkSlots = 256;
-__device__ unsigned long long g_work_slots[kWorkSlots];
-
-// The next index of this launch's counter (0, 1, 2, ...).  A lock-free retry:
-// each failed compare-and-swap means another CTA claimed one, so the loop
-// ends; the bound only guards against a slot shared with a runaway launch.
-__device__ __forceinline__ int claim_item(unsigned long long* slot, uint32_t epoch, int* err) {
-  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(slot);
-  for (int attempt = 0; attempt < (1 << 20); ++attempt) {
-    const bool mine = static_cast<uint32_t>(cur >> 32) == epoch;
-    const unsigned long long want =
-        mine ? cur + 1 : ((static_cast<unsigned long long>(epoch) << 32) | 1ull);
-    const unsigned long long prev = atomicCAS(slot, cur, want);
-    if (prev == cur) return mine ? static_cast<int>(cur & 0xffffffffull) : 0;
-    cur = prev;
-  }
-  atomicOr(err, kErrTimeout);
-  return INT_MAX / 2;  // past every item: the CTA stops
-}
-
-// The CTA's ring of claimed item indices: the producer publishes each item
-// it claims (its k-th item in slot k % kRing); the MMA warp and the eight
-// softmax warps read them in the same order, so every role walks the same
-// items.  Full barriers take the producer's arrival, empty ones one arrival
-// per reading warp.
-constexpr int kRing = 4;
-constexpr int kRingReaders = 9;  // the MMA warp and the eight softmax warps
-constexpr int kRingBytes = 2 * kRing * 8 + kRing * 4;
-static_assert(kRingBytes <= 256, "the item ring's shared-memory block");
-
-struct ItemRing {
-  uint32_t bars;      // shared address: kRing full barriers, then kRing empty barriers
-  volatile int* idx;  // kRing item indices
-  __device__ uint32_t full(int s) const { return bars + 8u * static_cast<uint32_t>(s); }
-  __device__ uint32_t empty(int s) const { return bars + 8u * static_cast<uint32_t>(kRing + s); }
-};
-
-__device__ __forceinline__ void ring_init(const ItemRing& r) {
-  for (int s = 0; s < kRing; ++s) {
-    ptx::mbar_init(r.full(s), 1);
-    ptx::mbar_init(r.empty(s), kRingReaders);
-  }
-}
-
-// Producer (one thread): publish w as the CTA's k-th item.
-__device__ __forceinline__ bool ring_put(const ItemRing& r, uint32_t k, int w,
-                                         volatile uint32_t* abort_flag, const KParams& p) {
-  const int s = static_cast<int>(k % kRing);
-  const uint32_t use = k / kRing;
-  if (use > 0 && !wait1(r.empty(s), (use - 1) & 1u, abort_flag, p)) return false;
-  r.idx[s] = w;
-  ptx::mbar_arrive(r.full(s));
-  return true;
-}
-
-// A reading warp (every lane): the CTA's k-th item, or -1 if the wait gave up.
-__device__ __forceinline__ int ring_get(const ItemRing& r, uint32_t k,
-                                        volatile uint32_t* abort_flag, const KParams& p) {
-  const int s = static_cast<int>(k % kRing);
-  if (!wait_warp(r.full(s), (k / kRing) & 1u, abort_flag, p)) return -1;
-  const int w = r.idx[s];
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(r.empty(s));
-  return w;
 }
 
 // ---------------------------------------------------------------- softmax pieces
@@ -605,15 +534,18 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
       ptx::tma_prefetch_desc(&tmap_k);
       ptx::tma_prefetch_desc(&tmap_v);
       uint32_t kv_iter = 0, q_iter = 0;
+      unsigned long long ahead = 0;  // the claim of the CTA's next item
       // Loads started into each stage: the n-th one completes phase n - 1.
       uint32_t k_armed0 = 0, k_armed1 = 0, v_armed0 = 0, v_armed1 = 0;
       bool dropped = false;
       bool ok = true;
       for (int k = 0; ok; ++k) {
         const int w = !CPRING_DYNAMIC ? item_of(k, c, G)
-                      : (k == 0) ? c : G + claim_item(p.work_slot, p.epoch, p.err);
+                      : (k == 0) ? c : G + claimed_index(ahead, p.epoch, p.err);
         if (!ring_put(ring, static_cast<uint32_t>(k), w, abort_flag, p)) { ok = false; break; }
         if (w >= p.n_items) break;
+        if (CPRING_DYNAMIC)  // claim the CTA's next item now; it is read when that item starts
+          ahead = (k == 0) ? claim_first(p.work_slot, p.epoch) : claim_next(p.work_slot);
         Item it;
         decode_item(p, n_docs, w, it);
         if (it.F_lo > it.F_hi) continue;
@@ -1157,6 +1089,7 @@ __device__ __forceinline__ void attn_body_fp8(const CUtensorMap& tmap_q, const C
       ptx::tma_prefetch_desc(&tmap_k);
       ptx::tma_prefetch_desc(&tmap_v);
       uint32_t kv_iter = 0, q_iter = 0;
+      unsigned long long ahead = 0;  // the claim of the CTA's next item
       // Loads started into each stage (the n-th completes phase n - 1), held
       // in registers: a runtime index into a local array would live in memory.
       uint32_t k_armed0 = 0, k_armed1 = 0, k_armed2 = 0;
@@ -1168,9 +1101,11 @@ __device__ __forceinline__ void attn_body_fp8(const CUtensorMap& tmap_q, const C
       bool ok = true;
       for (int k = 0; ok; ++k) {
         const int w = !CPRING_DYNAMIC ? item_of(k, c, G)
-                      : (k == 0) ? c : G + claim_item(p.work_slot, p.epoch, p.err);
+                      : (k == 0) ? c : G + claimed_index(ahead, p.epoch, p.err);
         if (!ring_put(ring, static_cast<uint32_t>(k), w, abort_flag, p)) { ok = false; break; }
         if (w >= p.n_items) break;
+        if (CPRING_DYNAMIC)  // claim the CTA's next item now; it is read when that item starts
+          ahead = (k == 0) ? claim_first(p.work_slot, p.epoch) : claim_next(p.work_slot);
         Item it;
         decode_item(p, n_docs, w, it);
         if (it.F_lo > it.F_hi) continue;
@@ -1278,6 +1213,96 @@ __device__ __forceinline__ void attn_body_fp8(const CUtensorMap& tmap_q, const C
         if (!wait_warp(bar(k8QFull), q_iter & 1u, abort_flag, p)) { ok = false; break; }
         ++q_iter;
         ptx::tc_fence_after();
+#if CPRING_FP8_EVENT
+        {
+          // Per query tile: the next key tile whose S, and whose PV, is owed.
+          // A K (V) stage is released once every tile that visits its key
+          // tile has issued that S (PV); releases go out in key-tile order.
+          int s0 = it.f_lo[0], s1 = it.f_lo[1], v0 = it.f_lo[0], v1 = it.f_lo[1];
+          int k_rel = it.F_lo, v_rel = it.F_lo;
+          bool first0 = true, first1 = true, q_released = false;
+          auto stage = [&](int f) { return (kv_iter + static_cast<uint32_t>(f - it.F_lo)) % kStages8; };
+          auto phase = [&](int f) {
+            return ((kv_iter + static_cast<uint32_t>(f - it.F_lo)) / kStages8) & 1u;
+          };
+          auto ready = [&](uint32_t b, uint32_t ph) {
+            return __all_sync(0xffffffffu, ptx::mbar_test_wait(b, ph));
+          };
+          uint64_t idle_since = 0;
+          uint32_t idle = 0;
+          for (;;) {
+            bool moved = false;
+            // S of each tile: its softmax released the previous S, K is in
+            if (s0 <= it.f_hi[0] && (s_issued0 == 0 || ready(bar(k8SFree + 0), (s_issued0 - 1) & 1u)) &&
+                ready(bar(k8KFull + stage(s0)), phase(s0))) {
+              ptx::tc_fence_after();
+              if (!issue_s(0, s_issued0, stage(s0))) { ok = false; break; }
+              ++s0;
+              moved = true;
+            }
+            if (s1 <= it.f_hi[1] && (s_issued1 == 0 || ready(bar(k8SFree + 1), (s_issued1 - 1) & 1u)) &&
+                ready(bar(k8KFull + stage(s1)), phase(s1))) {
+              ptx::tc_fence_after();
+              if (!issue_s(1, s_issued1, stage(s1))) { ok = false; break; }
+              ++s1;
+              moved = true;
+            }
+            while (k_rel <= it.F_hi &&
+                   (k_rel < it.f_lo[0] || k_rel > it.f_hi[0] || s0 > k_rel) &&
+                   (k_rel < it.f_lo[1] || k_rel > it.f_hi[1] || s1 > k_rel)) {
+              ptx::mma_commit_w(bar(k8KEmpty + stage(k_rel)));  // K read by every S of it
+              ++k_rel;
+            }
+            if (!q_released && s0 > it.f_hi[0] && s1 > it.f_hi[1]) {
+              ptx::mma_commit_w(bar(k8QEmpty));  // every S of this item has been issued
+              q_released = true;
+            }
+            // PV of each tile: its P landed, V is in
+            if (v0 < s0 && ready(bar(k8PReady + (pv_issued0 & 1u)), (pv_issued0 >> 1) & 1u) &&
+                ready(bar(k8VFull + stage(v0)), phase(v0))) {
+              if (!issue_pv(0, pv_issued0, stage(v0), first0, v0 == it.f_hi[0])) { ok = false; break; }
+              ++v0;
+              moved = true;
+            }
+            if (v1 < s1 && ready(bar(k8PReady + 2 + (pv_issued1 & 1u)), (pv_issued1 >> 1) & 1u) &&
+                ready(bar(k8VFull + stage(v1)), phase(v1))) {
+              if (!issue_pv(1, pv_issued1, stage(v1), first1, v1 == it.f_hi[1])) { ok = false; break; }
+              ++v1;
+              moved = true;
+            }
+            while (v_rel <= it.F_hi &&
+                   (v_rel < it.f_lo[0] || v_rel > it.f_hi[0] || v0 > v_rel) &&
+                   (v_rel < it.f_lo[1] || v_rel > it.f_hi[1] || v1 > v_rel)) {
+              ptx::mma_commit_w(bar(k8VEmpty + stage(v_rel)));  // V read by every PV of it
+              ++v_rel;
+            }
+            if (v_rel > it.F_hi && k_rel > it.F_hi && q_released) break;  // the item is issued
+            if (moved) {
+              idle = 0;
+              continue;
+            }
+            // Nothing was ready: a bounded wait, as in wait_warp.
+            if (__any_sync(0xffffffffu, *abort_flag != 0u)) { ok = false; break; }
+            if ((++idle & 255u) == 0) {
+              int tout = 0;
+              if (lane == 0) {
+                const uint64_t now = ptx::globaltimer();
+                if (idle_since == 0) {
+                  idle_since = now;
+                } else if (now - idle_since > p.timeout_ns) {
+                  *abort_flag = 1u;
+                  atomicOr(p.err, kErrTimeout);
+                  tout = 1;
+                }
+              }
+              if (__shfl_sync(0xffffffffu, tout, 0)) { ok = false; break; }
+            }
+          }
+          if (!ok) break;
+          kv_iter += static_cast<uint32_t>(it.F_hi - it.F_lo + 1);
+          continue;
+        }
+#endif
         bool pend0 = false, pend1 = false;    // S issued whose PV is still owed
         bool first0 = true, first1 = true;    // next PV overwrites O
         uint32_t prev_st = 0, prev_ph = 0;
@@ -1539,26 +1564,6 @@ bool make_map_vt8(CUtensorMap* m, const void* base, int B, int S, int H, int D) 
   return r == CUDA_SUCCESS;
 }
 
-// Device address of the claim counters (g_work_slots) for the current
-// device, looked up once per device with that device current.
-unsigned long long* work_slots_address() {
-  static std::mutex mu;
-  static unsigned long long* addr[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_work_slots) != cudaSuccess) return nullptr;
-    addr[dev] = static_cast<unsigned long long*>(ptr);
-  }
-  return addr[dev];
-}
-
-// Launch epochs: every tensor-core forward launch gets the next one (never
-// 0, the counters' initial tag) and the counter slot epoch % kWorkSlots.
-std::atomic<uint32_t> g_epoch{0};
-
 // Test hook state (see cp_test_set_wait_fault).
 std::atomic<int> g_fault_drop_k{0};
 std::atomic<unsigned long long> g_wait_limit_ns{kTimeoutNs};
@@ -1665,8 +1670,8 @@ cudaError_t launch_t(const AttnArgs& a, cudaStream_t stream) {
   p.fault_drop_k = g_fault_drop_k.load();
   unsigned long long* slots = work_slots_address();
   if (!slots) return cudaErrorInvalidValue;
-  uint32_t epoch = ++g_epoch;
-  if (epoch == 0) epoch = ++g_epoch;
+  const uint32_t epoch = next_epoch(slots);
+  if (epoch == 0) return cudaErrorInvalidValue;
   p.epoch = epoch;
   p.work_slot = slots + epoch % kWorkSlots;
   const int grid = static_cast<int>(std::min<long long>(items, sm_count()));
