@@ -99,11 +99,6 @@ constexpr float kRescaleLog2 = 8.0f;
 //  CPRING_FP8_FAST         the FP8 kernel uses the same no-max fast pass, with
 //                          the guards at 2^8 so that every P it keeps is at
 //                          most 2^8, inside E4M3's range (448).
-//  CPRING_FP8_EVENT        the FP8 MMA warp issues each query tile's S and PV
-//                          as soon as that tile's inputs are ready, polling
-//                          both tiles, instead of in a fixed interleaved
-//                          order (the tiles then drift apart by up to the
-//                          K/V ring's depth).
 //  CPRING_FP8_EARLY_SFREE  the FP8 softmax releases a tile's S columns as
 //                          soon as it has loaded them (the rare redo then
 //                          works from the scores kept in registers) instead
@@ -128,9 +123,6 @@ constexpr float kRescaleLog2 = 8.0f;
 #endif
 #ifndef CPRING_FP8_EARLY_SFREE
 #define CPRING_FP8_EARLY_SFREE 0
-#endif
-#ifndef CPRING_FP8_EVENT
-#define CPRING_FP8_EVENT 0
 #endif
 constexpr int kPReadyCount = 128;
 constexpr float kOverflowGuard = 18446744073709551616.0f;  // 2^64
@@ -1213,96 +1205,6 @@ __device__ __forceinline__ void attn_body_fp8(const CUtensorMap& tmap_q, const C
         if (!wait_warp(bar(k8QFull), q_iter & 1u, abort_flag, p)) { ok = false; break; }
         ++q_iter;
         ptx::tc_fence_after();
-#if CPRING_FP8_EVENT
-        {
-          // Per query tile: the next key tile whose S, and whose PV, is owed.
-          // A K (V) stage is released once every tile that visits its key
-          // tile has issued that S (PV); releases go out in key-tile order.
-          int s0 = it.f_lo[0], s1 = it.f_lo[1], v0 = it.f_lo[0], v1 = it.f_lo[1];
-          int k_rel = it.F_lo, v_rel = it.F_lo;
-          bool first0 = true, first1 = true, q_released = false;
-          auto stage = [&](int f) { return (kv_iter + static_cast<uint32_t>(f - it.F_lo)) % kStages8; };
-          auto phase = [&](int f) {
-            return ((kv_iter + static_cast<uint32_t>(f - it.F_lo)) / kStages8) & 1u;
-          };
-          auto ready = [&](uint32_t b, uint32_t ph) {
-            return __all_sync(0xffffffffu, ptx::mbar_test_wait(b, ph));
-          };
-          uint64_t idle_since = 0;
-          uint32_t idle = 0;
-          for (;;) {
-            bool moved = false;
-            // S of each tile: its softmax released the previous S, K is in
-            if (s0 <= it.f_hi[0] && (s_issued0 == 0 || ready(bar(k8SFree + 0), (s_issued0 - 1) & 1u)) &&
-                ready(bar(k8KFull + stage(s0)), phase(s0))) {
-              ptx::tc_fence_after();
-              if (!issue_s(0, s_issued0, stage(s0))) { ok = false; break; }
-              ++s0;
-              moved = true;
-            }
-            if (s1 <= it.f_hi[1] && (s_issued1 == 0 || ready(bar(k8SFree + 1), (s_issued1 - 1) & 1u)) &&
-                ready(bar(k8KFull + stage(s1)), phase(s1))) {
-              ptx::tc_fence_after();
-              if (!issue_s(1, s_issued1, stage(s1))) { ok = false; break; }
-              ++s1;
-              moved = true;
-            }
-            while (k_rel <= it.F_hi &&
-                   (k_rel < it.f_lo[0] || k_rel > it.f_hi[0] || s0 > k_rel) &&
-                   (k_rel < it.f_lo[1] || k_rel > it.f_hi[1] || s1 > k_rel)) {
-              ptx::mma_commit_w(bar(k8KEmpty + stage(k_rel)));  // K read by every S of it
-              ++k_rel;
-            }
-            if (!q_released && s0 > it.f_hi[0] && s1 > it.f_hi[1]) {
-              ptx::mma_commit_w(bar(k8QEmpty));  // every S of this item has been issued
-              q_released = true;
-            }
-            // PV of each tile: its P landed, V is in
-            if (v0 < s0 && ready(bar(k8PReady + (pv_issued0 & 1u)), (pv_issued0 >> 1) & 1u) &&
-                ready(bar(k8VFull + stage(v0)), phase(v0))) {
-              if (!issue_pv(0, pv_issued0, stage(v0), first0, v0 == it.f_hi[0])) { ok = false; break; }
-              ++v0;
-              moved = true;
-            }
-            if (v1 < s1 && ready(bar(k8PReady + 2 + (pv_issued1 & 1u)), (pv_issued1 >> 1) & 1u) &&
-                ready(bar(k8VFull + stage(v1)), phase(v1))) {
-              if (!issue_pv(1, pv_issued1, stage(v1), first1, v1 == it.f_hi[1])) { ok = false; break; }
-              ++v1;
-              moved = true;
-            }
-            while (v_rel <= it.F_hi &&
-                   (v_rel < it.f_lo[0] || v_rel > it.f_hi[0] || v0 > v_rel) &&
-                   (v_rel < it.f_lo[1] || v_rel > it.f_hi[1] || v1 > v_rel)) {
-              ptx::mma_commit_w(bar(k8VEmpty + stage(v_rel)));  // V read by every PV of it
-              ++v_rel;
-            }
-            if (v_rel > it.F_hi && k_rel > it.F_hi && q_released) break;  // the item is issued
-            if (moved) {
-              idle = 0;
-              continue;
-            }
-            // Nothing was ready: a bounded wait, as in wait_warp.
-            if (__any_sync(0xffffffffu, *abort_flag != 0u)) { ok = false; break; }
-            if ((++idle & 255u) == 0) {
-              int tout = 0;
-              if (lane == 0) {
-                const uint64_t now = ptx::globaltimer();
-                if (idle_since == 0) {
-                  idle_since = now;
-                } else if (now - idle_since > p.timeout_ns) {
-                  *abort_flag = 1u;
-                  atomicOr(p.err, kErrTimeout);
-                  tout = 1;
-                }
-              }
-              if (__shfl_sync(0xffffffffu, tout, 0)) { ok = false; break; }
-            }
-          }
-          if (!ok) break;
-          kv_iter += static_cast<uint32_t>(it.F_hi - it.F_lo + 1);
-          continue;
-        }
-#endif
         bool pend0 = false, pend1 = false;    // S issued whose PV is still owed
         bool first0 = true, first1 = true;    // next PV overwrites O
         uint32_t prev_st = 0, prev_ph = 0;
