@@ -188,6 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* vec = reinterpret_cast<float*>(smem + Lay::kVec);
   const ItemRing ring{sbase + Lay::kRingOff,
                       reinterpret_cast<volatile int*>(smem + Lay::kRingOff + 2 * kRing * 8)};
+  // the item whose fixed tiles the producer is loading (the MMA warp's copy)
+  volatile int* fix_item = reinterpret_cast<volatile int*>(smem + Lay::kRingOff + 128);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -222,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(bar(kPReadyS), kSoftmaxThreads);
     ptx::mbar_init(bar(kPReadyS + 1), kSoftmaxThreads);
     ptx::mbar_init(bar(kDrain), 1);
-    ring_init(ring);
+    ring_init(ring, kSoftmaxThreads / 32);  // the softmax warps read the ring
     *abort_flag = 0u;
     ptx::fence_barrier_init();
   }
@@ -263,6 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         BItem it;
         decode_bitem<kDKDV>(p, n_docs, w, it);
         if (!wait1(bar(kFixEmpty), (fix_iter & 1u) ^ 1u, abort_flag, p)) { ok = false; break; }
+        *fix_item = w;  // the MMA warp reads it once this phase of kFixFull completes
         ptx::mbar_arrive_expect_tx(bar(kFixFull), 2 * Lay::kTileBytes);
         for (int pn = 0; pn < Lay::kPanels; ++pn) {
           ptx::tma_load_4d(sbase + Lay::kF0 + pn * Lay::kPanelBytes, &tm_f0, bar(kFixFull),
@@ -296,6 +299,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++armed1[s1];
           ++x_iter;
         }
+      }
+      // No more items: tell the MMA warp through the next phase of kFixFull.
+      if (ok && wait1(bar(kFixEmpty), (fix_iter & 1u) ^ 1u, abort_flag, p)) {
+        *fix_item = p.n_items;
+        ptx::mbar_arrive(bar(kFixFull));
+        ++fix_iter;
       }
       // Let every copy this thread started land before the CTA can exit.
       if (fix_iter > 0) wait1(bar(kFixFull), (fix_iter - 1) & 1u, abort_flag, p, false);
@@ -362,14 +371,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                       kIdescG, (first && s == 0) ? 0u : 1u);
         }
       };
-      for (int k = 0; ok; ++k) {
-        const int w = ring_get(ring, static_cast<uint32_t>(k), abort_flag, p);
-        if (w < 0) { ok = false; break; }
+      for (;;) {
+        // The producer publishes each item with its fixed tiles' load (and
+        // the end of the work with a plain arrival), so this warp needs no
+        // wait beyond the one for those tiles.
+        if (!wait_warp(bar(kFixFull), fix_iter & 1u, abort_flag, p)) { ok = false; break; }
+        ++fix_iter;
+        const int w = *fix_item;
         if (w >= p.n_items) break;
         BItem it;
         decode_bitem<kDKDV>(p, n_docs, w, it);
-        if (!wait_warp(bar(kFixFull), fix_iter & 1u, abort_flag, p)) { ok = false; break; }
-        ++fix_iter;
         ptx::tc_fence_after();
         if constexpr (!kDKDV) {
           // S, dP of step n + 1 go out once the softmax has read those of

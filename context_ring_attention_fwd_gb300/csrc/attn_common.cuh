@@ -121,8 +121,9 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity,
 // once on a device before one would reuse the slot of another still running.
 constexpr int kWorkSlots = 256;
 __device__ unsigned long long g_work_slots[kWorkSlots];
-// Tuning switch: CTAs claim items from the launch's counter (1) or take them
-// in the fixed snake order of item_of (0).
+// Tuning switch of the backward kernels: CTAs claim items from the launch's
+// counter (1) or take them in the fixed snake order of item_of (0).  (The
+// forward chooses per launch.)
 #ifndef CPRING_DYNAMIC
 #define CPRING_DYNAMIC 1
 #endif
@@ -156,10 +157,10 @@ __device__ __forceinline__ int claimed_index(unsigned long long v, uint32_t epoc
 }
 
 // The CTA's ring of claimed item indices: the producer publishes each item
-// it claims (its k-th item in slot k % kRing); the MMA warp and the eight
-// softmax warps read them in the same order, so every role walks the same
-// items.  Full barriers take the producer's arrival, empty ones one arrival
-// per reading warp.
+// it claims (its k-th item in slot k % kRing); the reading warps (by default
+// the MMA warp and the eight softmax warps) read them in the same order, so
+// every role walks the same items.  Full barriers take the producer's
+// arrival, empty ones one arrival per reading warp.
 constexpr int kRing = 4;
 constexpr int kRingReaders = 9;  // the MMA warp and the eight softmax warps
 constexpr int kRingBytes = 2 * kRing * 8 + kRing * 4;
@@ -172,10 +173,10 @@ struct ItemRing {
   __device__ uint32_t empty(int s) const { return bars + 8u * static_cast<uint32_t>(kRing + s); }
 };
 
-__device__ __forceinline__ void ring_init(const ItemRing& r) {
+__device__ __forceinline__ void ring_init(const ItemRing& r, int readers = kRingReaders) {
   for (int s = 0; s < kRing; ++s) {
     ptx::mbar_init(r.full(s), 1);
-    ptx::mbar_init(r.empty(s), kRingReaders);
+    ptx::mbar_init(r.empty(s), readers);
   }
 }
 

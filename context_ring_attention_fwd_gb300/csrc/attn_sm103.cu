@@ -84,9 +84,9 @@ constexpr float kRescaleLog2 = 8.0f;
 //  CPRING_GROUP_MIN_ROUNDS ... when the launch has at least this many rounds;
 //                          shorter launches deal every item from one pool.
 //  CPRING_GROUP_DOCS       launches with documents group heads too.
-//  CPRING_DYNAMIC          (attn_common.cuh) CTAs claim items from the
-//                          launch's counter (1) or take them in a fixed snake
-//                          order (0).
+//  CPRING_DYNAMIC_ALWAYS   the whole-sequence bf16 launch without documents
+//                          claims its items too (otherwise it takes the
+//                          fixed snake deal; every other launch claims).
 //  CPRING_FUSED_NOMAX      fused forward only: after the first tile, skip the
 //                          row max and redo a tile only if its first 64 keys'
 //                          row sum or its last 64 keys' row max shows an
@@ -111,6 +111,9 @@ constexpr float kRescaleLog2 = 8.0f;
 #endif
 #ifndef CPRING_GROUP_DOCS
 #define CPRING_GROUP_DOCS 0
+#endif
+#ifndef CPRING_DYNAMIC_ALWAYS
+#define CPRING_DYNAMIC_ALWAYS 0
 #endif
 #ifndef CPRING_FUSED_NOMAX
 #define CPRING_FUSED_NOMAX 1
@@ -257,6 +260,10 @@ __device__ __forceinline__ void decode_item(const KParams& p, int n_docs, int w,
     }
   }
 }
+
+// The softmax warps read the item ring; the MMA warp learns each item from
+// its Q load instead (see the producer).
+constexpr int kSoftmaxRingReaders = 8;
 
 // ---------------------------------------------------------------- softmax pieces
 __device__ __forceinline__ float max3(float a, float b, float c) {
@@ -459,7 +466,10 @@ __device__ __forceinline__ void store_p_half(uint32_t tS, const uint32_t (&pk)[2
 
 // ---------------------------------------------------------------- kernel
 // The body shared by the bf16 and the FP8 kernels (see the wrappers below).
-template <int D, bool kPartial>
+// kDynamic: CTAs claim items at run time (the producer hands each to the
+// softmax warps through the item ring and to the MMA warp with its Q load);
+// otherwise every role walks the fixed snake deal by itself.
+template <int D, bool kPartial, bool kDynamic>
 __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
                                           const CUtensorMap& tmap_v, const KParams& p) {
   using Lay = Layout<D, 2>;
@@ -474,6 +484,8 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
       reinterpret_cast<volatile uint32_t*>(smem + Lay::kBarOff + kAbortSlot);
   const ItemRing ring{sbase + Lay::kRingOff,
                       reinterpret_cast<volatile int*>(smem + Lay::kRingOff + 2 * kRing * 8)};
+  // the item whose Q the producer is loading (the MMA warp's copy of the work)
+  volatile int* q_item = reinterpret_cast<volatile int*>(smem + Lay::kRingOff + 128);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -500,7 +512,7 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
       ptx::mbar_init(bar(kOBar + t), 1);
     }
     ptx::mbar_init(bar(kDrain), 1);
-    ring_init(ring);
+    if (kDynamic) ring_init(ring, kSoftmaxRingReaders);
     *abort_flag = 0u;
     ptx::fence_barrier_init();
   }
@@ -532,16 +544,19 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
       bool dropped = false;
       bool ok = true;
       for (int k = 0; ok; ++k) {
-        const int w = !CPRING_DYNAMIC ? item_of(k, c, G)
+        const int w = !kDynamic ? item_of(k, c, G)
                       : (k == 0) ? c : G + claimed_index(ahead, p.epoch, p.err);
-        if (!ring_put(ring, static_cast<uint32_t>(k), w, abort_flag, p)) { ok = false; break; }
+        if constexpr (kDynamic) {
+          if (!ring_put(ring, static_cast<uint32_t>(k), w, abort_flag, p)) { ok = false; break; }
+        }
         if (w >= p.n_items) break;
-        if (CPRING_DYNAMIC)  // claim the CTA's next item now; it is read when that item starts
+        if constexpr (kDynamic)  // claim the CTA's next item now; it is read when that item starts
           ahead = (k == 0) ? claim_first(p.work_slot, p.epoch) : claim_next(p.work_slot);
         Item it;
         decode_item(p, n_docs, w, it);
         if (it.F_lo > it.F_hi) continue;
         if (!wait1(bar(kQEmpty), (q_iter & 1u) ^ 1u, abort_flag, p)) { ok = false; break; }
+        if constexpr (kDynamic) *q_item = w;  // the MMA warp reads it with this phase of kQFull
         ptx::mbar_arrive_expect_tx(bar(kQFull), kQTiles * Lay::kTileBytes);
 #pragma unroll
         for (int t = 0; t < kQTiles; ++t)
@@ -577,6 +592,12 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
           if (st == 0) ++v_armed0; else ++v_armed1;
           ++kv_iter;
         }
+      }
+      // No more items: tell the MMA warp through the next phase of kQFull.
+      if (kDynamic && ok && wait1(bar(kQEmpty), (q_iter & 1u) ^ 1u, abort_flag, p)) {
+        *q_item = p.n_items;
+        ptx::mbar_arrive(bar(kQFull));
+        ++q_iter;
       }
       // Let every copy this thread started land before the CTA can exit.
       if (q_iter > 0) wait1(bar(kQFull), (q_iter - 1) & 1u, abort_flag, p, false);
@@ -630,15 +651,26 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
         }
         ptx::mma_commit_w(bar(kSFull + t));
       };
-      for (int k = 0; ok; ++k) {
-        const int w = ring_get(ring, static_cast<uint32_t>(k), abort_flag, p);
-        if (w < 0) { ok = false; break; }
-        if (w >= p.n_items) break;
+      for (int k = 0;; ++k) {
+        // Claimed items: the producer publishes each item that has work with
+        // its Q load (and the end of the work with a plain arrival), so this
+        // warp needs no wait beyond the one for Q.  The fixed deal: this
+        // warp walks it and skips items with nothing to compute.
         Item it;
-        decode_item(p, n_docs, w, it);
-        if (it.F_lo > it.F_hi) continue;
-        if (!wait_warp(bar(kQFull), q_iter & 1u, abort_flag, p)) { ok = false; break; }
-        ++q_iter;
+        if constexpr (kDynamic) {
+          if (!wait_warp(bar(kQFull), q_iter & 1u, abort_flag, p)) { ok = false; break; }
+          ++q_iter;
+          const int w = *q_item;
+          if (w >= p.n_items) break;
+          decode_item(p, n_docs, w, it);
+        } else {
+          const int w = item_of(k, c, G);
+          if (w >= p.n_items) break;
+          decode_item(p, n_docs, w, it);
+          if (it.F_lo > it.F_hi) continue;
+          if (!wait_warp(bar(kQFull), q_iter & 1u, abort_flag, p)) { ok = false; break; }
+          ++q_iter;
+        }
         ptx::tc_fence_after();
         bool pend0 = false, pend1 = false;    // an S issued whose PV is still owed
         bool first0 = true, first1 = true;    // next PV overwrites O
@@ -720,8 +752,13 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmap_q, const CUten
     uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const int w = ring_get(ring, static_cast<uint32_t>(k), abort_flag, p);
-      if (w < 0) { ok = false; break; }
+      int w;
+      if constexpr (kDynamic) {
+        w = ring_get(ring, static_cast<uint32_t>(k), abort_flag, p);
+        if (w < 0) { ok = false; break; }
+      } else {
+        w = item_of(k, c, G);
+      }
       if (w >= p.n_items) break;
       Item it;
       decode_item(p, n_docs, w, it);
@@ -1027,6 +1064,8 @@ __device__ __forceinline__ void attn_body_fp8(const CUtensorMap& tmap_q, const C
       reinterpret_cast<volatile uint32_t*>(smem + Lay::kBarOff + kAbortSlot8);
   const ItemRing ring{sbase + Lay::kRingOff,
                       reinterpret_cast<volatile int*>(smem + Lay::kRingOff + 2 * kRing * 8)};
+  // the item whose Q the producer is loading (the MMA warp's copy of the work)
+  volatile int* q_item = reinterpret_cast<volatile int*>(smem + Lay::kRingOff + 128);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -1056,7 +1095,7 @@ __device__ __forceinline__ void attn_body_fp8(const CUtensorMap& tmap_q, const C
       }
     }
     ptx::mbar_init(bar(k8Drain), 1);
-    ring_init(ring);
+    ring_init(ring, kSoftmaxRingReaders);
     *abort_flag = 0u;
     ptx::fence_barrier_init();
   }
@@ -1092,16 +1131,16 @@ __device__ __forceinline__ void attn_body_fp8(const CUtensorMap& tmap_q, const C
       bool dropped = false;
       bool ok = true;
       for (int k = 0; ok; ++k) {
-        const int w = !CPRING_DYNAMIC ? item_of(k, c, G)
-                      : (k == 0) ? c : G + claimed_index(ahead, p.epoch, p.err);
+        const int w = (k == 0) ? c : G + claimed_index(ahead, p.epoch, p.err);
         if (!ring_put(ring, static_cast<uint32_t>(k), w, abort_flag, p)) { ok = false; break; }
         if (w >= p.n_items) break;
-        if (CPRING_DYNAMIC)  // claim the CTA's next item now; it is read when that item starts
-          ahead = (k == 0) ? claim_first(p.work_slot, p.epoch) : claim_next(p.work_slot);
+        // claim the CTA's next item now; it is read when that item starts
+        ahead = (k == 0) ? claim_first(p.work_slot, p.epoch) : claim_next(p.work_slot);
         Item it;
         decode_item(p, n_docs, w, it);
         if (it.F_lo > it.F_hi) continue;
         if (!wait1(bar(k8QEmpty), (q_iter & 1u) ^ 1u, abort_flag, p)) { ok = false; break; }
+        *q_item = w;  // the MMA warp reads it once this phase of k8QFull completes
         ptx::mbar_arrive_expect_tx(bar(k8QFull), kQTiles * Lay::kTileBytes);
 #pragma unroll
         for (int t = 0; t < kQTiles; ++t)
@@ -1132,6 +1171,12 @@ __device__ __forceinline__ void attn_body_fp8(const CUtensorMap& tmap_q, const C
           bump(st, v_armed0, v_armed1, v_armed2);
           ++kv_iter;
         }
+      }
+      // No more items: tell the MMA warp through the next phase of k8QFull.
+      if (ok && wait1(bar(k8QEmpty), (q_iter & 1u) ^ 1u, abort_flag, p)) {
+        *q_item = p.n_items;
+        ptx::mbar_arrive(bar(k8QFull));
+        ++q_iter;
       }
       // Let every copy this thread started land before the CTA can exit.
       if (q_iter > 0) wait1(bar(k8QFull), (q_iter - 1) & 1u, abort_flag, p, false);
@@ -1195,15 +1240,16 @@ __device__ __forceinline__ void attn_body_fp8(const CUtensorMap& tmap_q, const C
         ++n_s;
         return true;
       };
-      for (int k = 0; ok; ++k) {
-        const int w = ring_get(ring, static_cast<uint32_t>(k), abort_flag, p);
-        if (w < 0) { ok = false; break; }
+      for (;;) {
+        // The producer publishes each item that has work with its Q load
+        // (and the end of the work with a plain arrival), so this warp needs
+        // no wait beyond the one for Q.
+        if (!wait_warp(bar(k8QFull), q_iter & 1u, abort_flag, p)) { ok = false; break; }
+        ++q_iter;
+        const int w = *q_item;
         if (w >= p.n_items) break;
         Item it;
         decode_item(p, n_docs, w, it);
-        if (it.F_lo > it.F_hi) continue;
-        if (!wait_warp(bar(k8QFull), q_iter & 1u, abort_flag, p)) { ok = false; break; }
-        ++q_iter;
         ptx::tc_fence_after();
         bool pend0 = false, pend1 = false;    // S issued whose PV is still owed
         bool first0 = true, first1 = true;    // next PV overwrites O
@@ -1432,12 +1478,12 @@ __device__ __forceinline__ void attn_body_fp8(const CUtensorMap& tmap_q, const C
   }
 }
 
-template <int D, bool kPartial>
+template <int D, bool kPartial, bool kDynamic>
 __global__ void __launch_bounds__(kThreads, 1)
     ring_attn_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q,
                           const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_v, const KParams p) {
-  attn_body<D, kPartial>(tmap_q, tmap_k, tmap_v, p);
+  attn_body<D, kPartial, kDynamic>(tmap_q, tmap_k, tmap_v, p);
 }
 
 template <int D>
@@ -1510,7 +1556,7 @@ __global__ void __launch_bounds__(1024) slot_order_kernel(KParams p, int32_t* __
   }
 }
 
-template <int D, bool kPartial, bool kFp8 = false>
+template <int D, bool kPartial, bool kFp8 = false, bool kDynamic = true>
 cudaError_t launch_t(const AttnArgs& a, cudaStream_t stream) {
   using Lay = std::conditional_t<kFp8, Fp8Layout, Layout<D, 2>>;
   static_assert(Lay::kAlloc <= 232448, "shared memory budget");
@@ -1518,7 +1564,7 @@ cudaError_t launch_t(const AttnArgs& a, cudaStream_t stream) {
   if constexpr (kFp8)
     kern = ring_attn_fp8_kernel<D>;
   else
-    kern = ring_attn_bf16_kernel<D, kPartial>;
+    kern = ring_attn_bf16_kernel<D, kPartial, kDynamic>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
@@ -1610,8 +1656,20 @@ cudaError_t launch_t(const AttnArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_attn_bf16(const AttnArgs& a, cudaStream_t stream) {
   const bool partial = (a.k_shard >= 0);
-  if (a.d == 128) return partial ? launch_t<128, true>(a, stream) : launch_t<128, false>(a, stream);
-  if (a.d == 64) return partial ? launch_t<64, true>(a, stream) : launch_t<64, false>(a, stream);
+  // Claimed items pay where the items' costs are uneven or few: documents,
+  // one rank's or one step's launch; the whole-sequence launch without
+  // documents takes the fixed snake deal, which measured faster there.
+  const bool dynamic = CPRING_DYNAMIC_ALWAYS || a.doc_offsets != nullptr || a.q_shard >= 0 || partial;
+  if (a.d == 128) {
+    if (partial) return launch_t<128, true, false, true>(a, stream);
+    return dynamic ? launch_t<128, false, false, true>(a, stream)
+                   : launch_t<128, false, false, false>(a, stream);
+  }
+  if (a.d == 64) {
+    if (partial) return launch_t<64, true, false, true>(a, stream);
+    return dynamic ? launch_t<64, false, false, true>(a, stream)
+                   : launch_t<64, false, false, false>(a, stream);
+  }
   return cudaErrorInvalidValue;
 }
 
