@@ -44,8 +44,8 @@ DEFAULT_WORKLOAD = "bf16_causal_128k"
 # on: "sources" is the SHA-256 prefix of the forward kernel's source files
 # (KERNEL_SOURCES), and a line whose sources differ reports traffic null.
 NCU_TRAFFIC = {
-    # 5.037 GB read + 1.079 GB written (ncu, ring_attn_bf16_kernel<128, 0>, 1 pass)
-    "bf16_causal_128k": {"bytes": 5.036873984e9 + 1.078599168e9, "sources": "66171fdee802b093"},
+    # 14.923 GB read + 1.083 GB written (ncu, ring_attn_bf16_kernel<128, 0, 0>, 1 pass)
+    "bf16_causal_128k": {"bytes": 14.922612992e9 + 1.083377408e9, "sources": "a9b2b2a488a4820d"},
 }
 KERNEL_SOURCES = ("context_ring_attention_fwd_gb300/csrc/attn_sm103.cu",
                   "context_ring_attention_fwd_gb300/csrc/attn_common.cuh",
@@ -523,8 +523,12 @@ def schedule_gates(pkg, w, q, k, v, out, lse, stream, dev, rounds: int = 3):
     ideal = computed_tile_ratio(w.S, w.n_shards)
     spread = (max(by_n.values()) - min(by_n.values())) / min(by_n.values())
     ratio = t_causal / t_full
+    # the stated limit at the 128K shape; elsewhere the same margin over the
+    # computed-tile ratio (shorter sequences carry more diagonal tiles)
+    limit = 0.53 if (w.S, w.H, w.d, w.n_shards) == (131072, 32, 128, 4) else ideal + 0.03
     return {"ms_causal": t_causal, "ms_full": t_full, "causal_over_full": ratio,
-            "computed_tile_ratio": ideal, "causal_over_full_ok": ratio <= 0.53,
+            "computed_tile_ratio": ideal, "causal_over_full_limit": limit,
+            "causal_over_full_ok": ratio <= limit,
             "ms_causal_by_n_shards": {str(n): t for n, t in by_n.items()},
             "n_shards_spread": spread, "n_shards_spread_ok": spread <= 0.03,
             "rounds": rounds, "timing": "round-robin over the configurations, median per one"}
@@ -634,14 +638,14 @@ def run_ulysses(args, w, local):
     tensor_bytes = q.numel() * q.element_size()
     perm_bytes = 8 * tensor_bytes  # Q, K, V in and O out, each read once and written once
     hbm, _, _ = measured_peaks_hbm()
-    perm_ms = max(ms_u - ms_a, 1e-9)
     return {
         "metric": METRIC, "impl": "ulysses_all_to_all", "unit": UNIT,
         "value": flops / (ms_u * 1e-3) / 1e12, "ms_per_step": ms_u, "ms_fused_ring": ms_f,
         "ms_head_group_attention": ms_a,
         "a2a_bytes_counted": moved[-1], "permutation_bytes_in_hbm": perm_bytes,
+        # the form's time beyond its attention launch: a difference of two
+        # totals, so it carries their noise (no bandwidth is derived from it)
         "ms_permutations_and_lse": ms_u - ms_a,
-        "permutation_GBps": perm_bytes / (perm_ms * 1e-3) / 1e9,
         "hbm_peak_GBps": hbm,
         "steps": args.steps, "warmup": args.warmup, "n_gpus": 1, "dtype": w.dtype,
         "data": "synthetic", "config": _config(w, docs, 1),
