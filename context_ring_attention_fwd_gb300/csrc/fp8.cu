@@ -19,7 +19,7 @@
 //                       per column sweep of a block
 //   fp8_quant_kernel    x8 in the same [B, S, H, d] layout (Q and K)
 //   fp8_quant_t_kernel  x8 as [B, H, d, S] (V^T, keys contiguous), through a
-//                       shared-memory tile of 64 tokens
+//                       shared-memory tile of 128 tokens
 //   fp8_descale_kernel  amax -> descale in place
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -111,39 +111,56 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-constexpr int kTTokens = 64;               // tokens per transposed tile
-constexpr int kTPitch = kTTokens + 16;     // bytes per d-row of the tile (16-byte multiple)
+constexpr int kTTokens = 128;  // tokens per transposed tile (one 128-byte output segment)
 
-// Block (x, h, b) covers tokens [x * 64, ...) of head h: it reads 64 token
-// rows of d bf16, quantizes them into a [d][64] byte tile, and writes d rows
-// of 64 keys to y[b, h, :, s0 .. s0 + 64).  S % 16 == 0, so a 16-byte
-// segment of keys is either wholly inside [0, S) or wholly past it.
+// Block (x, h, b) covers tokens [s0, s0 + 128) of head h, s0 = 128 x.
+// Phase 1: the block reads the 128 token rows of d bf16 (coalesced 16-byte
+// loads), quantizes them and stores the codes row-major in shared memory,
+// 128 bytes per token row, word w of token r at word w ^ (4 (r / 16)) of its
+// row.  Phase 2: thread (d4, g) gathers words d4 (four consecutive channels)
+// of tokens 16 g .. 16 g + 15, transposes the 4 x 16 bytes in registers and
+// writes four 16-byte segments, channel rows 4 d4 .. 4 d4 + 3 of
+// y[b, h, :, s0 + 16 g ..].  With g the fastest thread index, 8 lanes write
+// one full 128-byte segment of a row; the swizzle makes both phases' shared
+// accesses conflict-free.  S % 16 == 0, so a 16-token segment is either
+// wholly inside [0, S) or wholly past it.
 __global__ void __launch_bounds__(kThreads)
     fp8_quant_t_kernel(const uint4* __restrict__ x, uint8_t* __restrict__ y,
                        const float* __restrict__ amax, int S, int H, int d) {
-  __shared__ __align__(16) uint8_t tile[128 * kTPitch];
+  __shared__ __align__(16) uint32_t tile[kTTokens * 32];  // 128 rows x 128 bytes
   const int h = blockIdx.y, b = blockIdx.z;
   const int s0 = blockIdx.x * kTTokens;
-  const int g = d / 8;
+  const int g8 = d / 8;   // 16-byte input vectors per token row of one head
   const float inv = inv_scale(amax[b * H + h]);
-  for (int idx = threadIdx.x; idx < kTTokens * g; idx += kThreads) {
-    const int r = idx / g, cv = idx % g;
+  for (int idx = threadIdx.x; idx < kTTokens * g8; idx += kThreads) {
+    const int r = idx / g8, cv = idx - (idx / g8) * g8;
     uint2 q = make_uint2(0u, 0u);
     if (s0 + r < S)
-      q = quant8(x[((static_cast<long long>(b) * S + s0 + r) * H + h) * g + cv], inv);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint32_t w = k < 4 ? q.x : q.y;
-      tile[(cv * 8 + k) * kTPitch + r] = static_cast<uint8_t>(w >> (8 * (k & 3)));
-    }
+      q = quant8(x[((static_cast<long long>(b) * S + s0 + r) * H + h) * g8 + cv], inv);
+    const int w = (2 * cv) ^ (4 * (r >> 4));  // words 2 cv, 2 cv + 1 stay adjacent
+    *reinterpret_cast<uint2*>(tile + r * 32 + w) = q;
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < d * (kTTokens / 16); idx += kThreads) {
-    const int dd = idx / (kTTokens / 16), seg = idx % (kTTokens / 16);
-    const int s = s0 + seg * 16;
-    if (s < S) {
-      const uint4 v = *reinterpret_cast<const uint4*>(tile + dd * kTPitch + seg * 16);
-      *reinterpret_cast<uint4*>(y + ((static_cast<long long>(b) * H + h) * d + dd) * S + s) = v;
+  const int n_d4 = d / 4;
+  for (int idx = threadIdx.x; idx < n_d4 * 8; idx += kThreads) {
+    const int g = idx & 7, d4 = idx >> 3;
+    const int s = s0 + 16 * g;
+    if (s >= S) continue;
+    uint32_t wv[16];  // word d4 (channels 4 d4 .. +3) of tokens 16 g + j
+#pragma unroll
+    for (int j = 0; j < 16; ++j) wv[j] = tile[(16 * g + j) * 32 + (d4 ^ (4 * g))];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      // channel 4 d4 + c of the 16 tokens: byte c of each word, token j at byte j
+      uint32_t o[4];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const uint32_t lo = __byte_perm(wv[4 * q4 + 0], wv[4 * q4 + 1], 0x0040 | (c << 4) | c) & 0xffffu;
+        const uint32_t hi = __byte_perm(wv[4 * q4 + 2], wv[4 * q4 + 3], 0x0040 | (c << 4) | c) & 0xffffu;
+        o[q4] = lo | (hi << 16);
+      }
+      *reinterpret_cast<uint4*>(y + ((static_cast<long long>(b) * H + h) * d + 4 * d4 + c) * S + s) =
+          make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
 }
