@@ -87,6 +87,8 @@ constexpr float kRescaleLog2 = 8.0f;
 //  CPRING_DYNAMIC_ALWAYS   the whole-sequence bf16 launch without documents
 //                          claims its items too (otherwise it takes the
 //                          fixed snake deal; every other launch claims).
+//  CPRING_RANK_DYNAMIC     one rank's launch without documents claims its
+//                          items (1) or takes the fixed deal (0).
 //  CPRING_FUSED_NOMAX      fused forward only: after the first tile, skip the
 //                          row max and redo a tile only if its first 64 keys'
 //                          row sum or its last 64 keys' row max shows an
@@ -103,6 +105,10 @@ constexpr float kRescaleLog2 = 8.0f;
 //                          soon as it has loaded them (the rare redo then
 //                          works from the scores kept in registers) instead
 //                          of after its exponentials.
+//  CPRING_FP8_EXP_F16      FP8 fast pass: P = 2^x from the paired half-precision
+//                          exponential (two per instruction) and converted to
+//                          E4M3 from half precision; row sums in half pairs
+//                          over 32 keys, then added into fp32.
 #ifndef CPRING_BALANCE
 #define CPRING_BALANCE 2
 #endif
@@ -115,6 +121,9 @@ constexpr float kRescaleLog2 = 8.0f;
 #ifndef CPRING_DYNAMIC_ALWAYS
 #define CPRING_DYNAMIC_ALWAYS 0
 #endif
+#ifndef CPRING_RANK_DYNAMIC
+#define CPRING_RANK_DYNAMIC 0
+#endif
 #ifndef CPRING_FUSED_NOMAX
 #define CPRING_FUSED_NOMAX 1
 #endif
@@ -126,6 +135,9 @@ constexpr float kRescaleLog2 = 8.0f;
 #endif
 #ifndef CPRING_FP8_EARLY_SFREE
 #define CPRING_FP8_EARLY_SFREE 0
+#endif
+#ifndef CPRING_FP8_EXP_F16
+#define CPRING_FP8_EXP_F16 1
 #endif
 constexpr int kPReadyCount = 128;
 constexpr float kOverflowGuard = 18446744073709551616.0f;  // 2^64
@@ -434,6 +446,45 @@ __device__ __forceinline__ void exp_chunks_f8(const uint32_t (&sv)[4][32], int h
       add2(acc, p2, p3);
       pk[0][ch * 8 + x] = ptx::pack_e4m3x4(p0, p1, p2, p3);
     }
+  }
+}
+
+// exp_chunks_f8 with the exponentials in half precision: 2^x for two keys
+// per ex2.approx.f16x2, E4M3 from the half pair, and the row sum of each
+// 32-key chunk formed in half pairs (at most 32 * 2^8, exact to 11 bits per
+// add) before it enters the fp32 sum.  The argument is rounded to half
+// precision (10 bits): 2^x then carries a relative error below 2^-8 for
+// x >= -8, far inside E4M3's 2^-4 rounding, and keys further below the
+// reference give P under E4M3's smallest step either way.  An argument
+// above half precision's range gives +inf, which the caller's 2^8 guard
+// sends to the fp32 redo.
+__device__ __forceinline__ void exp_chunks_f8h(const uint32_t (&sv)[4][32], int half, float sc,
+                                               float base, uint32_t (&pk)[2][32], float& ls) {
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc) {
+    const int ch = 2 * half + cc;
+    uint32_t hs = 0;  // two half-precision zeros
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+      float e0, e1, e2, e3;
+      fma2(e0, e1, __uint_as_float(sv[ch][4 * x]), __uint_as_float(sv[ch][4 * x + 1]), sc, -base);
+      fma2(e2, e3, __uint_as_float(sv[ch][4 * x + 2]), __uint_as_float(sv[ch][4 * x + 3]), sc, -base);
+      uint32_t h01, h23;
+      asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h01) : "f"(e1), "f"(e0));
+      asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h23) : "f"(e3), "f"(e2));
+      asm("ex2.approx.f16x2 %0, %0;" : "+r"(h01));
+      asm("ex2.approx.f16x2 %0, %0;" : "+r"(h23));
+      uint16_t lo, hi;
+      asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(lo) : "r"(h01));
+      asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(hi) : "r"(h23));
+      pk[0][ch * 8 + x] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+      asm("add.rn.f16x2 %0, %0, %1;" : "+r"(hs) : "r"(h01));
+      asm("add.rn.f16x2 %0, %0, %1;" : "+r"(hs) : "r"(h23));
+    }
+    asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+        "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %0, hi, %0;\n\t}"
+        : "+f"(ls)
+        : "r"(hs));
   }
 }
 
@@ -1355,10 +1406,15 @@ __device__ __forceinline__ void attn_body_fp8(const CUtensorMap& tmap_q, const C
           // One pass over the 128 keys against the current reference; a row
           // sum above 2^8 sends the tile to the redo below, which keeps every
           // P inside E4M3's range (448).
-          uint64_t acc = 0;  // two fp32 zeros
-          exp_chunks_f8(sv, 0, sc, m_used, pk, acc);
-          exp_chunks_f8(sv, 1, sc, m_used, pk, acc);
-          lsum = sum2(acc);
+          if (CPRING_FP8_EXP_F16) {
+            exp_chunks_f8h(sv, 0, sc, m_used, pk, lsum);
+            exp_chunks_f8h(sv, 1, sc, m_used, pk, lsum);
+          } else {
+            uint64_t acc = 0;  // two fp32 zeros
+            exp_chunks_f8(sv, 0, sc, m_used, pk, acc);
+            exp_chunks_f8(sv, 1, sc, m_used, pk, acc);
+            lsum = sum2(acc);
+          }
           const bool redo = !(lsum <= kOverflowGuardFp8);
           if (__any_sync(0xffffffffu, redo)) {
             // Rare: a sum above the guard means this tile's max is above the
@@ -1656,10 +1712,13 @@ cudaError_t launch_t(const AttnArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_attn_bf16(const AttnArgs& a, cudaStream_t stream) {
   const bool partial = (a.k_shard >= 0);
-  // Claimed items pay where the items' costs are uneven or few: documents,
-  // one rank's or one step's launch; the whole-sequence launch without
-  // documents takes the fixed snake deal, which measured faster there.
-  const bool dynamic = CPRING_DYNAMIC_ALWAYS || a.doc_offsets != nullptr || a.q_shard >= 0 || partial;
+  // Claimed items pay where the items' costs are uneven or few: documents
+  // and one step's launch.  A launch without documents over whole key ranges
+  // (all ranks, or one rank's query shard) takes the fixed snake deal, which
+  // measured faster there (81.4 against 85.7 ms for all ranks at 128K, and
+  // 87.2 against 89.5 ms for the four rank launches of the same shape).
+  const bool dynamic = CPRING_DYNAMIC_ALWAYS || a.doc_offsets != nullptr ||
+                       (CPRING_RANK_DYNAMIC && a.q_shard >= 0) || partial;
   if (a.d == 128) {
     if (partial) return launch_t<128, true, false, true>(a, stream);
     return dynamic ? launch_t<128, false, false, true>(a, stream)
