@@ -439,6 +439,35 @@ def test_host_entry_through_the_c_abi_twice_and_fp32():
                 _check_f32(ho, hl, wo, wl)
 
 
+def test_host_entry_with_documents_and_without_mask_equals_fused():
+    """cp_ring_attn_fwd_host on packed documents and without the causal mask
+    (every rank then waits for every shard): bf16 and fp32 outputs equal the
+    fused call with the same shard count bit for bit."""
+    import ctypes
+    B, S, H, d, N = 2, 4096, 2, 128, 2
+    lib = pkg.lib()
+    stream = torch.cuda.current_stream()
+    p = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    for dt in (torch.bfloat16, torch.float32):
+        esz = 2 if dt == torch.bfloat16 else 4
+        name = "cp_ring_attn_fwd_host" if esz == 2 else "cp_ring_attn_fwd_host_f32"
+        ws = torch.empty(pkg.cp_ring_attn_fwd_host_workspace_bytes(B, S, H, d, N, esz),
+                         dtype=torch.uint8, device=DEV)
+        q, k, v = (t.pin_memory() for t in inputs.make_qkv(B, S, H, d, 73, dt))
+        for causal, docs in ((True, None), (True, [0, 700, 701, 2500, 4096]), (False, None)):
+            docs_t = pkg.doc_offsets_tensor(docs, DEV)
+            ho = torch.full((B, S, H, d), 7.0, dtype=dt)
+            hl = torch.full((B, H, S), 7.0, dtype=torch.float32)
+            st = getattr(lib, name)(p(q), p(k), p(v), p(ho), p(hl), B, S, H, d, N, int(causal),
+                                    p(docs_t), p(ws), ws.numel(),
+                                    ctypes.c_void_p(stream.cuda_stream))
+            assert st == 0, pkg.STATUS_NAMES.get(st, st)
+            stream.synchronize()
+            assert pkg.cp_get_last_status() == 0
+            fo, fl = pkg.ring_attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), N, causal, docs)
+            assert torch.equal(ho, fo.cpu()) and torch.equal(hl, fl.cpu()), (dt, causal, docs)
+
+
 def test_native_kernels_launch():
     before = pkg.launch_counts()
     q, k, v = (t.to(DEV) for t in inputs.make_qkv(1, 256, 1, 128, seed=1, dtype=torch.bfloat16))
