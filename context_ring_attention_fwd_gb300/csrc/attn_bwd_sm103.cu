@@ -825,6 +825,56 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// The dQ launch reads nothing that the dK/dV launch writes, so it can run on
+// a second stream of the library's (one per device, created on first use
+// and kept for the process's life): its CTAs then take the SMs that the
+// dK/dV launch's last items leave idle instead of waiting for all of them.
+// The caller's stream waits for it before anything enqueued later.
+#ifndef CPRING_BWD_OVERLAP
+#define CPRING_BWD_OVERLAP 1
+#endif
+struct BwdSideStream {
+  std::mutex mu;
+  cudaStream_t s = nullptr;
+};
+constexpr int kMaxBwdDevices = 64;
+BwdSideStream g_bwd_side[kMaxBwdDevices];
+
+cudaStream_t bwd_side_stream() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxBwdDevices) return nullptr;
+  BwdSideStream& b = g_bwd_side[dev];
+  std::lock_guard<std::mutex> lock(b.mu);
+  if (!b.s && cudaStreamCreateWithFlags(&b.s, cudaStreamNonBlocking) != cudaSuccess) b.s = nullptr;
+  return b.s;
+}
+
+// dK/dV on `stream`, dQ beside it; both after everything already on `stream`.
+template <int D>
+cudaError_t launch_bwd_pair(const BwdArgs& a, cudaStream_t stream) {
+  cudaStream_t side = CPRING_BWD_OVERLAP ? bwd_side_stream() : nullptr;
+  if (!side) {
+    cudaError_t e = launch_bwd_t<D, true>(a, stream);
+    return e == cudaSuccess ? launch_bwd_t<D, false>(a, stream) : e;
+  }
+  cudaEvent_t ready = nullptr, dq_done = nullptr;
+  if (cudaEventCreateWithFlags(&ready, cudaEventDisableTiming) != cudaSuccess) return cudaErrorUnknown;
+  if (cudaEventCreateWithFlags(&dq_done, cudaEventDisableTiming) != cudaSuccess) {
+    cudaEventDestroy(ready);
+    return cudaErrorUnknown;
+  }
+  cudaError_t e = cudaEventRecord(ready, stream);
+  if (e == cudaSuccess) e = launch_bwd_t<D, true>(a, stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(side, ready, 0);
+  if (e == cudaSuccess) e = launch_bwd_t<D, false>(a, side);
+  if (e == cudaSuccess) e = cudaEventRecord(dq_done, side);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, dq_done, 0);
+  // (destroying a recorded event releases it once the work it marks is done)
+  cudaEventDestroy(ready);
+  cudaEventDestroy(dq_done);
+  return e;
+}
+
 }  // namespace
 
 cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
@@ -839,17 +889,9 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e;
-  if (a.d == 128) {
-    e = launch_bwd_t<128, true>(a, stream);
-    if (e == cudaSuccess) e = launch_bwd_t<128, false>(a, stream);
-  } else if (a.d == 64) {
-    e = launch_bwd_t<64, true>(a, stream);
-    if (e == cudaSuccess) e = launch_bwd_t<64, false>(a, stream);
-  } else {
-    e = cudaErrorInvalidValue;
-  }
-  return e;
+  if (a.d == 128) return launch_bwd_pair<128>(a, stream);
+  if (a.d == 64) return launch_bwd_pair<64>(a, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace cpring

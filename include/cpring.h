@@ -394,9 +394,13 @@ void cp_launch_counts(int64_t* counts4);
  *             word); nothing is allocated.
  *  Shapes, masks, d, alignment and errors as cp_ring_attn_fwd; a workspace
  *  too small returns CP_ERR_BUFFER.
- * Four launches on `stream` (with doc_offsets, five): D, the dK/dV kernel
- * (one CTA per 128-key tile), the dQ kernel (one CTA per 128-query tile).
- * Both run on tcgen05 with fp32 accumulation and bf16 P / dS operands.
+ * Three launches (with doc_offsets, four: the doc scan first): D and the
+ * dK/dV kernel (one CTA per 128-key tile) on `stream`, and the dQ kernel (one
+ * CTA per 128-query tile), which reads nothing the dK/dV kernel writes, on a
+ * second stream owned by the library (one per device, kept for the
+ * process's life) after D; `stream` then waits for it, so work enqueued
+ * later on `stream` sees every gradient.  Both kernels run on tcgen05 with
+ * fp32 accumulation and bf16 P / dS operands.
  */
 int64_t cp_ring_attn_bwd_workspace_bytes(int B, int S, int H, int d, int n_shards);
 cp_status cp_ring_attn_bwd(const void* q, const void* k, const void* v, const void* out,
