@@ -130,16 +130,19 @@ def test_fp8_fused_against_oracle(B, S, H, N, causal, docs, scale):
 
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("blocks", [(128, 384), (192, 448)], ids=["first-half", "second-half"])
-def test_fp8_scores_jump_past_the_reference(causal, blocks):
-    """Blocks of keys whose scores rise by about 2^16 and 2^32 (as base-2
-    exponents) over the first key tile's: past the FP8 pass's 2^8 guard, so
-    the kernel must move its reference point (keeping every P inside E4M3's
-    range) instead of saturating."""
+@pytest.mark.parametrize("bumps", [(1.0, 2.0), (0.75, 0.875)], ids=["past-f16", "inside-f16"])
+def test_fp8_scores_jump_past_the_reference(causal, blocks, bumps):
+    """Blocks of keys whose scores rise by about 16 and 32 (or 12 and 14) as
+    base-2 exponents over the first key tile's: past the FP8 pass's 2^8
+    guard, so the kernel must move its reference point (keeping every P
+    inside E4M3's range) instead of saturating.  The fast pass exponentiates
+    in half precision: the larger jumps overflow it to +inf, the smaller ones
+    stay finite with a row sum above the guard; both must reach the redo."""
     B, S, H, d = 1, 768, 2, 128
     q, k, v = inputs.make_qkv(B, S, H, d, seed=72, dtype=torch.bfloat16)
     q = (q.float() * 0.25 + 1.0).to(torch.bfloat16)
     k = k.float() * 0.25
-    for a, bump in zip(blocks, (1.0, 2.0)):
+    for a, bump in zip(blocks, bumps):
         k[:, a:a + 32] += bump
     fp8 = pkg.fp8_quantize_qkv(q.to(DEV), k.to(torch.bfloat16).to(DEV), v.to(DEV))
     out, lse = pkg.ring_attn_fwd_fp8(fp8, 2, causal)
