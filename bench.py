@@ -281,8 +281,10 @@ def oracle_sample(w, get_head, docs, budget_s: float, rows_per_head: int, seed: 
         heads_done += 1
         if dt >= budget_s:
             break
-    desc = (f"{rows_per_head} seeded query rows x {heads_done} (b,h) heads of "
-            f"{w.name} ({w.describe()}), fp64 numpy oracle")
+    what = ("all query rows" if rows_per_head >= w.S else f"{rows_per_head} seeded query rows")
+    whole = " (the whole workload)" if rows_per_head >= w.S and heads_done == w.B * w.H else ""
+    desc = (f"{what} x {heads_done} (b,h) heads of {w.name} ({w.describe()}){whole}, "
+            f"fp64 numpy oracle")
     return flops, dt, desc
 
 
@@ -468,8 +470,10 @@ def run_ours(args, w, rank, world, local):
         def get_head(b, h):
             return tuple(t[b:b + 1, :, h:h + 1].float().numpy() for t in host_inputs)
 
-        f, dt, desc = oracle_sample(w, get_head, docs, budget_s=args.cpu_budget,
-                                    rows_per_head=args.cpu_rows)
+        rows = args.cpu_rows if args.cpu_rows is not None else (w.S if w.S <= 8192 else 512)
+        # the whole oracle on every head when the rows are all of them
+        budget = args.cpu_budget if rows < w.S else max(args.cpu_budget, 60.0)
+        f, dt, desc = oracle_sample(w, get_head, docs, budget_s=budget, rows_per_head=rows)
         cpu = {"value": f / dt / 1e12, "unit": UNIT, **core_record(), "kind": "oracle",
                "sample": desc, "seconds": dt,
                # the whole workload at the sample's rate (extrapolated, not run)
@@ -481,6 +485,9 @@ def run_ours(args, w, rank, world, local):
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": _config(w, docs, world),
         "frac_of_peak": value / world / peak_burst,
+        # each timed launch between its own events: the median and the spread
+        "ms_launch_median": statistics.median(per_launch_ms),
+        "ms_launch_min_max": [min(per_launch_ms), max(per_launch_ms)],
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
         "clocks": clk, "gates": gates,
         "effective_flops_per_step": flops * world,
@@ -918,7 +925,9 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
-    ap.add_argument("--cpu-rows", type=int, default=512)
+    ap.add_argument("--cpu-rows", type=int, default=None,
+                    help="query rows per head for the oracle timing (default: every row up "
+                         "to S = 8192, where the whole oracle fits the budget; 512 above)")
     ap.add_argument("--no-gates", action="store_true",
                     help="leave the schedule checks out of the default line")
     ap.add_argument("--hbm-kernels", action="store_true",
