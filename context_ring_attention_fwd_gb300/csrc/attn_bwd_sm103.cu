@@ -51,6 +51,12 @@
 #include "internal.h"
 #include "ptx.cuh"
 
+// Head-group size of the backward's deal: the smallest group of heads whose
+// items fill this many rounds of the grid (see launch_bwd_t).
+#ifndef CPRING_BWD_BALANCE
+#define CPRING_BWD_BALANCE 2
+#endif
+
 namespace cpring {
 namespace {
 
@@ -809,12 +815,13 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
   const int grid = static_cast<int>(std::min<long long>(items, sm_count()));
   // Head groups as in the forward: a launch with at least 16 rounds of the
   // grid and no document layout takes the smallest group whose items fill
-  // two rounds; otherwise one pool, so that the lightest items come last.
+  // CPRING_BWD_BALANCE rounds; otherwise one pool, so that the lightest
+  // items come last.
   {
     const int BH = a.B * a.H;
     long long hg = BH;
     if (a.doc_offsets == nullptr && items >= 16LL * grid) {
-      hg = (2LL * grid + p.n_tiles - 1) / p.n_tiles;
+      hg = (static_cast<long long>(CPRING_BWD_BALANCE) * grid + p.n_tiles - 1) / p.n_tiles;
       hg = std::max<long long>(1, std::min<long long>(hg, BH));
     }
     p.head_group = static_cast<int>(hg);

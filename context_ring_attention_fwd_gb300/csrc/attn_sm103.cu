@@ -110,7 +110,7 @@ constexpr float kRescaleLog2 = 8.0f;
 //                          E4M3 from half precision; row sums in half pairs
 //                          over 32 keys, then added into fp32.
 #ifndef CPRING_BALANCE
-#define CPRING_BALANCE 2
+#define CPRING_BALANCE 1
 #endif
 #ifndef CPRING_GROUP_MIN_ROUNDS
 #define CPRING_GROUP_MIN_ROUNDS 16
