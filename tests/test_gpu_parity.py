@@ -468,6 +468,30 @@ def test_host_entry_with_documents_and_without_mask_equals_fused():
             assert torch.equal(ho, fo.cpu()) and torch.equal(hl, fl.cpu()), (dt, causal, docs)
 
 
+@pytest.mark.parametrize("B,S,H,d,N,causal", [(1, 2048, 4, 128, 4, True), (2, 1280, 3, 128, 5, False),
+                                               (1, 1000, 2, 64, 4, True),
+                                               (1, 16384, 32, 128, 4, True)])  # grouped heads
+def test_claimed_items_equal_the_fixed_deal(B, S, H, d, N, causal):
+    """One document covering the whole sequence ([0, S]) sends the launch
+    down the claimed-items path (work queue, item ring, items published with
+    their Q loads, slots ranked by cost) with the arithmetic of the launch
+    without documents, which takes the fixed deal: the two must agree bit
+    for bit, whole-sequence and rank by rank, so no item is lost, repeated
+    or given the wrong rows by either deal."""
+    q, k, v = (t.to(DEV) for t in inputs.make_qkv(B, S, H, d, seed=S + N, dtype=torch.bfloat16))
+    fo, fl = pkg.ring_attn_fwd(q, k, v, N, causal, None)
+    co, cl = pkg.ring_attn_fwd(q, k, v, N, causal, [0, S])
+    assert pkg.cp_get_last_status() == 0
+    assert torch.equal(fo, co) and torch.equal(fl, cl)
+    docs_t = pkg.doc_offsets_tensor([0, S], DEV)
+    ro = torch.full_like(q, 7.0)
+    rl = torch.full((B, H, S), 7.0, dtype=torch.float32, device=DEV)
+    for i in range(N):
+        pkg.cp_ring_attn_fwd_rank(q, k, v, ro, rl, N, i, causal, docs_t)
+    assert pkg.cp_get_last_status() == 0
+    assert torch.equal(ro, fo) and torch.equal(rl, fl)
+
+
 def test_native_kernels_launch():
     before = pkg.launch_counts()
     q, k, v = (t.to(DEV) for t in inputs.make_qkv(1, 256, 1, 128, seed=1, dtype=torch.bfloat16))
