@@ -43,13 +43,23 @@ DEFAULT_WORKLOAD = "bf16_causal_128k"
 # workload named.  Each figure holds only for the kernel source it was taken
 # on: "sources" is the SHA-256 prefix of the forward kernel's source files
 # (KERNEL_SOURCES), and a line whose sources differ reports traffic null.
-NCU_TRAFFIC = {
-    # 15.624 GB read + 1.085 GB written (ncu, ring_attn_bf16_kernel<128, 0, 0>, 1 pass)
-    "bf16_causal_128k": {"bytes": 15.62352e9 + 1.084840704e9, "sources": "796d8eda62a368da"},
-}
 KERNEL_SOURCES = ("context_ring_attention_fwd_gb300/csrc/attn_sm103.cu",
                   "context_ring_attention_fwd_gb300/csrc/attn_common.cuh",
                   "context_ring_attention_fwd_gb300/csrc/ptx.cuh")
+BWD_KERNEL_SOURCES = ("context_ring_attention_fwd_gb300/csrc/attn_bwd_sm103.cu",
+                      "context_ring_attention_fwd_gb300/csrc/attn_common.cuh",
+                      "context_ring_attention_fwd_gb300/csrc/ptx.cuh")
+NCU_TRAFFIC = {
+    # 15.624 GB read + 1.085 GB written (ncu, ring_attn_bf16_kernel<128, 0, 0>, 1 pass)
+    "bf16_causal_128k": {"bytes": 15.62352e9 + 1.084840704e9, "sources": "796d8eda62a368da"},
+    # the FP8 forward (--fp8; ring_attn_fp8_kernel<128>: 2.141 GB read + 1.063 GB
+    # written) and the backward's dK/dV kernel (--bwd; ring_attn_bwd_kernel<128, 1>:
+    # 5.998 GB read + 2.124 GB written), same capture form
+    "fp8:bf16_causal_128k": {"bytes": 2.141138432e9 + 1.063419392e9,
+                             "sources": "796d8eda62a368da"},
+    "bwd:bf16_causal_128k": {"bytes": 5.998427392e9 + 2.124013312e9,
+                             "sources": "a3bf7d58f6868ad3", "files": BWD_KERNEL_SOURCES},
+}
 # tcgen05 dense bf16 -> fp32 rate per SM and clock: a 128x128x16 MMA
 # (524,288 FLOPs) every 64 clocks.
 TCGEN05_BF16_FLOP_PER_CLK_SM = 8192
@@ -67,11 +77,11 @@ def effective_flops(w, docs) -> int:
     return 4 * w.d * visible_pairs(w.S, w.causal, docs) * w.B * w.H
 
 
-def kernel_sources_digest() -> str:
-    """SHA-256 prefix over the forward kernel's source files."""
+def kernel_sources_digest(files=KERNEL_SOURCES) -> str:
+    """SHA-256 prefix over a kernel's source files (default: the forward's)."""
     import hashlib
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in files:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -81,7 +91,8 @@ def ncu_traffic(name: str):
     """The recorded DRAM traffic of the kernel for this workload, or None when
     it was not recorded for the kernel source as it stands."""
     rec = NCU_TRAFFIC.get(name)
-    if not rec or rec["bytes"] is None or rec["sources"] != kernel_sources_digest():
+    if (not rec or rec["bytes"] is None
+            or rec["sources"] != kernel_sources_digest(rec.get("files", KERNEL_SOURCES))):
         return None
     return rec["bytes"]
 
@@ -711,7 +722,12 @@ def run_fp8(args, w, local):
         "metric": METRIC, "impl": "fp8_e4m3", "unit": UNIT, "value": achieved,
         "ms_per_step": ms_8, "ms_quantize_qkv": ms_q, "ms_bf16_fused": ms_b,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": 2 * peak_burst,
-                     "unit": "TFLOP/s", "frac": achieved / (2 * peak_burst), "traffic": None,
+                     "unit": "TFLOP/s", "frac": achieved / (2 * peak_burst),
+                     "traffic": ncu_traffic("fp8:" + w.name),
+                     "traffic_sources": kernel_sources_digest(),
+                     # Q, K, V read once as E4M3; O (bf16) and LSE written once
+                     "algorithmic_bytes": 3 * w.B * w.S * w.H * w.d + 2 * w.B * w.S * w.H * w.d
+                     + 4 * w.B * w.H * w.S,
                      "peak_kind": f"{peak_src} bf16 dense burst (cuBLAS) x 2 (nominal FP8/bf16)"},
         "ring_send_plus_recv_bytes_fp8": int(sum(g8)),
         "ring_send_plus_recv_bytes_bf16": int(sum(g16)),
@@ -773,7 +789,11 @@ def run_bwd(args, w, local):
         "metric": "effective TFLOP/s of the ring-attention backward (1 GB300)", "impl": "bwd",
         "unit": UNIT, "value": achieved, "ms_per_step": ms, "higher_is_better": True,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_burst,
-                     "unit": "TFLOP/s", "frac": achieved / peak_burst, "traffic": None,
+                     "unit": "TFLOP/s", "frac": achieved / peak_burst,
+                     # DRAM bytes of one launch of the dominant kernel (dK/dV)
+                     "traffic": ncu_traffic("bwd:" + w.name),
+                     "traffic_kernel": "ring_attn_bwd_kernel<128, 1> (dK, dV)",
+                     "traffic_sources": kernel_sources_digest(BWD_KERNEL_SOURCES),
                      "peak_kind": f"{peak_src} bf16 dense burst (cuBLAS)",
                      "executed_tflops": achieved * 14 / 10},
         "gpu_launches": int(sum(launches1) - sum(launches0)),
