@@ -68,3 +68,24 @@ def test_reference_arm_line_under_two_ranks():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_recorded_traffic_holds_only_for_its_kernel_sources(monkeypatch):
+    """A recorded DRAM figure is reported only while the kernel sources it
+    was captured on are unchanged (their digest matches); any other digest,
+    or a workload with no record, gives None, so a stale figure never
+    reaches a bench line."""
+    for name, rec in bench.NCU_TRAFFIC.items():
+        files = rec.get("files", bench.KERNEL_SOURCES)
+        if rec["bytes"] is not None and rec["sources"] == bench.kernel_sources_digest(files):
+            assert bench.ncu_traffic(name) == rec["bytes"]
+        else:
+            assert bench.ncu_traffic(name) is None
+    assert bench.ncu_traffic("no_such_workload") is None
+    stale = {k: dict(v, sources="0000000000000000") for k, v in bench.NCU_TRAFFIC.items()}
+    monkeypatch.setattr(bench, "NCU_TRAFFIC", stale)
+    assert all(bench.ncu_traffic(k) is None for k in stale)
+    # the digest covers every listed file: changing one byte of any changes it
+    real = bench.kernel_sources_digest()
+    assert len(real) == 16 and real != bench.kernel_sources_digest(bench.BWD_KERNEL_SOURCES)
+
