@@ -57,8 +57,8 @@ NCU_TRAFFIC = {
     # 5.998 GB read + 2.124 GB written), same capture form
     "fp8:bf16_causal_128k": {"bytes": 2.141138432e9 + 1.063419392e9,
                              "sources": "796d8eda62a368da"},
-    "bwd:bf16_causal_128k": {"bytes": 5.998427392e9 + 2.124013312e9,
-                             "sources": "a3bf7d58f6868ad3", "files": BWD_KERNEL_SOURCES},
+    "bwd:bf16_causal_128k": {"bytes": 5.99819904e9 + 2.123562752e9,
+                             "sources": "cd6d651611556bb3", "files": BWD_KERNEL_SOURCES},
 }
 # tcgen05 dense bf16 -> fp32 rate per SM and clock: a 128x128x16 MMA
 # (524,288 FLOPs) every 64 clocks.

@@ -54,7 +54,7 @@
 // Head-group size of the backward's deal: the smallest group of heads whose
 // items fill this many rounds of the grid (see launch_bwd_t).
 #ifndef CPRING_BWD_BALANCE
-#define CPRING_BWD_BALANCE 2
+#define CPRING_BWD_BALANCE 1
 #endif
 
 namespace cpring {
