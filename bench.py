@@ -50,15 +50,15 @@ BWD_KERNEL_SOURCES = ("context_ring_attention_fwd_gb300/csrc/attn_bwd_sm103.cu",
                       "context_ring_attention_fwd_gb300/csrc/attn_common.cuh",
                       "context_ring_attention_fwd_gb300/csrc/ptx.cuh")
 NCU_TRAFFIC = {
-    # 15.624 GB read + 1.085 GB written (ncu, ring_attn_bf16_kernel<128, 0, 0>, 1 pass)
-    "bf16_causal_128k": {"bytes": 15.62352e9 + 1.084840704e9, "sources": "796d8eda62a368da"},
-    # the FP8 forward (--fp8; ring_attn_fp8_kernel<128>: 2.141 GB read + 1.063 GB
+    # 16.718 GB read + 1.084 GB written (ncu, ring_attn_bf16_kernel<128, 0, 0>, 1 pass)
+    "bf16_causal_128k": {"bytes": 16.71847808e9 + 1.084292352e9, "sources": "a2bf8212ad5f2d98"},
+    # the FP8 forward (--fp8; ring_attn_fp8_kernel<128>: 2.137 GB read + 1.063 GB
     # written) and the backward's dK/dV kernel (--bwd; ring_attn_bwd_kernel<128, 1>:
-    # 5.998 GB read + 2.124 GB written), same capture form
-    "fp8:bf16_causal_128k": {"bytes": 2.141138432e9 + 1.063419392e9,
-                             "sources": "796d8eda62a368da"},
-    "bwd:bf16_causal_128k": {"bytes": 5.99819904e9 + 2.123562752e9,
-                             "sources": "cd6d651611556bb3", "files": BWD_KERNEL_SOURCES},
+    # 5.995 GB read + 2.124 GB written), same capture form
+    "fp8:bf16_causal_128k": {"bytes": 2.136846848e9 + 1.063047936e9,
+                             "sources": "a2bf8212ad5f2d98"},
+    "bwd:bf16_causal_128k": {"bytes": 5.995067904e9 + 2.123589376e9,
+                             "sources": "22a468516fa74477", "files": BWD_KERNEL_SOURCES},
 }
 # tcgen05 dense bf16 -> fp32 rate per SM and clock: a 128x128x16 MMA
 # (524,288 FLOPs) every 64 clocks.

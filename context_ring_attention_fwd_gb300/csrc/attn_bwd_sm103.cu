@@ -767,11 +767,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
   static_assert(Lay::kAlloc <= 232448, "shared memory budget");
   static_assert(Lay::kX0Slots <= 3 && Lay::kX1Slots == 2, "barrier slots");
   auto kern = ring_attn_bwd_kernel<D, kDKDV>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kAlloc);
-  });
+  const cudaError_t attr_err = ensure_smem_limit(reinterpret_cast<const void*>(kern), Lay::kAlloc);
   if (attr_err != cudaSuccess) return attr_err;
   // kDQ: fixed (Q, dO), streamed (K, V); kDKDV: fixed (K, V), streamed (Q, dO)
   const void* f0 = kDKDV ? a.k : a.q;

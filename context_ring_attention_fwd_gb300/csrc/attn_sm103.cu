@@ -1621,11 +1621,7 @@ cudaError_t launch_t(const AttnArgs& a, cudaStream_t stream) {
     kern = ring_attn_fp8_kernel<D>;
   else
     kern = ring_attn_bf16_kernel<D, kPartial, kDynamic>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kAlloc);
-  });
+  const cudaError_t attr_err = ensure_smem_limit(reinterpret_cast<const void*>(kern), Lay::kAlloc);
   if (attr_err != cudaSuccess) return attr_err;
 
   CUtensorMap mq, mk, mv;

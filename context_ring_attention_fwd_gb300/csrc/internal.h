@@ -170,6 +170,10 @@ void count_launch(int which);
 
 // Multiprocessor count of the current device (cached per device).
 int sm_count();
+// Raises `kern`'s dynamic shared-memory limit to `bytes` on the current
+// device: once per (kernel, device) for the process's life, under a lock,
+// with the first call's result returned to every later one.
+cudaError_t ensure_smem_limit(const void* kern, int bytes);
 // Compute capability major*10+minor of the current device (cached).
 int device_cc();
 

@@ -20,6 +20,7 @@
 #include <atomic>
 #include <cmath>
 #include <mutex>
+#include <vector>
 
 #include "internal.h"
 
@@ -249,6 +250,25 @@ int* device_error_word() {
     addr[dev] = static_cast<int*>(p);
   }
   return addr[dev];
+}
+
+cudaError_t ensure_smem_limit(const void* kern, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  struct Done {
+    const void* kern;
+    int dev;
+    cudaError_t err;
+  };
+  static std::mutex mu;
+  static std::vector<Done> done;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Done& d : done)
+    if (d.kern == kern && d.dev == dev) return d.err;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  done.push_back(Done{kern, dev, e});
+  return e;
 }
 
 int sm_count() {
