@@ -115,7 +115,9 @@ constexpr int kTTokens = 128;  // tokens per transposed tile (one 128-byte outpu
 
 // Block (x, h, b) covers tokens [s0, s0 + 128) of head h, s0 = 128 x.
 // Phase 1: the block reads the 128 token rows of d bf16 (coalesced 16-byte
-// loads), quantizes them and stores the codes row-major in shared memory,
+// loads, all of a thread's loads issued before the first is used, so that
+// enough bytes are in flight to cover the memory latency), quantizes them
+// and stores the codes row-major in shared memory,
 // 128 bytes per token row, word w of token r at word w ^ (4 (r / 16)) of its
 // row.  Phase 2: thread (d4, g) gathers words d4 (four consecutive channels)
 // of tokens 16 g .. 16 g + 15, transposes the 4 x 16 bytes in registers and
@@ -124,24 +126,35 @@ constexpr int kTTokens = 128;  // tokens per transposed tile (one 128-byte outpu
 // one full 128-byte segment of a row; the swizzle makes both phases' shared
 // accesses conflict-free.  S % 16 == 0, so a 16-token segment is either
 // wholly inside [0, S) or wholly past it.
+template <int D>
 __global__ void __launch_bounds__(kThreads)
     fp8_quant_t_kernel(const uint4* __restrict__ x, uint8_t* __restrict__ y,
-                       const float* __restrict__ amax, int S, int H, int d) {
+                       const float* __restrict__ amax, int S, int H) {
   __shared__ __align__(16) uint32_t tile[kTTokens * 32];  // 128 rows x 128 bytes
+  constexpr int g8 = D / 8;                         // 16-byte input vectors per token row
+  constexpr int kVecs = kTTokens * g8 / kThreads;   // of them per thread: 8 (d = 128), 4 (64)
+  static_assert(kVecs * kThreads == kTTokens * g8, "whole vectors per thread");
   const int h = blockIdx.y, b = blockIdx.z;
   const int s0 = blockIdx.x * kTTokens;
-  const int g8 = d / 8;   // 16-byte input vectors per token row of one head
+  uint4 v[kVecs];
+#pragma unroll
+  for (int i = 0; i < kVecs; ++i) {
+    const int idx = threadIdx.x + i * kThreads;
+    const int r = idx / g8, cv = idx % g8;
+    v[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (s0 + r < S) v[i] = x[((static_cast<long long>(b) * S + s0 + r) * H + h) * g8 + cv];
+  }
   const float inv = inv_scale(amax[b * H + h]);
-  for (int idx = threadIdx.x; idx < kTTokens * g8; idx += kThreads) {
-    const int r = idx / g8, cv = idx - (idx / g8) * g8;
-    uint2 q = make_uint2(0u, 0u);
-    if (s0 + r < S)
-      q = quant8(x[((static_cast<long long>(b) * S + s0 + r) * H + h) * g8 + cv], inv);
+#pragma unroll
+  for (int i = 0; i < kVecs; ++i) {
+    const int idx = threadIdx.x + i * kThreads;
+    const int r = idx / g8, cv = idx % g8;
+    const uint2 q = (s0 + r < S) ? quant8(v[i], inv) : make_uint2(0u, 0u);
     const int w = (2 * cv) ^ (4 * (r >> 4));  // words 2 cv, 2 cv + 1 stay adjacent
     *reinterpret_cast<uint2*>(tile + r * 32 + w) = q;
   }
   __syncthreads();
-  const int n_d4 = d / 4;
+  constexpr int n_d4 = D / 4;
   for (int idx = threadIdx.x; idx < n_d4 * 8; idx += kThreads) {
     const int g = idx & 7, d4 = idx >> 3;
     const int s = s0 + 16 * g;
@@ -159,7 +172,7 @@ __global__ void __launch_bounds__(kThreads)
         const uint32_t hi = __byte_perm(wv[4 * q4 + 2], wv[4 * q4 + 3], 0x0040 | (c << 4) | c) & 0xffffu;
         o[q4] = lo | (hi << 16);
       }
-      *reinterpret_cast<uint4*>(y + ((static_cast<long long>(b) * H + h) * d + 4 * d4 + c) * S + s) =
+      *reinterpret_cast<uint4*>(y + ((static_cast<long long>(b) * H + h) * D + 4 * d4 + c) * S + s) =
           make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
@@ -198,8 +211,12 @@ extern "C" cp_status cp_fp8_quantize(const void* x, void* x8, float* descale, in
                                                       reinterpret_cast<unsigned*>(descale), S, H, d);
   if (transpose) {
     const dim3 grid_t((S + kTTokens - 1) / kTTokens, H, B);
-    fp8_quant_t_kernel<<<grid_t, kThreads, 0, stream>>>(static_cast<const uint4*>(x),
-                                                        static_cast<uint8_t*>(x8), descale, S, H, d);
+    if (d == 128)
+      fp8_quant_t_kernel<128><<<grid_t, kThreads, 0, stream>>>(
+          static_cast<const uint4*>(x), static_cast<uint8_t*>(x8), descale, S, H);
+    else
+      fp8_quant_t_kernel<64><<<grid_t, kThreads, 0, stream>>>(
+          static_cast<const uint4*>(x), static_cast<uint8_t*>(x8), descale, S, H);
   } else {
     fp8_quant_kernel<<<grid_rows, kThreads, 0, stream>>>(static_cast<const uint4*>(x),
                                                          static_cast<uint2*>(x8), descale, S, H, d);
