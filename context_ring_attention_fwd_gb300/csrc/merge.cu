@@ -271,29 +271,36 @@ cudaError_t ensure_smem_limit(const void* kern, int bytes) {
   return e;
 }
 
+// The two device attributes below are cached per device in atomics: host
+// threads calling at once may both query the device, and store the same
+// value.
 int sm_count() {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-  if (cache[dev] == 0) {
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
     int n = 0;
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cache[dev] = n > 0 ? n : 1;
+    v = n > 0 ? n : 1;
+    cache[dev].store(v, std::memory_order_relaxed);
   }
-  return cache[dev];
+  return v;
 }
 
 int device_cc() {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cache[dev] == 0) {
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
     int ma = 0, mi = 0;
     cudaDeviceGetAttribute(&ma, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&mi, cudaDevAttrComputeCapabilityMinor, dev);
-    cache[dev] = ma * 10 + mi;
+    v = ma * 10 + mi;
+    cache[dev].store(v, std::memory_order_relaxed);
   }
-  return cache[dev];
+  return v;
 }
 
 cudaError_t launch_doc_scan(const int32_t* doc_offsets, int S, int32_t* doc_info,
